@@ -1,0 +1,120 @@
+/*
+ * flce.h — fused LM-head projection + cross-entropy on GB300 (sm_103a).
+ *
+ * The operation is the last step of a language-model training step, as written
+ * out in "What-Each-Parallelism-Actually-Shards" §1.4: hidden states X[N,H]
+ * (N = B*S tokens) are projected by the LM head W[V,H] to logits
+ * z[N,V] = X W^T, and the loss is the cross-entropy of those logits against
+ * integer labels, with rows whose label equals ignore_index left out (the fused
+ * call in §7.4 passes ignore_index = -100).  §7.4 describes the fused form this
+ * library implements: keep a running log-sum-exp over the vocabulary, take only
+ * the target token's logit, recompute logits in the backward pass, and never
+ * write the [N,V] logits to global memory.
+ *
+ * Definitions (i = row, j = vocabulary id, y_i = label):
+ *   lse_i  = log sum_j exp(z_ij)
+ *   loss_i = (lse_i - z_{i,y_i}) * valid_i,   valid_i = [y_i != ignore_index]
+ *   loss   = sum_i loss_i / n_valid  (FLCE_REDUCTION_MEAN; 0 when n_valid = 0)
+ *          = sum_i loss_i            (FLCE_REDUCTION_SUM)
+ *   G_ij   = s * (exp(z_ij - lse_i) - [j = y_i]) * valid_i,
+ *            s = g / n_valid (mean) or g (sum), g = upstream gradient of loss
+ *   dX = G W   (bf16 [N,H]),   dW = G^T X   (bf16 [V,H])
+ *
+ * Conventions for every call:
+ *   - X, W, dX, dW are bf16, dense row-major, H contiguous.  labels is int32.
+ *     loss, lse, grad_loss are fp32.  All data pointers are DEVICE pointers
+ *     owned by the caller; the library never allocates or frees memory.
+ *   - ws / ws_bytes: caller-owned device workspace of at least
+ *     flce_workspace_bytes(p) bytes, 256-byte aligned.  It is the only extra
+ *     device memory the library touches.  Its size grows with N and H but not
+ *     with V.  Calls that share a workspace must be ordered on one stream.
+ *   - Requirements: n >= 1, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
+ *     the tensor-memory-access engine), X / W / dX / dW 16-byte aligned,
+ *     labels / lse 4-byte aligned.  Violations return an error and launch
+ *     nothing.
+ *   - stream: a cudaStream_t (NULL = legacy default stream).  Every call is
+ *     asynchronous on it.  Host-detectable errors return immediately.
+ *     Errors found on the device (a label outside [0,V) that is not
+ *     ignore_index; a bounded wait inside a kernel that ran out) are recorded
+ *     in the workspace's status word; read them with flce_read_device_status.
+ *     After any error the outputs are unspecified.
+ *   - Thread safety: calls on different workspaces may run concurrently.
+ */
+#ifndef FLCE_H
+#define FLCE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;                       /* same type as cudaStream_t's target */
+typedef struct CUstream_st* flce_stream_t;
+
+typedef enum {
+  FLCE_OK = 0,
+  FLCE_ERR_INVALID_ARGUMENT = 1,    /* null pointer, bad enum, n/h/v < 1 */
+  FLCE_ERR_UNSUPPORTED_SHAPE = 2,   /* h % 8 != 0, h < 8, or sizes beyond int32 tile coordinates */
+  FLCE_ERR_MISALIGNED = 3,          /* a pointer breaks the alignment rules above */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < flce_workspace_bytes(p) */
+  FLCE_ERR_LABEL_OUT_OF_RANGE = 5,  /* device: some label not in [0,V) and not ignore_index */
+  FLCE_ERR_TIMEOUT = 6,             /* device: a bounded pipeline wait gave up (no hang, no trap) */
+  FLCE_ERR_CUDA = 7,                /* a CUDA runtime/driver call failed, or no sm_100-family GPU */
+  FLCE_ERR_NO_DEVICE_STATUS = 8     /* flce_read_device_status could not read the word */
+} flce_status_t;
+
+typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction_t;
+
+typedef struct {
+  int64_t n;             /* rows (tokens), N = B*S */
+  int64_t h;             /* hidden size */
+  int64_t v;             /* vocabulary size */
+  int32_t ignore_index;  /* label value that marks a row as ignored (commonly -100) */
+  int32_t reduction;     /* flce_reduction_t */
+} flce_problem_t;
+
+/* Workspace size in bytes for every call below on problem p (0 if p is invalid).
+ * Holds the device status word, per-row partial (max, sum) pairs, target
+ * logits, one vocabulary chunk of bf16 G (N x C, C a fixed chunk width) and an
+ * fp32 accumulator for dX (N x H).  Independent of V. */
+size_t flce_workspace_bytes(const flce_problem_t* p);
+
+/* Forward ("What-Each-Parallelism-Actually-Shards" §7.4: online log-sum-exp over
+ * vocabulary tiles, target logit only).  Writes *loss (device fp32 scalar) and
+ * lse[N] (fp32).  Reads X, W, labels.  Never stores logits. */
+flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W,
+                           const int32_t* labels, float* loss, float* lse,
+                           void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* Backward (§7.4: recompute logits instead of saving them).  Given lse from
+ * flce_forward on the same X, W, labels, writes dX [N,H] and dW [V,H] (bf16,
+ * fp32 accumulation).  grad_loss: device fp32 scalar g, or NULL for g = 1. */
+flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* W,
+                            const int32_t* labels, const float* lse, const float* grad_loss,
+                            void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* Forward then backward with g = 1: loss, lse, dX, dW in one call. */
+flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W,
+                           const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
+                           void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* Synchronises `stream`, then returns the status word recorded in ws by the
+ * kernels of earlier calls (FLCE_OK if none) and clears it. */
+flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);
+
+/* Launches one kernel whose pipeline wait is on a barrier that nothing
+ * completes, with the given limit in nanoseconds; the wait gives up, records
+ * FLCE_ERR_TIMEOUT in ws and the kernel returns.  Exercises the error path of
+ * the bounded waits used by every kernel. */
+flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream);
+
+/* Static description of a status code. */
+const char* flce_status_string(flce_status_t s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FLCE_H */

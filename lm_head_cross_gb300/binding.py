@@ -1,0 +1,245 @@
+"""ctypes binding over ``libflce.so`` (C-ABI declared in ``include/flce.h``).
+
+Argument marshalling only: shapes, dtypes and device pointers are checked and
+passed through; every step of the computation runs in the library's kernels.
+PyTorch is used for device memory and the current stream.  There is no CPU
+fallback: if the library is missing or fails to load, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB = None
+
+FLCE_OK = 0
+FLCE_ERR_LABEL_OUT_OF_RANGE = 5
+FLCE_ERR_TIMEOUT = 6
+REDUCTIONS = {"mean": 0, "sum": 1}
+
+EXPORTED = ("flce_workspace_bytes", "flce_forward", "flce_backward", "flce_fwd_bwd",
+            "flce_read_device_status", "flce_selftest_timeout", "flce_status_string")
+
+
+class FlceError(RuntimeError):
+    def __init__(self, code: int, where: str = ""):
+        self.code = int(code)
+        msg = status_string(code) if _LIB is not None else f"status {code}"
+        super().__init__(f"{where}: {msg} (status {code})" if where else f"{msg} (status {code})")
+
+
+class Problem(ctypes.Structure):
+    _fields_ = [("n", ctypes.c_int64), ("h", ctypes.c_int64), ("v", ctypes.c_int64),
+                ("ignore_index", ctypes.c_int32), ("reduction", ctypes.c_int32)]
+
+
+def lib_path() -> str:
+    return os.environ.get("FLCE_LIB", os.path.join(HERE, "libflce.so"))
+
+
+def lib():
+    """Load the C-ABI library (once).  Raises if it is not built."""
+    global _LIB
+    if _LIB is not None:
+        return _LIB
+    path = lib_path()
+    if not os.path.exists(path):
+        raise FlceError(-1, f"{path} is not built; run __graft_entry__.build() or "
+                            "python -m lm_head_cross_gb300.build")
+    L = ctypes.CDLL(path)
+    vp, sz = ctypes.c_void_p, ctypes.c_size_t
+    P = ctypes.POINTER(Problem)
+    L.flce_workspace_bytes.argtypes = [P]
+    L.flce_workspace_bytes.restype = sz
+    L.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_forward.restype = ctypes.c_int
+    L.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_backward.restype = ctypes.c_int
+    L.flce_fwd_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_fwd_bwd.restype = ctypes.c_int
+    L.flce_read_device_status.argtypes = [vp, vp]
+    L.flce_read_device_status.restype = ctypes.c_int
+    L.flce_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
+    L.flce_selftest_timeout.restype = ctypes.c_int
+    L.flce_status_string.argtypes = [ctypes.c_int]
+    L.flce_status_string.restype = ctypes.c_char_p
+    _LIB = L
+    return L
+
+
+def status_string(code: int) -> str:
+    return lib().flce_status_string(int(code)).decode()
+
+
+def logits_footprint_bytes(n_rows: int, v: int, elem_bytes: int) -> int:
+    """Bytes of a materialised [N, V] logits tensor (what the fused path never allocates)."""
+    return int(n_rows) * int(v) * int(elem_bytes)
+
+
+def _problem(n, h, v, ignore_index, reduction) -> Problem:
+    if reduction not in REDUCTIONS:
+        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
+    return Problem(int(n), int(h), int(v), int(ignore_index), REDUCTIONS[reduction])
+
+
+def workspace_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
+    p = _problem(n, h, v, ignore_index, reduction)
+    return int(lib().flce_workspace_bytes(ctypes.byref(p)))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _stream_ptr(stream):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check_inputs(x, w, labels):
+    torch = _torch()
+    if x.dim() != 2 or w.dim() != 2 or labels.dim() != 1:
+        raise ValueError("x must be [N, H], w [V, H], labels [N]")
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16:
+        raise TypeError("x and w must be bfloat16")
+    if labels.dtype != torch.int32:
+        raise TypeError("labels must be int32")
+    if not (x.is_cuda and w.is_cuda and labels.is_cuda):
+        raise ValueError("x, w and labels must be CUDA tensors")
+    if not (x.is_contiguous() and w.is_contiguous() and labels.is_contiguous()):
+        raise ValueError("x, w and labels must be contiguous")
+    if x.shape[1] != w.shape[1] or labels.shape[0] != x.shape[0]:
+        raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}, labels {tuple(labels.shape)}")
+
+
+def _alloc_ws(n, h, v, ignore_index, reduction, device):
+    torch = _torch()
+    nbytes = workspace_bytes(n, h, v, ignore_index, reduction)
+    if nbytes == 0:
+        raise FlceError(1, "workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def _call(name, code):
+    if code != FLCE_OK:
+        raise FlceError(code, name)
+
+
+def forward(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, check=False):
+    """Returns (loss [1] fp32, lse [N] fp32, ws)."""
+    torch = _torch()
+    _check_inputs(x, w, labels)
+    n, h = x.shape
+    v = w.shape[0]
+    p = _problem(n, h, v, ignore_index, reduction)
+    if ws is None:
+        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
+    loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    lse = torch.empty(n, dtype=torch.float32, device=x.device)
+    s = _stream_ptr(stream)
+    _call("flce_forward", lib().flce_forward(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
+                                             loss.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), s))
+    if check:
+        _call("device", read_device_status(ws, stream))
+    return loss, lse, ws
+
+
+def backward(x, w, labels, lse, grad_loss=None, ignore_index=-100, reduction="mean", ws=None, stream=None,
+             check=False):
+    """Returns (dX [N,H] bf16, dW [V,H] bf16, ws).  grad_loss: None or a 1-element fp32 CUDA tensor."""
+    torch = _torch()
+    _check_inputs(x, w, labels)
+    n, h = x.shape
+    v = w.shape[0]
+    if lse.dtype != torch.float32 or lse.shape != (n,) or not lse.is_contiguous():
+        raise ValueError("lse must be contiguous fp32 [N]")
+    if grad_loss is not None and (grad_loss.dtype != torch.float32 or grad_loss.numel() != 1 or not grad_loss.is_cuda):
+        raise ValueError("grad_loss must be a one-element fp32 CUDA tensor")
+    p = _problem(n, h, v, ignore_index, reduction)
+    if ws is None:
+        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
+    dX = torch.empty_like(x)
+    dW = torch.empty_like(w)
+    s = _stream_ptr(stream)
+    g = None if grad_loss is None else grad_loss.data_ptr()
+    _call("flce_backward", lib().flce_backward(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
+                                               lse.data_ptr(), g, dX.data_ptr(), dW.data_ptr(), ws.data_ptr(),
+                                               ws.numel(), s))
+    if check:
+        _call("device", read_device_status(ws, stream))
+    return dX, dW, ws
+
+
+def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, out=None, check=False):
+    """Returns (loss, lse, dX, dW, ws).  ``out`` may pass preallocated (loss, lse, dX, dW)."""
+    torch = _torch()
+    _check_inputs(x, w, labels)
+    n, h = x.shape
+    v = w.shape[0]
+    p = _problem(n, h, v, ignore_index, reduction)
+    if ws is None:
+        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
+    if out is None:
+        out = (torch.empty(1, dtype=torch.float32, device=x.device), torch.empty(n, dtype=torch.float32, device=x.device),
+               torch.empty_like(x), torch.empty_like(w))
+    loss, lse, dX, dW = out
+    s = _stream_ptr(stream)
+    _call("flce_fwd_bwd", lib().flce_fwd_bwd(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
+                                             loss.data_ptr(), lse.data_ptr(), dX.data_ptr(), dW.data_ptr(),
+                                             ws.data_ptr(), ws.numel(), s))
+    if check:
+        _call("device", read_device_status(ws, stream))
+    return loss, lse, dX, dW, ws
+
+
+def read_device_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns (and clears) the workspace's status word."""
+    return int(lib().flce_read_device_status(ctypes.c_void_p(ws.data_ptr()), _stream_ptr(stream)))
+
+
+class _LinearCrossEntropy:
+    """torch.autograd.Function wrapper, built lazily so importing needs no torch."""
+    fn = None
+
+    @classmethod
+    def get(cls):
+        if cls.fn is None:
+            torch = _torch()
+
+            class Fn(torch.autograd.Function):
+                @staticmethod
+                def forward(ctx, x2, w, labels, ignore_index, reduction):
+                    loss, lse, ws = forward(x2, w, labels, ignore_index, reduction)
+                    ctx.save_for_backward(x2, w, labels, lse)
+                    ctx.ignore_index = ignore_index
+                    ctx.reduction = reduction
+                    ctx.ws = ws
+                    return loss.reshape(())
+
+                @staticmethod
+                def backward(ctx, grad):
+                    x2, w, labels, lse = ctx.saved_tensors
+                    g = grad.detach().to(torch.float32).reshape(1).contiguous()
+                    dX, dW, _ = backward(x2, w, labels, lse, g, ctx.ignore_index, ctx.reduction, ws=ctx.ws)
+                    ctx.ws = None
+                    return dX, dW, None, None, None
+
+            cls.fn = Fn
+        return cls.fn
+
+
+def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str = "mean"):
+    """Cross-entropy of ``x @ w.T`` against ``labels`` without materialising the logits.
+
+    x: [..., H] bf16 CUDA, w: [V, H] bf16, labels: [...] integer (same leading
+    shape as x).  Returns a scalar fp32 loss with autograd to x and w.
+    """
+    torch = _torch()
+    h = x.shape[-1]
+    x2 = x.reshape(-1, h).contiguous()
+    lab = labels.reshape(-1).to(torch.int32).contiguous()
+    loss = _LinearCrossEntropy.get().apply(x2, w.contiguous(), lab, int(ignore_index), reduction)
+    return loss

@@ -1,0 +1,397 @@
+// C-ABI entry points declared in include/flce.h: argument validation, the
+// workspace layout, TMA tensor maps, and the order of kernel launches.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <cstdlib>
+#include <mutex>
+
+#include "../../include/flce.h"
+#include "flce_internal.h"
+
+namespace flce {
+namespace {
+
+constexpr size_t kAlign = 256;
+constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s; a healthy wait lasts microseconds
+
+size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+// Workspace layout (byte offsets from ws, each 256-byte aligned).
+struct Layout {
+  size_t status, n_valid, scale;  // header words
+  size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
+  size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
+  size_t g;                       // backward: one vocabulary chunk of G, bf16 [N, chunk]
+  size_t dx_acc;                  // backward: fp32 dX accumulator [N, H]
+  size_t total;
+  int nblk, chunk;
+};
+
+Layout make_layout(const flce_problem_t& p) {
+  Layout L{};
+  const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h);
+  L.nblk = static_cast<int>((p.n + kFinalizeThreads - 1) / kFinalizeThreads);
+  L.chunk = chunk_width(p.n);
+  size_t off = 0;
+  L.status = off;
+  L.n_valid = off + 4;
+  L.scale = off + 8;
+  off += kAlign;
+  L.blk_loss = off;
+  off = align_up(off + sizeof(double) * L.nblk);
+  L.blk_valid = off;
+  off = align_up(off + sizeof(int) * L.nblk);
+  L.part_m = off;
+  off = align_up(off + sizeof(float) * kMaxSplit * n);
+  L.part_l = off;
+  off = align_up(off + sizeof(float) * kMaxSplit * n);
+  L.tgt = off;
+  off = align_up(off + sizeof(float) * n);
+  L.g = off;
+  off = align_up(off + 2 * n * static_cast<size_t>(L.chunk));
+  L.dx_acc = off;
+  off = align_up(off + 4 * n * h);
+  L.total = off;
+  return L;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+// 2-D row-major tensor [outer, inner] with row pitch `pitch_bytes`, box
+// {box_inner, box_outer}, 128-byte swizzle, zero fill outside the tensor.
+bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t inner, uint64_t outer,
+              uint64_t pitch_bytes, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+uint64_t timeout_ns() {
+  static uint64_t t = [] {
+    const char* e = std::getenv("FLCE_TIMEOUT_NS");
+    if (e && *e) {
+      const unsigned long long v = std::strtoull(e, nullptr, 10);
+      if (v > 0) return static_cast<uint64_t>(v);
+    }
+    return kDefaultTimeoutNs;
+  }();
+  return t;
+}
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+flce_status_t check_problem(const flce_problem_t* p) {
+  if (!p) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->n < 1 || p->h < 1 || p->v < 1) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->h < 8 || p->h % 8 != 0) return FLCE_ERR_UNSUPPORTED_SHAPE;
+  // TMA coordinates and the kernels' tile indices are 32-bit.
+  if (p->n > (int64_t{1} << 30) || p->v > (int64_t{1} << 30) || p->h > (int64_t{1} << 20))
+    return FLCE_ERR_UNSUPPORTED_SHAPE;
+  return FLCE_OK;
+}
+
+struct Device {
+  int sms = 0;
+  bool ok = false;
+};
+
+flce_status_t device_info(Device* d) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (major != 10) return FLCE_ERR_CUDA;  // the binary carries sm_103a code only
+  if (cudaDeviceGetAttribute(&d->sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return FLCE_ERR_CUDA;
+  d->ok = true;
+  return FLCE_OK;
+}
+
+// Forward split count: the number of vocabulary ranges each row tile is cut
+// into.  Picks the count (4..32, at most the number of vocabulary tiles) whose
+// round-robin assignment of (row tile, range) units to `grid` CTAs gives the
+// smallest largest per-CTA tile count; a wave then holds about grid/vsplit row
+// tiles, which keeps the X panels it reads resident in L2.
+int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid) {
+  const int lo = std::min(4, vocab_tiles);
+  const int hi = std::min(kMaxSplit, vocab_tiles);
+  int best = lo;
+  long long best_cost = -1;
+  for (int vs = lo; vs <= hi; ++vs) {
+    const long long units = static_cast<long long>(row_tiles) * vs;
+    const int g = static_cast<int>(std::min<long long>(grid, units));
+    // per CTA b: units b, b+g, ...; unit u has split u % vs
+    long long worst = 0;
+    for (int b = 0; b < g; ++b) {
+      long long tiles = 0;
+      for (long long u = b; u < units; u += g) {
+        const int sp = static_cast<int>(u % vs);
+        tiles += (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
+      }
+      worst = std::max(worst, tiles);
+    }
+    if (best_cost < 0 || worst < best_cost) {
+      best_cost = worst;
+      best = vs;
+    }
+  }
+  return best;
+}
+
+int choose_vsplit(int row_tiles, int vocab_tiles, int grid) {
+  static std::mutex mu;
+  static int key[3] = {-1, -1, -1};
+  static int val = 1;
+  std::lock_guard<std::mutex> lock(mu);
+  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid) {
+    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid);
+    key[0] = row_tiles;
+    key[1] = vocab_tiles;
+    key[2] = grid;
+  }
+  return val;
+}
+
+struct Ctx {
+  const flce_problem_t* p;
+  Layout L;
+  uint8_t* ws;
+  cudaStream_t stream;
+  Device dev;
+  int* status() const { return reinterpret_cast<int*>(ws + L.status); }
+  int* n_valid() const { return reinterpret_cast<int*>(ws + L.n_valid); }
+  float* scale() const { return reinterpret_cast<float*>(ws + L.scale); }
+  double* blk_loss() const { return reinterpret_cast<double*>(ws + L.blk_loss); }
+  int* blk_valid() const { return reinterpret_cast<int*>(ws + L.blk_valid); }
+  float* part_m() const { return reinterpret_cast<float*>(ws + L.part_m); }
+  float* part_l() const { return reinterpret_cast<float*>(ws + L.part_l); }
+  float* tgt() const { return reinterpret_cast<float*>(ws + L.tgt); }
+  void* g() const { return ws + L.g; }
+  float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
+};
+
+flce_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
+
+flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  c->p = p;
+  c->L = make_layout(*p);
+  if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  c->ws = static_cast<uint8_t*>(ws);
+  c->stream = reinterpret_cast<cudaStream_t>(stream);
+  st = device_info(&c->dev);
+  if (st != FLCE_OK) return st;
+  if (!encode_fn()) return FLCE_ERR_CUDA;
+  // the status word starts every call cleared
+  return cuda_status(cudaMemsetAsync(c->status(), 0, sizeof(int), c->stream));
+}
+
+flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
+                          const float* grad_loss) {
+  const flce_problem_t& p = *c.p;
+  TcMaps maps;
+  if (!make_map(&maps.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
+  if (!make_map(&maps.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  maps.out = maps.a2 = maps.b2 = maps.out2 = maps.a;  // unused in this mode
+
+  TcParams tp{};
+  tp.n = static_cast<int>(p.n);
+  tp.h = static_cast<int>(p.h);
+  tp.v = static_cast<int>(p.v);
+  tp.ignore_index = p.ignore_index;
+  tp.timeout_ns = timeout_ns();
+  tp.status = c.status();
+  tp.row_tiles = static_cast<int>((p.n + kBM - 1) / kBM);
+  tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms);
+  tp.part_m = c.part_m();
+  tp.part_l = c.part_l();
+  tp.tgt = c.tgt();
+  tp.labels = labels;
+  const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
+  const int grid = static_cast<int>(std::min<long long>(c.dev.sms, units));
+  flce_status_t st = cuda_status(launch_tc(kModeForward, maps, tp, grid, c.stream));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(launch_fwd_finalize(tp.n, tp.v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels,
+                                       lse, c.blk_loss(), c.blk_valid(), c.status(), c.stream));
+  if (st != FLCE_OK) return st;
+  return cuda_status(launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, grad_loss, loss,
+                                         c.n_valid(), c.scale(), c.stream));
+}
+
+// Backward given lse and the scale already in the workspace.
+flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int32_t* labels, const float* lse,
+                           void* dX, void* dW) {
+  const flce_problem_t& p = *c.p;
+  const int chunk = c.L.chunk;
+  TcParams tp{};
+  tp.n = static_cast<int>(p.n);
+  tp.h = static_cast<int>(p.h);
+  tp.v = static_cast<int>(p.v);
+  tp.ignore_index = p.ignore_index;
+  tp.timeout_ns = timeout_ns();
+  tp.status = c.status();
+  tp.labels = labels;
+  tp.lse = lse;
+  tp.scale = c.scale();
+  tp.row_tiles = static_cast<int>((p.n + kBM - 1) / kBM);
+  tp.h_tiles = static_cast<int>((p.h + kBN - 1) / kBN);
+
+  TcMaps gm;  // grad: X, W K-major; G store
+  if (!make_map(&gm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
+  if (!make_map(&gm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  TcMaps bm;  // bwd: W MN-major (dX B operand), X MN-major (dW B operand), dX fp32 acc, dW store
+  if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.out, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.n, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.out2, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
+
+  for (int64_t c0 = 0; c0 < p.v; c0 += chunk) {
+    const int cw = static_cast<int>(std::min<int64_t>(chunk, p.v - c0));
+    tp.c0 = static_cast<int>(c0);
+    tp.cw = cw;
+    // G for this chunk: [N, cw] bf16 with row pitch `chunk`
+    if (!make_map(&gm.out, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, 64, 32))
+      return FLCE_ERR_CUDA;
+    gm.a2 = gm.b2 = gm.out2 = gm.a;  // unused in this mode
+    tp.grad_n_tiles = (cw + kBN - 1) / kBN;
+    const long long gtiles = static_cast<long long>(tp.row_tiles) * tp.grad_n_tiles;
+    flce_status_t st = cuda_status(
+        launch_tc(kModeGrad, gm, tp, static_cast<int>(std::min<long long>(c.dev.sms, gtiles)), c.stream));
+    if (st != FLCE_OK) return st;
+
+    if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, kBK, kBM))
+      return FLCE_ERR_CUDA;
+    if (!make_map(&bm.a2, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, 64, kBK))
+      return FLCE_ERR_CUDA;
+    tp.dw_m_tiles = (cw + kBM - 1) / kBM;
+    tp.dw_tiles = tp.dw_m_tiles * tp.h_tiles;
+    tp.dx_tiles = tp.row_tiles * tp.h_tiles;
+    tp.dx_accumulate = c0 > 0 ? 1 : 0;
+    const long long btiles = static_cast<long long>(tp.dw_tiles) + tp.dx_tiles;
+    st = cuda_status(launch_tc(kModeBwd, bm, tp, static_cast<int>(std::min<long long>(c.dev.sms, btiles)), c.stream));
+    if (st != FLCE_OK) return st;
+  }
+  return cuda_status(launch_convert_bf16(c.dx_acc(), dX, p.n * p.h, c.stream));
+}
+
+}  // namespace
+
+int chunk_width(int64_t n) { return n <= 16384 ? 8192 : 4096; }
+
+}  // namespace flce
+
+using namespace flce;
+
+extern "C" {
+
+size_t flce_workspace_bytes(const flce_problem_t* p) {
+  if (check_problem(p) != FLCE_OK) return 0;
+  return make_layout(*p).total;
+}
+
+flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
+                           float* lse, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!X || !W || !labels || !loss || !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(labels, 4) || !aligned(lse, 4) || !aligned(loss, 4))
+    return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  if (st != FLCE_OK) return st;
+  return run_forward(c, X, W, labels, loss, lse, nullptr);
+}
+
+flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
+                            const float* lse, const float* grad_loss, void* dX, void* dW, void* ws, size_t ws_bytes,
+                            flce_stream_t stream) {
+  if (!X || !W || !labels || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(labels, 4) ||
+      !aligned(lse, 4) || (grad_loss && !aligned(grad_loss, 4)))
+    return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  if (st != FLCE_OK) return st;
+  st = cuda_status(launch_label_scan(static_cast<int>(p->n), static_cast<int>(p->v), p->ignore_index, labels,
+                                     c.blk_loss(), c.blk_valid(), c.status(), c.stream));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction, grad_loss, nullptr,
+                                       c.n_valid(), c.scale(), c.stream));
+  if (st != FLCE_OK) return st;
+  return run_backward(c, X, W, labels, lse, dX, dW);
+}
+
+flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
+                           float* lse, void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!X || !W || !labels || !loss || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(labels, 4) ||
+      !aligned(lse, 4) || !aligned(loss, 4))
+    return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  if (st != FLCE_OK) return st;
+  st = run_forward(c, X, W, labels, loss, lse, nullptr);
+  if (st != FLCE_OK) return st;
+  return run_backward(c, X, W, labels, lse, dX, dW);
+}
+
+flce_status_t flce_read_device_status(void* ws, flce_stream_t stream) {
+  if (!ws || !aligned(ws, kAlign)) return FLCE_ERR_INVALID_ARGUMENT;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaStreamSynchronize(s) != cudaSuccess) return FLCE_ERR_CUDA;
+  int word = 0;
+  if (cudaMemcpy(&word, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return FLCE_ERR_NO_DEVICE_STATUS;
+  const int zero = 0;
+  if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FLCE_ERR_NO_DEVICE_STATUS;
+  return static_cast<flce_status_t>(word);
+}
+
+flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream) {
+  if (!ws || ws_bytes < kAlign) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  if (limit_ns == 0 || limit_ns > 10000000000ull) return FLCE_ERR_INVALID_ARGUMENT;
+  if (cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FLCE_ERR_CUDA;
+  return cuda_status(launch_timeout_selftest(static_cast<int*>(ws), limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+const char* flce_status_string(flce_status_t s) {
+  switch (s) {
+    case FLCE_OK: return "ok";
+    case FLCE_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case FLCE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape (h must be a multiple of 8, >= 8)";
+    case FLCE_ERR_MISALIGNED: return "misaligned pointer";
+    case FLCE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case FLCE_ERR_LABEL_OUT_OF_RANGE: return "label outside [0, V) and not ignore_index";
+    case FLCE_ERR_TIMEOUT: return "a bounded device wait timed out";
+    case FLCE_ERR_CUDA: return "CUDA error or unsupported device";
+    case FLCE_ERR_NO_DEVICE_STATUS: return "could not read the device status word";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

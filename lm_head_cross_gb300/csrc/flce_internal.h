@@ -1,0 +1,76 @@
+// Internal interface between the C-ABI layer (flce_api.cu) and the kernels
+// (flce_kernels.cu).  Not part of the public header.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace flce {
+
+// Tile shape of every tensor-core kernel: 128 rows (TMEM lanes) x 256 columns
+// (TMEM columns of one accumulator), K staged 64 bf16 (one 128-byte swizzle row)
+// at a time.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
+constexpr int kMaxSplit = 32;  // most vocabulary splits of the forward pass
+
+// Vocabulary chunk width of the backward pass (a multiple of kBN).  The
+// workspace holds one chunk of G, N x chunk bf16.
+int chunk_width(int64_t n);
+
+enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2 };
+
+// Everything a tensor-core launch needs besides its tensor maps.
+struct TcParams {
+  int n, h, v;
+  int ignore_index;
+  uint64_t timeout_ns;
+  int* status;
+  // forward: row tiles x vocabulary splits
+  int row_tiles, vocab_tiles, vsplit;
+  float* part_m;  // [vsplit][n] running max, log2 units
+  float* part_l;  // [vsplit][n] running sum of 2^(t - m)
+  float* tgt;     // [n] target logit z_{i, y_i}
+  const int32_t* labels;
+  // grad / bwd: one vocabulary chunk [c0, c0 + cw)
+  int c0, cw;
+  const float* lse;
+  const float* scale;  // device scalar s
+  int grad_n_tiles;    // grad: vocabulary tiles in the chunk
+  // bwd: dX tiles then dW tiles
+  int dx_tiles, dw_tiles;
+  int h_tiles;          // ceil(h / kBN)
+  int dw_m_tiles;       // ceil(cw / kBM)
+  int dx_accumulate;    // 0: first chunk stores, 1: later chunks add
+};
+
+struct TcMaps {
+  CUtensorMap a;   // forward/grad: X (K-major, box 64x128); bwd: G K-major (dX)
+  CUtensorMap b;   // forward/grad: W (K-major, box 64x256); bwd: W MN-major (dX)
+  CUtensorMap out; // grad: G store (bf16 box 64x32); bwd: dX fp32 accumulator (box 32x32)
+  CUtensorMap a2;  // bwd: G MN-major (dW A operand, box 64x64)
+  CUtensorMap b2;  // bwd: X MN-major (dW B operand, box 64x64)
+  CUtensorMap out2;// bwd: dW bf16 store (box 64x32)
+};
+
+// Launchers (asynchronous on `stream`; return the launch error, if any).
+cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
+cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m,
+                                const float* part_l, const float* tgt, const int32_t* labels, float* lse,
+                                double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
+cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss,
+                              int* blk_valid, int* status, cudaStream_t stream);
+cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,
+                                const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
+                                cudaStream_t stream);
+cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
+cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+int tc_smem_bytes();
+constexpr int kFinalizeThreads = 256;
+
+}  // namespace flce

@@ -1,0 +1,705 @@
+// Kernels of the fused LM-head projection + cross-entropy.
+//
+// One persistent, warp-specialised tcgen05 kernel template does all the dense
+// work ("What-Each-Parallelism-Actually-Shards" §7.4: fuse the projection, the
+// log-sum-exp, the target-logit read and the backward, so the [N,V] logits are
+// never written to global memory):
+//
+//   kModeForward  S = X W^T tile by tile (K = H) into TMEM; the epilogue keeps
+//                 a running (max, sum-of-exp) per row over the vocabulary tiles
+//                 of its split and picks out the target logit.  Nothing of S
+//                 leaves the SM.
+//   kModeGrad     recomputes S for one vocabulary chunk and writes
+//                 G = s (exp(S - lse) - onehot) valid as bf16 into the chunk
+//                 buffer (N x chunk, the only O(N x tile) scratch).
+//   kModeBwd      two contractions on that chunk in one launch:
+//                 dW[chunk] = G^T X (K = N, written once as bf16) and
+//                 dX += G W[chunk] (K = chunk, fp32 accumulated with TMA
+//                 reduce-add at L2).
+//
+// Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage shared-memory ring;
+// warp 1 lane 0 issues tcgen05.mma (128 x 256 x 16, bf16 -> fp32) into one of
+// two TMEM accumulators (2 x 256 columns); warps 2-5 drain the other
+// accumulator with tcgen05.ld (one TMEM lane = one row per thread), so row
+// reductions need no shuffles.  Every wait is bounded (see mbar_wait).
+#include "flce_device.cuh"
+#include "flce_internal.h"
+
+namespace flce {
+
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+constexpr int kAStage = kBM * kBK * 2;             // 16 KiB
+constexpr int kBStage = kBN * kBK * 2;             // 32 KiB
+constexpr int kStageBytes = kAStage + kBStage;     // 48 KiB
+constexpr int kMnBlock = 64 * kBK * 2;             // one 64-wide MN block of 64 K rows: 8 KiB
+constexpr int kStagingBuf = 32 * 128;              // 32 rows x 128 B
+constexpr int kStagingPerWarp = 2 * kStagingBuf;
+constexpr int kSmemStages = kStages * kStageBytes;
+constexpr int kSmemStagingOff = kSmemStages;
+constexpr int kSmemBarOff = kSmemStagingOff + 4 * kStagingPerWarp;
+constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;  // barriers, slot, flag; 1 KiB alignment slack
+constexpr uint32_t kTmemCols = 2 * kBN;
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+struct Tile {
+  int m0, n0;   // origin in the output index space of this tile's GEMM
+  int kblocks;  // K steps of kBK
+  int kind;     // 0 forward, 1 grad, 2 dX, 3 dW
+  int first, last, split;
+};
+
+struct Sched {
+  int unit, rt, sp, vt, ve;  // forward
+  int t;                     // grad / bwd
+  bool done;
+};
+
+__device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+__device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
+  const int units = p.row_tiles * p.vsplit;
+  if (s.unit >= units) {
+    s.done = true;
+    return;
+  }
+  s.rt = s.unit / p.vsplit;
+  s.sp = s.unit % p.vsplit;
+  s.vt = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
+  s.ve = static_cast<int>(static_cast<int64_t>(s.sp + 1) * p.vocab_tiles / p.vsplit);
+}
+
+template <int MODE>
+__device__ __forceinline__ void sched_init(const TcParams& p, Sched& s) {
+  s.done = false;
+  if (MODE == kModeForward) {
+    s.unit = blockIdx.x;
+    fwd_unit_begin(p, s);
+  } else {
+    s.t = blockIdx.x;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Tile& t) {
+  if (MODE == kModeForward) {
+    if (s.done) return false;
+    const int vb = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
+    t.m0 = s.rt * kBM;
+    t.n0 = s.vt * kBN;
+    t.kblocks = ceil_div(p.h, kBK);
+    t.kind = 0;
+    t.first = (s.vt == vb);
+    t.last = (s.vt == s.ve - 1);
+    t.split = s.sp;
+    return true;
+  } else if (MODE == kModeGrad) {
+    if (s.t >= p.row_tiles * p.grad_n_tiles) return false;
+    t.m0 = (s.t / p.grad_n_tiles) * kBM;
+    t.n0 = (s.t % p.grad_n_tiles) * kBN;  // chunk-local vocabulary column
+    t.kblocks = ceil_div(p.h, kBK);
+    t.kind = 1;
+    t.first = t.last = 0;
+    t.split = 0;
+    return true;
+  } else {
+    if (s.t >= p.dw_tiles + p.dx_tiles) return false;
+    if (s.t < p.dw_tiles) {  // dW tiles first: they are the long ones (K = N)
+      t.m0 = (s.t / p.h_tiles) * kBM;  // chunk-local vocabulary row
+      t.n0 = (s.t % p.h_tiles) * kBN;  // hidden column
+      t.kblocks = ceil_div(p.n, kBK);
+      t.kind = 3;
+    } else {
+      const int u = s.t - p.dw_tiles;
+      t.m0 = (u / p.h_tiles) * kBM;  // token row
+      t.n0 = (u % p.h_tiles) * kBN;  // hidden column
+      t.kblocks = ceil_div(p.cw, kBK);
+      t.kind = 2;
+    }
+    t.first = t.last = 0;
+    t.split = 0;
+    return true;
+  }
+}
+
+template <int MODE>
+__device__ __forceinline__ void sched_next(const TcParams& p, Sched& s) {
+  if (MODE == kModeForward) {
+    if (++s.vt >= s.ve) {
+      s.unit += gridDim.x;
+      fwd_unit_begin(p, s);
+    }
+  } else {
+    s.t += gridDim.x;
+  }
+}
+
+__device__ __forceinline__ void record_timeout(const TcParams& p, volatile int* abort_flag) {
+  *abort_flag = 1;
+  atomicCAS(p.status, 0, kErrTimeout);
+}
+
+// ----------------------------------------------------------------------------- producer (TMA)
+
+template <int MODE>
+__device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                             volatile int* abort_flag) {
+  Sched s;
+  sched_init<MODE>(p, s);
+  Tile t;
+  int stage = 0;
+  uint32_t phase = 0;
+  while (sched_get<MODE>(p, s, t)) {
+    for (int kb = 0; kb < t.kblocks; ++kb) {
+      if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
+        record_timeout(p, abort_flag);
+        return;
+      }
+      uint8_t* sa = smem + stage * kStageBytes;
+      uint8_t* sb = sa + kAStage;
+      uint64_t* bar = &full[stage];
+      mbar_arrive_expect_tx(bar, kStageBytes);
+      const int k0 = kb * kBK;
+      if (t.kind <= 1) {  // A = X [N,H] K-major, B = W [V,H] K-major
+        const int vcol = (t.kind == 1) ? p.c0 + t.n0 : t.n0;
+        tma_load_2d(sa, &maps.a, bar, k0, t.m0);
+        tma_load_2d(sb, &maps.b, bar, k0, vcol);
+      } else if (t.kind == 2) {  // dX: A = G [N, cw] K-major, B = W rows of the chunk, MN-major
+        tma_load_2d(sa, &maps.a, bar, k0, t.m0);
+#pragma unroll
+        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b, bar, t.n0 + 64 * j, p.c0 + k0);
+      } else {  // dW: A = G^T (G MN-major), B = X MN-major; K runs over token rows
+#pragma unroll
+        for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
+#pragma unroll
+        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b2, bar, t.n0 + 64 * j, k0);
+      }
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    sched_next<MODE>(p, s);
+  }
+}
+
+// ----------------------------------------------------------------------------- MMA issuer
+
+template <int MODE>
+__device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* tfull,
+                        uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
+  Sched s;
+  sched_init<MODE>(p, s);
+  Tile t;
+  int stage = 0;
+  uint32_t phase = 0;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+  while (sched_get<MODE>(p, s, t)) {
+    const bool a_mn = (t.kind == 3);
+    const bool b_mn = (t.kind >= 2);
+    const uint32_t idesc = instr_desc_bf16(kBM, kBN, a_mn, b_mn);
+    if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
+      record_timeout(p, abort_flag);
+      return;
+    }
+    tc_fence_after_sync();
+    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
+    for (int kb = 0; kb < t.kblocks; ++kb) {
+      if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
+        record_timeout(p, abort_flag);
+        return;
+      }
+      tc_fence_after_sync();
+      const uint32_t sa = smem_u32(smem + stage * kStageBytes);
+      const uint32_t sb = sa + kAStage;
+#pragma unroll
+      for (int k = 0; k < kBK / 16; ++k) {
+        const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, kMnBlock, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
+        const uint64_t bd = b_mn ? smem_desc_sw128(sb + k * 2048, kMnBlock, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
+        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+      }
+      umma_commit(&empty[stage]);  // frees this stage once the MMAs above have read it
+      if (++stage == kStages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+    sched_next<MODE>(p, s);
+  }
+}
+
+// ----------------------------------------------------------------------------- epilogue helpers
+
+// Write one 128-byte row per lane into a 32-row staging buffer laid out the
+// way a 128-byte-swizzled TMA box expects (16-byte chunk c of row r at c ^ (r & 7)).
+__device__ __forceinline__ void stage_rows(uint8_t* buf, int lane, const uint32_t (&w)[32]) {
+  uint8_t* row = buf + lane * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+}
+
+// Stage 32 rows x 128 B and hand them to TMA (store or reduce-add); two
+// alternating buffers per warp so the next tile overlaps the previous copy.
+__device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t* stg, int& sbuf, int lane,
+                                                const uint32_t (&w)[32], int x, int y, bool reduce) {
+  uint8_t* buf = stg + sbuf * kStagingBuf;
+  if (lane == 0) bulk_wait_group_read<1>();
+  __syncwarp();
+  stage_rows(buf, lane, w);
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    if (reduce)
+      tma_reduce_add_2d(map, buf, x, y);
+    else
+      tma_store_2d(map, buf, x, y);
+    bulk_commit_group();
+  }
+  sbuf ^= 1;
+}
+
+__device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int lane) {
+  tc_fence_before_sync();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(tempty_acc);
+}
+
+// ----------------------------------------------------------------------------- epilogue
+
+template <int MODE>
+__device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* staging, uint64_t* tfull,
+                             uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int quarter = warp & 3;  // a warp may only touch TMEM lanes [32*(warp%4), +32)
+  const int r = quarter * 32 + lane;
+  uint8_t* stg = staging + (warp - 2) * kStagingPerWarp;
+  int sbuf = 0;
+
+  Sched s;
+  sched_init<MODE>(p, s);
+  Tile t;
+  int acc = 0;
+  uint32_t acc_phase = 0;
+
+  // forward state (one row per thread)
+  float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
+  bool found = false;
+  int y_fwd = p.ignore_index;
+  const float scale = (MODE == kModeGrad) ? *p.scale : 0.f;
+
+  while (sched_get<MODE>(p, s, t)) {
+    if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag)) {
+      record_timeout(p, abort_flag);
+      break;
+    }
+    __syncwarp();
+    tc_fence_after_sync();
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
+
+    if (MODE == kModeForward) {
+      const int row = t.m0 + r;
+      if (t.first) {
+        run_m = -INFINITY;
+        run_l = 0.f;
+        found = false;
+        y_fwd = (row < p.n) ? p.labels[row] : p.ignore_index;
+      }
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; ++c) {
+        const int col0 = t.n0 + c * 32;
+        if (col0 >= p.v) break;  // same for the whole warp
+        __syncwarp();
+        uint32_t v[32];
+        tmem_ld_32x32(tbase + c * 32, v);
+        const int yi = y_fwd - col0;
+        if (static_cast<unsigned>(yi) < 32u) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            if (j == yi) z_tgt = __uint_as_float(v[j]);
+          found = true;
+        }
+        const int nv = min(32, p.v - col0);
+        float cmax = -INFINITY;
+        if (nv == 32) {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, __uint_as_float(v[j]));
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (j >= nv) v[j] = __float_as_uint(-INFINITY);
+            cmax = fmaxf(cmax, __uint_as_float(v[j]));
+          }
+        }
+        const float new_m = fmaxf(run_m, cmax * kLog2e);
+        float sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
+        run_l = run_l * fast_exp2(run_m - new_m) + sum;
+        run_m = new_m;
+      }
+      release_accumulator(&tempty[acc], lane);
+      if (t.last && row < p.n) {
+        p.part_m[static_cast<int64_t>(t.split) * p.n + row] = run_m;
+        p.part_l[static_cast<int64_t>(t.split) * p.n + row] = run_l;
+        if (found) p.tgt[row] = z_tgt;
+      }
+    } else if (MODE == kModeGrad) {
+      const int row = t.m0 + r;
+      const int y = (row < p.n) ? p.labels[row] : p.ignore_index;
+      const bool valid = (row < p.n) && (y != p.ignore_index);
+      const float coef = valid ? scale : 0.f;
+      const float lse2 = (row < p.n) ? p.lse[row] * kLog2e : 0.f;
+      const int ycol = y - (p.c0 + t.n0);  // label position inside this tile (if any)
+#pragma unroll 1
+      for (int g = 0; g < kBN / 64; ++g) {
+        if (t.n0 + g * 64 >= p.cw) break;
+        __syncwarp();
+        uint32_t v[64];
+        tmem_ld_32x64(tbase + g * 64, v);
+        uint32_t w[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int c = g * 64 + 2 * j;
+          float a = fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -lse2));
+          float b = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -lse2));
+          a = coef * (a - (c == ycol ? 1.f : 0.f));
+          b = coef * (b - (c + 1 == ycol ? 1.f : 0.f));
+          w[j] = pack_bf16x2(a, b);
+        }
+        // columns at or beyond the chunk width fall outside the store box's tensor and are dropped by TMA
+        stage_and_store(&maps.out, stg, sbuf, lane, w, t.n0 + g * 64, t.m0 + quarter * 32, false);
+      }
+      release_accumulator(&tempty[acc], lane);
+    } else {
+      if (t.kind == 2) {  // dX partial: fp32, stored (first chunk) or added at L2
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          if (t.n0 + c * 32 >= p.h) break;
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32(tbase + c * 32, v);
+          stage_and_store(&maps.out, stg, sbuf, lane, v, t.n0 + c * 32, t.m0 + quarter * 32, p.dx_accumulate != 0);
+        }
+      } else {  // dW rows of the chunk: complete sums over all tokens, bf16
+#pragma unroll 1
+        for (int g = 0; g < kBN / 64; ++g) {
+          if (t.n0 + g * 64 >= p.h) break;
+          __syncwarp();
+          uint32_t v[64];
+          tmem_ld_32x64(tbase + g * 64, v);
+          uint32_t w[32];
+#pragma unroll
+          for (int j = 0; j < 32; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          stage_and_store(&maps.out2, stg, sbuf, lane, w, t.n0 + g * 64, p.c0 + t.m0 + quarter * 32, false);
+        }
+      }
+      release_accumulator(&tempty[acc], lane);
+    }
+    acc ^= 1;
+    if (acc == 0) acc_phase ^= 1u;
+    sched_next<MODE>(p, s);
+  }
+  if (lane == 0) bulk_wait_group_all();
+  __syncwarp();
+}
+
+// ----------------------------------------------------------------------------- the kernel
+
+template <int MODE>
+__global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
+  uint64_t* full = bars;
+  uint64_t* empty = bars + kStages;
+  uint64_t* tfull = bars + 2 * kStages;
+  uint64_t* tempty = bars + 2 * kStages + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 5);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+    }
+    *abort_flag = 0;
+    mbar_fence_init();
+    fence_proxy_async_smem();
+    tma_prefetch_map(&maps.a);
+    tma_prefetch_map(&maps.b);
+    if (MODE != kModeForward) tma_prefetch_map(&maps.out);
+    if (MODE == kModeBwd) {
+      tma_prefetch_map(&maps.a2);
+      tma_prefetch_map(&maps.b2);
+      tma_prefetch_map(&maps.out2);
+    }
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) run_producer<MODE>(maps, p, smem, full, empty, abort_flag);
+  } else if (warp == 1) {
+    if (lane == 0) run_mma<MODE>(p, smem, full, empty, tfull, tempty, tmem_base, abort_flag);
+  } else {
+    run_epilogue<MODE>(maps, p, smem + kSmemStagingOff, tfull, tempty, tmem_base, abort_flag);
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (*abort_flag) {
+    // A wait gave up: let copies and MMAs already in flight land before the
+    // shared memory and TMEM are released (they finish in microseconds).
+    const uint64_t t0 = global_timer_ns();
+    while (global_timer_ns() - t0 < 2000000ull) {
+    }
+  }
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+// ----------------------------------------------------------------------------- small kernels
+
+// Merge the per-split (max, sum) pairs of each row into lse, check its label,
+// and reduce the per-row losses of the block in a fixed order.
+__global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
+    int n, int v, int vsplit, int ignore_index, const float* __restrict__ part_m, const float* __restrict__ part_l,
+    const float* __restrict__ tgt, const int32_t* __restrict__ labels, float* __restrict__ lse_out,
+    double* __restrict__ blk_loss, int* __restrict__ blk_valid, int* __restrict__ status) {
+  __shared__ double s_loss[kFinalizeThreads];
+  __shared__ int s_valid[kFinalizeThreads];
+  const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  double li = 0.0;
+  int valid = 0;
+  if (row < n) {
+    float m = -INFINITY;
+    for (int s = 0; s < vsplit; ++s) m = fmaxf(m, part_m[static_cast<int64_t>(s) * n + row]);
+    float l = 0.f;
+    for (int s = 0; s < vsplit; ++s)
+      l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
+    const float lse = (m + log2f(l)) * kLn2;
+    lse_out[row] = lse;
+    const int y = labels[row];
+    if (y != ignore_index) {
+      if (y >= 0 && y < v) {
+        valid = 1;
+        li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
+      } else {
+        atomicCAS(status, 0, kErrLabel);
+      }
+    }
+  }
+  s_loss[threadIdx.x] = li;
+  s_valid[threadIdx.x] = valid;
+  __syncthreads();
+  for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_loss[blockIdx.x] = s_loss[0];
+    blk_valid[blockIdx.x] = s_valid[0];
+  }
+}
+
+// Label scan: range check and valid count, for a backward call on its own.
+__global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int v, int ignore_index,
+                                                                       const int32_t* __restrict__ labels,
+                                                                       double* __restrict__ blk_loss,
+                                                                       int* __restrict__ blk_valid,
+                                                                       int* __restrict__ status) {
+  __shared__ int s_valid[kFinalizeThreads];
+  const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  int valid = 0;
+  if (row < n) {
+    const int y = labels[row];
+    if (y != ignore_index) {
+      if (y >= 0 && y < v)
+        valid = 1;
+      else
+        atomicCAS(status, 0, kErrLabel);
+    }
+  }
+  s_valid[threadIdx.x] = valid;
+  __syncthreads();
+  for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_loss[blockIdx.x] = 0.0;
+    blk_valid[blockIdx.x] = s_valid[0];
+  }
+}
+
+// One block: fixed-order sum of the block partials; loss, valid count and the
+// gradient scale s = g / n_valid (mean) or g (sum).
+__global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk, const double* __restrict__ blk_loss,
+                                                                         const int* __restrict__ blk_valid,
+                                                                         int reduction, const float* grad_loss,
+                                                                         float* loss_out, int* n_valid_out,
+                                                                         float* scale_out) {
+  __shared__ double s_loss[kFinalizeThreads];
+  __shared__ long long s_valid[kFinalizeThreads];
+  double l = 0.0;
+  long long c = 0;
+  for (int i = threadIdx.x; i < nblk; i += kFinalizeThreads) {
+    l += blk_loss[i];
+    c += blk_valid[i];
+  }
+  s_loss[threadIdx.x] = l;
+  s_valid[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double total = s_loss[0];
+    const long long nv = s_valid[0];
+    const double g = grad_loss ? static_cast<double>(*grad_loss) : 1.0;
+    double loss, scale;
+    if (reduction == 0) {  // mean over valid rows; no valid row gives 0
+      loss = nv > 0 ? total / static_cast<double>(nv) : 0.0;
+      scale = nv > 0 ? g / static_cast<double>(nv) : 0.0;
+    } else {
+      loss = total;
+      scale = g;
+    }
+    if (loss_out) *loss_out = static_cast<float>(loss);
+    *n_valid_out = static_cast<int>(nv);
+    *scale_out = static_cast<float>(scale);
+  }
+}
+
+__global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t count8) {
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+    uint4 o;
+    o.x = pack_bf16x2(a.x, a.y);
+    o.y = pack_bf16x2(a.z, a.w);
+    o.z = pack_bf16x2(b.x, b.y);
+    o.w = pack_bf16x2(b.z, b.w);
+    reinterpret_cast<uint4*>(dst)[i] = o;
+  }
+}
+
+// Waits on a barrier that nothing completes; the bounded wait gives up and the
+// timeout lands in the status word.
+__global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, limit_ns, &abort_flag)) atomicCAS(status, 0, kErrTimeout);
+  }
+}
+
+}  // namespace
+
+int tc_smem_bytes() { return kSmemBytes; }
+
+template <int MODE>
+static cudaError_t launch_mode(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
+  static int configured_device = -1;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  tc_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
+  switch (mode) {
+    case kModeForward: return launch_mode<kModeForward>(maps, p, grid, stream);
+    case kModeGrad: return launch_mode<kModeGrad>(maps, p, grid, stream);
+    case kModeBwd: return launch_mode<kModeBwd>(maps, p, grid, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
+                                const float* tgt, const int32_t* labels, float* lse, double* blk_loss, int* blk_valid,
+                                int* status, cudaStream_t stream) {
+  const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
+  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, vsplit, ignore_index, part_m, part_l, tgt, labels,
+                                                               lse, blk_loss, blk_valid, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss, int* blk_valid,
+                              int* status, cudaStream_t stream) {
+  const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
+  label_scan_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, ignore_index, labels, blk_loss, blk_valid, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,
+                                const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
+                                cudaStream_t stream) {
+  reduce_final_kernel<<<1, kFinalizeThreads, 0, stream>>>(nblk, blk_loss, blk_valid, reduction, grad_loss, loss_out,
+                                                          n_valid_out, scale_out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream) {
+  const int64_t count8 = count / 8;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (count8 + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  convert_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), count8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
+  timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace flce

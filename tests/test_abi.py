@@ -1,0 +1,85 @@
+"""The C-ABI library loads on the CPU, exports every symbol include/flce.h
+declares, and rejects bad arguments on the host (no GPU call is made)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import lm_head_cross_gb300 as flce
+from lm_head_cross_gb300 import binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "flce.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(flce_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    L = flce.lib()
+    names = _declared()
+    assert set(names) == set(binding.EXPORTED)
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_status_strings():
+    for code in range(0, 9):
+        assert flce.status_string(code)
+
+
+def test_workspace_size_rules():
+    ws = flce.workspace_bytes
+    assert ws(256, 128, 1024) > 0
+    # independent of V (the logits are never stored)
+    assert ws(8192, 2048, 32000) == ws(8192, 2048, 128256) == ws(8192, 2048, 7)
+    # grows with N
+    assert ws(16384, 2048, 32000) > ws(8192, 2048, 32000)
+    # invalid problems give 0
+    assert ws(0, 128, 10) == 0 and ws(10, 12, 10) == 0 and ws(10, 4, 10) == 0 and ws(10, 128, 0) == 0
+    # the largest workload stays under 4 GB of extra device memory
+    assert ws(131072, 4096, 131072) < 4e9
+
+
+def _call_forward(p, X=0x1000, W=0x2000, lab=0x3000, loss=0x4000, lse=0x5000, ws=0x100000, nbytes=None):
+    L = flce.lib()
+    if nbytes is None:
+        nbytes = L.flce_workspace_bytes(ctypes.byref(p))
+    return L.flce_forward(ctypes.byref(p), X, W, lab, loss, lse, ws, nbytes, None)
+
+
+def test_host_side_validation_without_gpu():
+    P = binding.Problem
+    ok = P(256, 128, 1024, -100, 0)
+    assert _call_forward(ok, X=None) == 1            # null pointer
+    assert _call_forward(ok, X=0x1008) == 3          # misaligned X
+    assert _call_forward(ok, lab=0x3002) == 3        # misaligned labels
+    assert _call_forward(ok, ws=0x100010) == 3       # misaligned workspace
+    assert _call_forward(ok, nbytes=16) == 4         # workspace too small
+    assert _call_forward(P(256, 12, 1024, -100, 0)) == 2   # h % 8 != 0
+    assert _call_forward(P(256, 128, 1024, -100, 7)) == 1  # bad reduction
+    assert _call_forward(P(0, 128, 1024, -100, 0)) == 1    # empty
+    L = flce.lib()
+    assert L.flce_selftest_timeout(None, 256, 1000, None) == 1
+    assert L.flce_selftest_timeout(0x100010, 256, 1000, None) == 3
+    assert L.flce_read_device_status(None, None) == 1
+
+
+def test_python_binding_rejects_bad_reduction():
+    with pytest.raises(ValueError):
+        flce.workspace_bytes(10, 16, 10, reduction="none")
+
+
+def test_footprint_golden():
+    """Logits footprint of the worked 128K x 128K case, as printed on the page."""
+    import os
+    from lm_head_cross_gb300 import logits_footprint_bytes
+    path = os.path.join(os.path.dirname(__file__), "golden", "footprint_128k.txt")
+    rows = [l.split() for l in open(path) if l.strip() and not l.startswith("#")]
+    assert rows
+    for b, s, v, e, want, _ in rows:
+        assert logits_footprint_bytes(int(b) * int(s), int(v), int(e)) == int(want)
+    assert logits_footprint_bytes(131072, 131072, 2) == 32 << 30

@@ -1,0 +1,172 @@
+"""GPU parity: the CUDA path through the C-ABI against the fp64 oracle, element
+by element, on the same seeded inputs.  Sizes span several tiles with ragged
+tails in every dimension (rows vs 128-row tiles, vocabulary vs 256-wide tiles
+and the backward's vocabulary chunks, hidden vs 64-wide K steps)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from helpers import assert_grad, assert_loss, assert_lse, to_device
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+import lm_head_cross_gb300 as flce  # noqa: E402
+
+
+def run(problem, **kw):
+    X, W, y = to_device(problem)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction, **kw)
+    st = flce.read_device_status(ws)
+    return dict(loss=float(loss.item()), lse=lse.cpu().numpy(), dX=dX.float().cpu().numpy(),
+                dW=dW.float().cpu().numpy(), status=st)
+
+
+def check_full(problem):
+    got = run(problem)
+    assert got["status"] == 0, flce.status_string(got["status"])
+    ref = oracle.full_bf16(problem)
+    assert_loss(got["loss"], ref["loss"])
+    assert_lse(got["lse"], ref["lse"])
+    assert_grad(got["dX"], ref["dX"], name="dX")
+    assert_grad(got["dW"], ref["dW"], name="dW")
+    valid = problem.labels != problem.ignore_index
+    assert np.all(got["dX"][~valid] == 0.0), "ignored rows must give exactly zero dX"
+    return got, ref
+
+
+@pytest.mark.parametrize("cfg", [1])
+def test_config_full(cfg):
+    check_full(synth.config_problem(cfg))
+
+
+@pytest.mark.parametrize("n,h,v,red,labels", [
+    (300, 136, 1000, "mean", "uniform"),      # ragged N, H (K tail), V
+    (129, 64, 257, "sum", "zipf"),            # one row past a tile, one column past a tile
+    (1, 8, 1, "mean", "uniform"),             # smallest shape; V = 1
+    (77, 72, 2, "sum", "uniform"),            # V = 2
+    (640, 256, 17000, "mean", "zipf"),        # three backward vocabulary chunks, ragged last chunk
+    (1000, 520, 8200, "sum", "uniform"),      # chunk boundary + 8 past it; H not a tile multiple
+])
+def test_ragged_shapes(n, h, v, red, labels):
+    p = synth.make_problem(n, h, v, seed=n + h + v, labels=labels, ignore_frac=0.1, reduction=red,
+                           w_std=0.05)
+    check_full(p)
+
+
+def test_outlier_rows_sum_reduction():
+    p = synth.make_problem(512, 256, 3000, seed=44, labels="zipf", ignore_frac=0.05, reduction="sum",
+                           outlier_rows=16, outlier_scale=10.0)
+    check_full(p)
+
+
+def test_all_rows_ignored_mean_gives_zero():
+    p = synth.make_problem(200, 64, 500, seed=3, ignore_frac=1.0, reduction="mean")
+    got = run(p)
+    assert got["status"] == 0
+    assert got["loss"] == 0.0
+    assert np.all(got["dX"] == 0) and np.all(got["dW"] == 0)
+    ref = oracle.full_bf16(p)
+    assert_lse(got["lse"], ref["lse"])
+
+
+def test_w_zero_closed_form():
+    """W = 0: loss = ln V exactly in the definition; dX = 0; dW from its closed form."""
+    p = synth.make_problem(384, 128, 3000, seed=5, ignore_frac=0.1)
+    p.W[:] = 0
+    got = run(p)
+    assert abs(got["loss"] - math.log(3000)) <= 1e-3 * math.log(3000)
+    assert np.all(got["dX"] == 0)
+    X = oracle.widen_bf16(p.X)
+    valid = p.labels != p.ignore_index
+    nv = valid.sum()
+    dW = np.tile(X[valid].sum(axis=0) / 3000, (3000, 1))
+    for i in np.nonzero(valid)[0]:
+        dW[p.labels[i]] -= X[i]
+    assert_grad(got["dW"], dW / nv, name="dW")
+
+
+def test_equal_rows_give_zero_dx_and_log_v():
+    p = synth.make_problem(256, 128, 700, seed=6, ignore_frac=0.0)
+    p.W[:] = p.W[3]
+    got = run(p)
+    assert abs(got["loss"] - math.log(700)) <= 1e-3 * math.log(700)
+    # every softmax row is uniform: dX_i = s (mean_j W_j - W_{y_i}) = 0
+    assert np.abs(got["dX"]).max() <= 1e-6
+
+
+def test_dw_vocab_sum_is_zero():
+    p = synth.make_problem(512, 256, 5000, seed=8, ignore_frac=0.05, reduction="sum")
+    got = run(p)
+    dW = got["dW"]
+    # each row of G sums to zero, so the vocabulary sum of dW vanishes up to bf16 rounding of dW
+    resid = np.abs(dW.astype(np.float64).sum(axis=0)).max()
+    bound = 2 * 2.0 ** -8 * np.abs(dW.astype(np.float64)).sum(axis=0).max()
+    assert resid <= bound, (resid, bound)
+
+
+def test_label_out_of_range_sets_status():
+    p = synth.make_problem(256, 64, 300, seed=9)
+    p.labels[17] = 300
+    X, W, y = to_device(p)
+    _, _, _, _, ws = flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction)
+    assert flce.read_device_status(ws) == 5
+    p.labels[17] = -5
+    X, W, y = to_device(p)
+    _, _, ws = flce.forward(X, W, y, p.ignore_index, p.reduction)
+    assert flce.read_device_status(ws) == 5
+    # a clean call clears the word
+    p.labels[17] = 0
+    X, W, y = to_device(p)
+    _, _, ws = flce.forward(X, W, y, p.ignore_index, p.reduction, ws=ws)
+    assert flce.read_device_status(ws) == 0
+
+
+def test_separate_forward_backward_with_upstream_gradient():
+    p = synth.make_problem(700, 192, 2500, seed=10, labels="zipf", ignore_frac=0.1, reduction="mean")
+    X, W, y = to_device(p)
+    loss, lse, ws = flce.forward(X, W, y, p.ignore_index, p.reduction)
+    g = torch.tensor([0.37], dtype=torch.float32, device="cuda")
+    dX, dW, _ = flce.backward(X, W, y, lse, g, p.ignore_index, p.reduction, ws=ws)
+    assert flce.read_device_status(ws) == 0
+    ref = oracle.full_bf16(p, grad_output=0.37)
+    assert_loss(float(loss.item()), ref["loss"])
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+def test_autograd_wrapper():
+    p = synth.make_problem(2 * 150, 128, 1500, seed=12, labels="zipf", ignore_frac=0.1)
+    X, W, y = to_device(p)
+    x3 = X.reshape(2, 150, 128).clone().requires_grad_(True)
+    w = W.clone().requires_grad_(True)
+    loss = flce.linear_cross_entropy(x3, w, y.reshape(2, 150).long())
+    loss.backward()
+    ref = oracle.full_bf16(p)
+    assert_loss(float(loss.item()), ref["loss"])
+    assert_grad(x3.grad.reshape(300, 128).float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+def test_repeat_calls_are_deterministic():
+    p = synth.make_problem(512, 256, 9000, seed=13, ignore_frac=0.05)
+    a = run(p)
+    b = run(p)
+    assert a["loss"] == b["loss"]
+    assert np.array_equal(a["lse"], b["lse"])
+    assert np.array_equal(a["dW"], b["dW"])
+
+
+def test_timeout_path_returns_status():
+    ws = torch.zeros(1024, dtype=torch.uint8, device="cuda")
+    L = flce.lib()
+    import ctypes
+    assert L.flce_selftest_timeout(ctypes.c_void_p(ws.data_ptr()), 1024, 20_000_000, None) == 0
+    assert flce.read_device_status(ws) == 6
+    # the context is still usable
+    p = synth.make_problem(128, 64, 256, seed=1)
+    got = run(p)
+    assert got["status"] == 0
