@@ -1,0 +1,382 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused LM-head projection + cross-entropy, forward + backward.
+
+Metric: credited TFLOP/s counting 6*N*H*V per step (2NHV for the logits, 2NHV
+each for dX and dW), with the extra device memory the op needs beside it.
+A step is one flce_fwd_bwd over one synthetic batch (loss, lse, dX, dW).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl flce|reference]
+
+Default workload: N = 4 x 2048 = 8192 tokens, H = 2048, V = 32000, labels
+Zipf(1.1) with 5% ignore_index, mean reduction (synth.CONFIGS[2]).
+Under torchrun each rank runs its own batch of that shape on its own GPU
+(weak scaling, no collective on the data path); rank 0 prints one JSON line.
+
+--impl reference times the fp64 CPU oracle on the host cores instead (bounded
+row samples of the same workload), the deliberately slow definition the
+CUDA path is checked against.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused linear-CE fwd+bwd TFLOP/s (6NHV), % of BF16 tensor peak; extra HBM"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--impl", choices=["flce", "reference"], default="flce")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def workload_config(cfg, problem_kw, l2_note, world):
+    import synth
+    c = synth.CONFIGS[cfg]
+    return {
+        "workload": f"config {cfg}: {c['name']}",
+        "n_tokens_per_rank": c["n"], "hidden": c["h"], "vocab": c["v"],
+        "labels": c["labels"] + ("(s=1.1)" if c["labels"] == "zipf" else ""),
+        "ignore_frac": c["ignore_frac"], "reduction": c["reduction"],
+        "x_std": c["x_std"], "w_std": c["w_std"], "outlier_rows": c.get("outlier_rows", 0),
+        "l2": l2_note,
+        "parallelism": f"replicas x{world} (rows sharded by rank, no collective)" if world > 1 else "single GPU",
+    }
+
+
+def credited_flops(n, h, v):
+    return 6.0 * n * h * v
+
+
+# ----------------------------------------------------------------------------- CPU oracle timing
+
+def oracle_sample_seconds(problem, rows):
+    """Time the fp64 oracle (loss, lse, dX, dW) on the first `rows` rows with the full W."""
+    import numpy as np
+    import oracle
+    X = oracle.widen_bf16(problem.X[:rows])
+    W = oracle.widen_bf16(problem.W)
+    lab = problem.labels[:rows]
+    t0 = time.perf_counter()
+    oracle.full(X, W, lab, problem.ignore_index, problem.reduction)
+    dt = time.perf_counter() - t0
+    del X, W, np
+    return dt
+
+
+def calibrate_rows(problem, target_s, max_rows):
+    r = min(64, max_rows)
+    dt = oracle_sample_seconds(problem, r)
+    per_row = dt / r
+    return int(max(1, min(max_rows, target_s / max(per_row, 1e-9))))
+
+
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(problem, target_s):
+    rows = calibrate_rows(problem, target_s, problem.n)
+    dt = oracle_sample_seconds(problem, rows)
+    val = credited_flops(rows, problem.h, problem.v) / dt / 1e12
+    return {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle (loss, lse, dX, dW) on the first {rows} of {problem.n} rows with the full "
+                      f"W [{problem.v}x{problem.h}], {dt:.1f} s; credited 6*rows*H*V flops; BLAS threads = numpy default"}
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return 0
+    import synth
+    problem = synth.config_problem(args.config)
+    total_steps = args.steps + args.warmup
+    per_step_s = max(0.5, min(10.0, 150.0 / max(1, total_steps)))
+    rows = calibrate_rows(problem, per_step_s, problem.n)
+    for _ in range(args.warmup):
+        oracle_sample_seconds(problem, rows)
+    times = [oracle_sample_seconds(problem, rows) for _ in range(args.steps)]
+    t = sum(times)
+    val = credited_flops(rows, problem.h, problem.v) * args.steps / t / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(args.config, None, "n/a (CPU)", world),
+        "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"each step: fp64 numpy oracle (loss, lse, dX, dW) on the first {rows} of "
+                                   f"{problem.n} rows with the full W"},
+        "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
+        power = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows), "power_w_max": max(power) if power else None}
+
+
+# ----------------------------------------------------------------------------- the CUDA arm
+
+def traffic_record(kind, cfg):
+    """DRAM bytes per launch of `kind` from a committed ncu capture, if it was taken
+    on the kernel source as it is now (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            recs = json.load(f)
+    except (OSError, ValueError):
+        return None
+    src = os.path.join(ROOT, "lm_head_cross_gb300", "csrc", "flce_kernels.cu")
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for r in recs:
+        if r.get("kind") == kind and r.get("config") == cfg and r.get("kernel_sha") == sha:
+            return float(r["bytes_per_launch"])
+    return None
+
+
+def run_flce(args, rank, world, local_rank):
+    import numpy as np
+    import torch
+    import lm_head_cross_gb300 as flce
+    import synth
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    c = dict(synth.CONFIGS[args.config])
+    c["seed"] = c["seed"] + 1000 * rank          # each rank: its own batch of the same shape
+    problem = synth.make_problem(**c)
+    n, h, v = problem.n, problem.h, problem.v
+    X = torch.from_numpy(problem.X.view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(problem.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.from_numpy(problem.labels).to(dev)
+    ws_bytes = flce.workspace_bytes(n, h, v, problem.ignore_index, problem.reduction)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = (torch.empty(1, dtype=torch.float32, device=dev), torch.empty(n, dtype=torch.float32, device=dev),
+           torch.empty_like(X), torch.empty_like(W))
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction, ws=ws, out=out)
+
+    # extra device memory of one call beyond its inputs and outputs
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    tmp_out = flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction)
+    torch.cuda.synchronize()
+    out_bytes = sum(t.numel() * t.element_size() for t in tmp_out[:4])
+    peak_delta = torch.cuda.max_memory_allocated(dev) - base - out_bytes
+    st = flce.read_device_status(tmp_out[4])
+    del tmp_out
+    if st != 0:
+        raise RuntimeError(f"device status {flce.status_string(st)}")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    clocks = ClockSampler(local_rank)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    flce.profile_enable(True)
+    clocks.start()
+    time.sleep(0.25)  # let the sampler take its first reading
+    t_wall0 = time.perf_counter()
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)                  # evict inputs from the 126 MB L2 between steps
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if dist is not None:
+        dist.barrier()
+    clk = clocks.stop()
+    prof = flce.profile_read()
+    flce.profile_enable(False)
+    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    total_ms = sum(step_ms)
+    if dist is not None:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    flops = credited_flops(n, h, v)
+    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+
+    # end to end through the public call with host buffers: H2D inputs, fwd_bwd, D2H outputs
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
+    Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True); Wh.copy_(W)
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True); yh.copy_(y)
+    outs_h = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out]
+    Xd, Wd, yd = torch.empty_like(X), torch.empty_like(W), torch.empty_like(y)
+
+    def e2e_step():
+        Xd.copy_(Xh, non_blocking=True)
+        Wd.copy_(Wh, non_blocking=True)
+        yd.copy_(yh, non_blocking=True)
+        flce.fwd_bwd(Xd, Wd, yd, problem.ignore_index, problem.reduction, ws=ws, out=out)
+        for dst, src in zip(outs_h, out):
+            dst.copy_(src, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if dist is not None:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
+    d2h = sum(t.numel() * t.element_size() for t in out)
+
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+    if rank != 0:
+        return 0
+
+    peaks, peak_src = load_peaks()
+    kinds = {k: {"launches": n_, "ms": ms_, "tflop": fl_ / 1e12} for k, (n_, ms_, fl_) in prof.items()}
+    dom = max((k for k in prof if prof[k][2] > 0), key=lambda k: prof[k][1])
+    n_l, ms_l, fl_l = prof[dom]
+    achieved = (fl_l / n_l) / ((ms_l / n_l) / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    gpu_launches = sum(x[0] for x in prof.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": workload_config(args.config, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
+                                                     "outside the per-step events)", world),
+        "frac_of_peak": value / world / peak_burst, "peak_src": f"{peak_src} bf16_tflops (burst)",
+        "executed_tflops": world * 8.0 * n * h * v * args.steps / (total_ms / 1e3) / 1e12,
+        "extra_hbm_bytes": ws_bytes, "peak_alloc_delta_bytes": int(peak_delta),
+        "materialised_logits_bytes": {"bf16": flce.logits_footprint_bytes(n, v, 2),
+                                      "fp32": flce.logits_footprint_bytes(n, v, 4)},
+        "wall_ms_per_step_incl_flush": 1e3 * t_wall / args.steps,
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "peak_note": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
+                                                           f"long loop); of burst {peak_burst}: {achieved / peak_burst:.3f}",
+                     "traffic": traffic_record(dom, args.config)},
+        "kernels": kinds,
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+        "e2e": {"value": world * flops * args.e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "note": "flce_fwd_bwd through the C-ABI with pinned host inputs copied in and loss/lse/dX/dW "
+                        "copied out every step"},
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(problem, args.cpu_seconds)
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    args = parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, rank, world)
+    return run_flce(args, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -110,6 +110,19 @@ flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);
  * the bounded waits used by every kernel. */
 flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream);
 
+/* Diagnostics: per-launch device timing.  While profiling is on, every kernel
+ * the calls above launch is bracketed by two CUDA events on its stream.
+ * flce_profile_read synchronises the recorded events and reports, for one
+ * kernel kind, the launches recorded, their summed device time (ms) and their
+ * summed algorithmic flops.  Kinds: 0 forward projection + online
+ * log-sum-exp (2*N*V*H flops), 1 recomputed logits -> G for one vocabulary
+ * chunk (2*N*C*H), 2 dX/dW contractions of one chunk (4*N*C*H), 3 small
+ * kernels (label scan, finalize, reductions, dX cast; 0 flops).  Enabling or
+ * disabling clears the totals.  Off by default.  Process-wide, not tied to a
+ * workspace. */
+flce_status_t flce_profile_enable(int on);
+flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, double* flops);
+
 /* Static description of a status code. */
 const char* flce_status_string(flce_status_t s);
 

@@ -19,7 +19,9 @@ FLCE_ERR_TIMEOUT = 6
 REDUCTIONS = {"mean": 0, "sum": 1}
 
 EXPORTED = ("flce_workspace_bytes", "flce_forward", "flce_backward", "flce_fwd_bwd",
-            "flce_read_device_status", "flce_selftest_timeout", "flce_status_string")
+            "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
+            "flce_status_string")
+KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
 class FlceError(RuntimeError):
@@ -62,6 +64,11 @@ def lib():
     L.flce_read_device_status.restype = ctypes.c_int
     L.flce_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
     L.flce_selftest_timeout.restype = ctypes.c_int
+    L.flce_profile_enable.argtypes = [ctypes.c_int]
+    L.flce_profile_enable.restype = ctypes.c_int
+    L.flce_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
+                                    ctypes.POINTER(ctypes.c_double)]
+    L.flce_profile_read.restype = ctypes.c_int
     L.flce_status_string.argtypes = [ctypes.c_int]
     L.flce_status_string.restype = ctypes.c_char_p
     _LIB = L
@@ -198,6 +205,20 @@ def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
 def read_device_status(ws, stream=None) -> int:
     """Synchronises the stream and returns (and clears) the workspace's status word."""
     return int(lib().flce_read_device_status(ctypes.c_void_p(ws.data_ptr()), _stream_ptr(stream)))
+
+
+def profile_enable(on: bool = True) -> None:
+    _call("flce_profile_enable", lib().flce_profile_enable(1 if on else 0))
+
+
+def profile_read() -> dict:
+    """{kind: (launches, total_ms, flops)} for the launches recorded since profile_enable."""
+    out = {}
+    for k, name in enumerate(KERNEL_KINDS):
+        n, ms, fl = ctypes.c_int64(), ctypes.c_double(), ctypes.c_double()
+        _call("flce_profile_read", lib().flce_profile_read(k, ctypes.byref(n), ctypes.byref(ms), ctypes.byref(fl)))
+        out[name] = (int(n.value), float(ms.value), float(fl.value))
+    return out
 
 
 class _LinearCrossEntropy:

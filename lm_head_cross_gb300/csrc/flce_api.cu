@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <mutex>
+#include <vector>
 
 #include "../../include/flce.h"
 #include "flce_internal.h"
@@ -195,6 +196,93 @@ struct Ctx {
 
 flce_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
 
+// ----------------------------------------------------------------------------- diagnostics: per-launch timing
+
+constexpr int kKinds = 4;  // forward, logits gradient, dX/dW contraction, small kernels
+
+struct ProfRecord {
+  int kind;
+  cudaEvent_t start, stop;
+  double flops;
+};
+
+struct Profiler {
+  std::mutex mu;
+  bool on = false;
+  std::vector<ProfRecord> records;
+  std::vector<cudaEvent_t> pool;
+  int64_t launches[kKinds] = {};
+  double ms[kKinds] = {};
+  double flops[kKinds] = {};
+
+  cudaEvent_t take() {
+    if (!pool.empty()) {
+      cudaEvent_t e = pool.back();
+      pool.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    return e;
+  }
+  // Synchronise recorded events, fold them into the totals, recycle them.
+  cudaError_t drain() {
+    cudaError_t err = cudaSuccess;
+    for (auto& r : records) {
+      float t = 0.f;
+      cudaError_t e = cudaEventSynchronize(r.stop);
+      if (e == cudaSuccess) e = cudaEventElapsedTime(&t, r.start, r.stop);
+      if (e != cudaSuccess) err = e;
+      launches[r.kind] += 1;
+      ms[r.kind] += t;
+      flops[r.kind] += r.flops;
+      pool.push_back(r.start);
+      pool.push_back(r.stop);
+    }
+    records.clear();
+    return err;
+  }
+  void clear() {
+    drain();
+    for (int k = 0; k < kKinds; ++k) {
+      launches[k] = 0;
+      ms[k] = 0.0;
+      flops[k] = 0.0;
+    }
+  }
+};
+
+Profiler& profiler() {
+  static Profiler p;
+  return p;
+}
+
+// Runs `launch` (which enqueues one kernel on `stream`), bracketed by two
+// events when profiling is on.
+template <typename F>
+cudaError_t timed(int kind, double flops, cudaStream_t stream, F&& launch) {
+  Profiler& P = profiler();
+  bool on;
+  {
+    std::lock_guard<std::mutex> lock(P.mu);
+    on = P.on;
+  }
+  if (!on) return launch();
+  cudaEvent_t a, b;
+  {
+    std::lock_guard<std::mutex> lock(P.mu);
+    a = P.take();
+    b = P.take();
+  }
+  if (!a || !b) return launch();
+  cudaEventRecord(a, stream);
+  cudaError_t e = launch();
+  cudaEventRecord(b, stream);
+  std::lock_guard<std::mutex> lock(P.mu);
+  P.records.push_back(ProfRecord{kind, a, b, flops});
+  return e;
+}
+
 flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes, flce_stream_t stream) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
@@ -236,13 +324,19 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.labels = labels;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = static_cast<int>(std::min<long long>(c.dev.sms, units));
-  flce_status_t st = cuda_status(launch_tc(kModeForward, maps, tp, grid, c.stream));
+  const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
+  flce_status_t st = cuda_status(
+      timed(0, flops, c.stream, [&] { return launch_tc(kModeForward, maps, tp, grid, c.stream); }));
   if (st != FLCE_OK) return st;
-  st = cuda_status(launch_fwd_finalize(tp.n, tp.v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels,
-                                       lse, c.blk_loss(), c.blk_valid(), c.status(), c.stream));
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_fwd_finalize(tp.n, tp.v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels, lse,
+                               c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+  }));
   if (st != FLCE_OK) return st;
-  return cuda_status(launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, grad_loss, loss,
-                                         c.n_valid(), c.scale(), c.stream));
+  return cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, grad_loss, loss, c.n_valid(),
+                               c.scale(), c.stream);
+  }));
 }
 
 // Backward given lse and the scale already in the workspace.
@@ -282,8 +376,10 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     gm.a2 = gm.b2 = gm.out2 = gm.a;  // unused in this mode
     tp.grad_n_tiles = (cw + kBN - 1) / kBN;
     const long long gtiles = static_cast<long long>(tp.row_tiles) * tp.grad_n_tiles;
-    flce_status_t st = cuda_status(
-        launch_tc(kModeGrad, gm, tp, static_cast<int>(std::min<long long>(c.dev.sms, gtiles)), c.stream));
+    const double gflops = 2.0 * static_cast<double>(p.n) * cw * static_cast<double>(p.h);
+    flce_status_t st = cuda_status(timed(1, gflops, c.stream, [&] {
+      return launch_tc(kModeGrad, gm, tp, static_cast<int>(std::min<long long>(c.dev.sms, gtiles)), c.stream);
+    }));
     if (st != FLCE_OK) return st;
 
     if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, kBK, kBM))
@@ -295,10 +391,12 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     tp.dx_tiles = tp.row_tiles * tp.h_tiles;
     tp.dx_accumulate = c0 > 0 ? 1 : 0;
     const long long btiles = static_cast<long long>(tp.dw_tiles) + tp.dx_tiles;
-    st = cuda_status(launch_tc(kModeBwd, bm, tp, static_cast<int>(std::min<long long>(c.dev.sms, btiles)), c.stream));
+    st = cuda_status(timed(2, 2.0 * gflops, c.stream, [&] {
+      return launch_tc(kModeBwd, bm, tp, static_cast<int>(std::min<long long>(c.dev.sms, btiles)), c.stream);
+    }));
     if (st != FLCE_OK) return st;
   }
-  return cuda_status(launch_convert_bf16(c.dx_acc(), dX, p.n * p.h, c.stream));
+  return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dX, p.n * p.h, c.stream); }));
 }
 
 }  // namespace
@@ -337,11 +435,15 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
   Ctx c;
   flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
-  st = cuda_status(launch_label_scan(static_cast<int>(p->n), static_cast<int>(p->v), p->ignore_index, labels,
-                                     c.blk_loss(), c.blk_valid(), c.status(), c.stream));
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_label_scan(static_cast<int>(p->n), static_cast<int>(p->v), p->ignore_index, labels, c.blk_loss(),
+                             c.blk_valid(), c.status(), c.stream);
+  }));
   if (st != FLCE_OK) return st;
-  st = cuda_status(launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction, grad_loss, nullptr,
-                                       c.n_valid(), c.scale(), c.stream));
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction, grad_loss, nullptr, c.n_valid(),
+                               c.scale(), c.stream);
+  }));
   if (st != FLCE_OK) return st;
   return run_backward(c, X, W, labels, lse, dX, dW);
 }
@@ -377,6 +479,25 @@ flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns
   if (limit_ns == 0 || limit_ns > 10000000000ull) return FLCE_ERR_INVALID_ARGUMENT;
   if (cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FLCE_ERR_CUDA;
   return cuda_status(launch_timeout_selftest(static_cast<int*>(ws), limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+flce_status_t flce_profile_enable(int on) {
+  Profiler& P = profiler();
+  std::lock_guard<std::mutex> lock(P.mu);
+  P.clear();
+  P.on = on != 0;
+  return FLCE_OK;
+}
+
+flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, double* flops) {
+  if (kind < 0 || kind >= kKinds || !launches || !total_ms || !flops) return FLCE_ERR_INVALID_ARGUMENT;
+  Profiler& P = profiler();
+  std::lock_guard<std::mutex> lock(P.mu);
+  const cudaError_t e = P.drain();
+  *launches = P.launches[kind];
+  *total_ms = P.ms[kind];
+  *flops = P.flops[kind];
+  return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }
 
 const char* flce_status_string(flce_status_t s) {
