@@ -62,7 +62,8 @@ typedef enum {
   FLCE_ERR_LABEL_OUT_OF_RANGE = 5,  /* device: some label not in [0,V) and not ignore_index */
   FLCE_ERR_TIMEOUT = 6,             /* device: a bounded pipeline wait gave up (no hang, no trap) */
   FLCE_ERR_CUDA = 7,                /* a CUDA runtime/driver call failed, or no sm_100-family GPU */
-  FLCE_ERR_NO_DEVICE_STATUS = 8     /* flce_read_device_status could not read the word */
+  FLCE_ERR_NO_DEVICE_STATUS = 8,    /* flce_read_device_status could not read the word */
+  FLCE_ERR_EXCEEDS_STATIC_SCRATCH = 9 /* flce_forward_noalloc: n above its fixed maximum */
 } flce_status_t;
 
 typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction_t;
@@ -122,6 +123,26 @@ flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns
  * workspace. */
 flce_status_t flce_profile_enable(int on);
 flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, double* flops);
+
+/* Forward pass that allocates nothing and takes no workspace.  The pages have
+ * no counterpart; it exists for callers that cannot allocate device memory —
+ * code embedded in another runtime that owns all device allocations and hands
+ * over only input and output buffers, or latency-critical loops where a
+ * cudaMalloc/cudaFree would synchronise the device.  Same arguments and
+ * results as flce_forward, minus ws/ws_bytes.
+ *   - Scratch: one fixed array of about 4.3 MiB in the library's own device
+ *     memory, held by every GPU that loads the library until the process exits.
+ *   - Limit: n <= 32768 rows (FLCE_ERR_EXCEEDS_STATIC_SCRATCH above that);
+ *     h and v as for the other calls.
+ *   - The first call on each device looks up the array's device address (with
+ *     that device current); make that first call before any stream capture.
+ *   - All calls share the one array: calls whose work overlaps on the GPU
+ *     (different streams, or different host threads without ordering) race
+ *     and give wrong results.  Order them on one stream.
+ *   - Errors found on the device (a label outside [0,V), a bounded wait that
+ *     ran out) set *loss to NaN; there is no status word to read. */
+flce_status_t flce_forward_noalloc(const flce_problem_t* p, const void* X, const void* W,
+                                   const int32_t* labels, float* loss, float* lse, flce_stream_t stream);
 
 /* Static description of a status code. */
 const char* flce_status_string(flce_status_t s);

@@ -20,7 +20,7 @@ REDUCTIONS = {"mean": 0, "sum": 1}
 
 EXPORTED = ("flce_workspace_bytes", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
-            "flce_status_string")
+            "flce_forward_noalloc", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 

@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libflce.so")
 BUILD_DIR = os.path.join(HERE, "_build")
-SOURCES = ["flce_kernels.cu", "flce_api.cu"]
+SOURCES = ["flce_kernels.cu", "flce_api.cu", "flce_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -511,6 +511,7 @@ const char* flce_status_string(flce_status_t s) {
     case FLCE_ERR_TIMEOUT: return "a bounded device wait timed out";
     case FLCE_ERR_CUDA: return "CUDA error or unsupported device";
     case FLCE_ERR_NO_DEVICE_STATUS: return "could not read the device status word";
+    case FLCE_ERR_EXCEEDS_STATIC_SCRATCH: return "n exceeds the fixed scratch of flce_forward_noalloc (32768 rows)";
     default: return "unknown status";
   }
 }

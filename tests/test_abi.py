@@ -27,7 +27,7 @@ def test_library_exports_every_declared_symbol():
 
 
 def test_status_strings():
-    for code in range(0, 9):
+    for code in range(0, 10):
         assert flce.status_string(code)
 
 
