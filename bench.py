@@ -78,6 +78,26 @@ def credited_flops(n, h, v):
     return 6.0 * n * h * v
 
 
+def rank_seed(base_seed, rank):
+    """Each rank draws its own batch of the workload's shape (rows shard by rank)."""
+    return base_seed + 1000 * rank
+
+
+def max_over_ranks(value, dist, device):
+    """The slowest rank's time decides the whole job's time."""
+    if dist is None:
+        return float(value)
+    import torch
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_tflops(world, flops_per_rank_step, steps, max_ms):
+    """Whole-job throughput: every rank's credited flops over the slowest rank's time."""
+    return world * flops_per_rank_step * steps / (max_ms / 1e3) / 1e12
+
+
 # ----------------------------------------------------------------------------- CPU oracle timing
 
 def oracle_sample_seconds(problem, rows):
@@ -162,7 +182,7 @@ class ClockSampler:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
 
@@ -225,7 +245,7 @@ def run_flce(args, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
 
     c = dict(synth.CONFIGS[args.config])
-    c["seed"] = c["seed"] + 1000 * rank          # each rank: its own batch of the same shape
+    c["seed"] = rank_seed(c["seed"], rank)
     problem = synth.make_problem(**c)
     n, h, v = problem.n, problem.h, problem.v
     X = torch.from_numpy(problem.X.view(np.int16)).view(torch.bfloat16).to(dev)
@@ -281,14 +301,10 @@ def run_flce(args, rank, world, local_rank):
     prof = flce.profile_read()
     flce.profile_enable(False)
     step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    total_ms = sum(step_ms)
-    if dist is not None:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     flops = credited_flops(n, h, v)
-    value = world * flops * args.steps / (total_ms / 1e3) / 1e12
+    value = job_tflops(world, flops, args.steps, total_ms)
 
     # end to end through the public call with host buffers: H2D inputs, fwd_bwd, D2H outputs
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
@@ -316,11 +332,7 @@ def run_flce(args, rank, world, local_rank):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
-    if dist is not None:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
     d2h = sum(t.numel() * t.element_size() for t in out)
 
@@ -350,6 +362,7 @@ def run_flce(args, rank, world, local_rank):
         "materialised_logits_bytes": {"bf16": flce.logits_footprint_bytes(n, v, 2),
                                       "fp32": flce.logits_footprint_bytes(n, v, 4)},
         "wall_ms_per_step_incl_flush": 1e3 * t_wall / args.steps,
+        "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "peak_note": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
                                                            f"long loop); of burst {peak_burst}: {achieved / peak_burst:.3f}",
@@ -357,7 +370,7 @@ def run_flce(args, rank, world, local_rank):
         "kernels": kinds,
         "gpu_launches": gpu_launches,
         "clocks": clk,
-        "e2e": {"value": world * flops * args.e2e_steps / (e2e_ms / 1e3) / 1e12, "unit": UNIT,
+        "e2e": {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "flce_fwd_bwd through the C-ABI with pinned host inputs copied in and loss/lse/dX/dW "
                         "copied out every step"},
