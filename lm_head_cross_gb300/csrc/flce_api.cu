@@ -24,6 +24,7 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 // Workspace layout (byte offsets from ws, each 256-byte aligned).
 struct Layout {
   size_t status, n_valid, scale;  // header words
+  size_t counter;                 // tile counter of the dynamically scheduled launches
   size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
   size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
   size_t g;                       // backward: one vocabulary chunk of G, bf16 [N, chunk]
@@ -41,6 +42,7 @@ Layout make_layout(const flce_problem_t& p) {
   L.status = off;
   L.n_valid = off + 4;
   L.scale = off + 8;
+  L.counter = off + 16;
   off += kAlign;
   L.blk_loss = off;
   off = align_up(off + sizeof(double) * L.nblk);
@@ -185,6 +187,7 @@ struct Ctx {
   int* status() const { return reinterpret_cast<int*>(ws + L.status); }
   int* n_valid() const { return reinterpret_cast<int*>(ws + L.n_valid); }
   float* scale() const { return reinterpret_cast<float*>(ws + L.scale); }
+  int* counter() const { return reinterpret_cast<int*>(ws + L.counter); }
   double* blk_loss() const { return reinterpret_cast<double*>(ws + L.blk_loss); }
   int* blk_valid() const { return reinterpret_cast<int*>(ws + L.blk_valid); }
   float* part_m() const { return reinterpret_cast<float*>(ws + L.part_m); }
@@ -390,6 +393,9 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     tp.dw_tiles = tp.dw_m_tiles * tp.h_tiles;
     tp.dx_tiles = tp.row_tiles * tp.h_tiles;
     tp.dx_accumulate = c0 > 0 ? 1 : 0;
+    tp.tile_counter = c.counter();
+    st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
+    if (st != FLCE_OK) return st;
     const long long btiles = static_cast<long long>(tp.dw_tiles) + tp.dx_tiles;
     st = cuda_status(timed(2, 2.0 * gflops, c.stream, [&] {
       return launch_tc(kModeBwd, bm, tp, static_cast<int>(std::min<long long>(c.dev.sms, btiles)), c.stream);

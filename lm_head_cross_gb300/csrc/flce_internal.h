@@ -46,6 +46,7 @@ struct TcParams {
   int h_tiles;          // ceil(h / kBN)
   int dw_m_tiles;       // ceil(cw / kBM)
   int dx_accumulate;    // 0: first chunk stores, 1: later chunks add
+  int* tile_counter;    // bwd: global tile counter, zero at launch
 };
 
 struct TcMaps {

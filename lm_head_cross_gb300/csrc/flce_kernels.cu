@@ -41,7 +41,7 @@ constexpr int kStagingPerWarp = 2 * kStagingBuf;
 constexpr int kSmemStages = kStages * kStageBytes;
 constexpr int kSmemStagingOff = kSmemStages;
 constexpr int kSmemBarOff = kSmemStagingOff + 4 * kStagingPerWarp;
-constexpr int kSmemBytes = kSmemBarOff + 256 + 1024;  // barriers, slot, flag; 1 KiB alignment slack
+constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;  // barriers, ring, slot, flag; 1 KiB alignment slack
 constexpr uint32_t kTmemCols = 2 * kBN;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
@@ -57,7 +57,22 @@ struct Sched {
   int unit, rt, sp, vt, ve;  // forward
   int t;                     // grad / bwd
   bool done;
+  // bwd: tiles handed out by a global counter; the producer publishes each
+  // tile index into a shared-memory ring that the MMA and epilogue warps read.
+  int ridx;
+  uint32_t rphase;
 };
+
+constexpr int kRing = 8;
+
+struct TileRing {
+  volatile int* slot;  // [kRing]
+  uint64_t* full;      // [kRing], one arrival (producer)
+  uint64_t* empty;     // [kRing], five arrivals (MMA thread + 4 epilogue warps)
+};
+
+template <int MODE>
+constexpr bool kDynamic = (MODE == kModeBwd);
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -143,13 +158,55 @@ __device__ __forceinline__ void record_timeout(const TcParams& p, volatile int* 
   atomicCAS(p.status, 0, kErrTimeout);
 }
 
+// Producer side of the dynamic schedule: publish tile index `t` (a value past
+// the last tile tells the readers to stop).
+__device__ __forceinline__ bool ring_publish(const TcParams& p, TileRing& ring, Sched& s, int t,
+                                             volatile int* abort_flag) {
+  if (!mbar_wait(&ring.empty[s.ridx], s.rphase ^ 1u, p.timeout_ns, abort_flag)) return false;
+  ring.slot[s.ridx] = t;
+  mbar_arrive(&ring.full[s.ridx]);
+  if (++s.ridx == kRing) {
+    s.ridx = 0;
+    s.rphase ^= 1u;
+  }
+  return true;
+}
+
+// Reader side: the next published tile index.  `arrive` is true for the one
+// thread per reader group that releases the slot.
+template <bool WHOLE_WARP>
+__device__ __forceinline__ bool ring_read(const TcParams& p, TileRing& ring, Sched& s, bool arrive,
+                                          volatile int* abort_flag) {
+  if (!mbar_wait(&ring.full[s.ridx], s.rphase, p.timeout_ns, abort_flag)) return false;
+  s.t = ring.slot[s.ridx];
+  if (WHOLE_WARP) __syncwarp();  // every lane has read the slot before it is released
+  if (arrive) mbar_arrive(&ring.empty[s.ridx]);
+  if (++s.ridx == kRing) {
+    s.ridx = 0;
+    s.rphase ^= 1u;
+  }
+  return true;
+}
+
+// Next tile index for the producer: its first tile is its block index, the
+// rest come from the global counter in the order the tiles are listed.
+__device__ __forceinline__ int dynamic_next_index(const TcParams& p) {
+  return static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+}
+
 // ----------------------------------------------------------------------------- producer (TMA)
 
 template <int MODE>
 __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                             volatile int* abort_flag) {
+                             TileRing ring, volatile int* abort_flag) {
   Sched s;
   sched_init<MODE>(p, s);
+  s.ridx = 0;
+  s.rphase = 0;
+  if (kDynamic<MODE> && !ring_publish(p, ring, s, s.t, abort_flag)) {
+    record_timeout(p, abort_flag);
+    return;
+  }
   Tile t;
   int stage = 0;
   uint32_t phase = 0;
@@ -183,7 +240,15 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* sme
         phase ^= 1u;
       }
     }
-    sched_next<MODE>(p, s);
+    if (kDynamic<MODE>) {
+      s.t = dynamic_next_index(p);
+      if (!ring_publish(p, ring, s, s.t, abort_flag)) {
+        record_timeout(p, abort_flag);
+        return;
+      }
+    } else {
+      sched_next<MODE>(p, s);
+    }
   }
 }
 
@@ -191,9 +256,15 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* sme
 
 template <int MODE>
 __device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* tfull,
-                        uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
+                        uint64_t* tempty, uint32_t tmem_base, TileRing ring, volatile int* abort_flag) {
   Sched s;
   sched_init<MODE>(p, s);
+  s.ridx = 0;
+  s.rphase = 0;
+  if (kDynamic<MODE> && !ring_read<false>(p, ring, s, true, abort_flag)) {
+    record_timeout(p, abort_flag);
+    return;
+  }
   Tile t;
   int stage = 0;
   uint32_t phase = 0;
@@ -232,7 +303,14 @@ __device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64
     umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
-    sched_next<MODE>(p, s);
+    if (kDynamic<MODE>) {
+      if (!ring_read<false>(p, ring, s, true, abort_flag)) {
+        record_timeout(p, abort_flag);
+        return;
+      }
+    } else {
+      sched_next<MODE>(p, s);
+    }
   }
 }
 
@@ -277,7 +355,7 @@ __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int la
 
 template <int MODE>
 __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* staging, uint64_t* tfull,
-                             uint64_t* tempty, uint32_t tmem_base, volatile int* abort_flag) {
+                             uint64_t* tempty, uint32_t tmem_base, TileRing ring, volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // a warp may only touch TMEM lanes [32*(warp%4), +32)
@@ -287,6 +365,12 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
 
   Sched s;
   sched_init<MODE>(p, s);
+  s.ridx = 0;
+  s.rphase = 0;
+  if (kDynamic<MODE> && !ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
+    record_timeout(p, abort_flag);
+    return;
+  }
   Tile t;
   int acc = 0;
   uint32_t acc_phase = 0;
@@ -407,7 +491,14 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
     }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
-    sched_next<MODE>(p, s);
+    if (kDynamic<MODE>) {
+      if (!ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
+        record_timeout(p, abort_flag);
+        break;
+      }
+    } else {
+      sched_next<MODE>(p, s);
+    }
   }
   if (lane == 0) bulk_wait_group_all();
   __syncwarp();
@@ -426,6 +517,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   uint64_t* tempty = bars + 2 * kStages + 2;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 5);
+  TileRing ring;
+  ring.full = bars + 2 * kStages + 6;
+  ring.empty = ring.full + kRing;
+  ring.slot = reinterpret_cast<volatile int*>(ring.empty + kRing);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -438,6 +533,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+    }
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(&ring.full[i], 1);
+      mbar_init(&ring.empty[i], 5);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -461,11 +560,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<MODE>(maps, p, smem, full, empty, abort_flag);
+    if (lane == 0) run_producer<MODE>(maps, p, smem, full, empty, ring, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<MODE>(p, smem, full, empty, tfull, tempty, tmem_base, abort_flag);
+    if (lane == 0) run_mma<MODE>(p, smem, full, empty, tfull, tempty, tmem_base, ring, abort_flag);
   } else {
-    run_epilogue<MODE>(maps, p, smem + kSmemStagingOff, tfull, tempty, tmem_base, abort_flag);
+    run_epilogue<MODE>(maps, p, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, abort_flag);
   }
 
   tc_fence_before_sync();
