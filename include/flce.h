@@ -24,10 +24,12 @@
  *   - X, W, dX, dW are bf16, dense row-major, H contiguous.  labels is int32.
  *     loss, lse, grad_loss are fp32.  All data pointers are DEVICE pointers
  *     owned by the caller; the library never allocates or frees memory.
- *   - ws / ws_bytes: caller-owned device workspace of at least
- *     flce_workspace_bytes(p) bytes, 256-byte aligned.  It is the only extra
- *     device memory the library touches.  Its size grows with N and H but not
- *     with V.  Calls that share a workspace must be ordered on one stream.
+ *   - ws / ws_bytes: caller-owned device workspace, 256-byte aligned, of at
+ *     least flce_workspace_bytes_min(p) bytes (grows with N and H, not with V);
+ *     flce_workspace_bytes(p) bytes (also holds a bounded row chunk of the
+ *     vocabulary gradient and an fp32 dW accumulator) lets flce_fwd_bwd take its
+ *     faster fused path.  It is the only extra device memory the library
+ *     touches.  Calls that share a workspace must be ordered on one stream.
  *   - Requirements: n >= 1, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
  *     the tensor-memory-access engine), X / W / dX / dW 16-byte aligned,
  *     labels / lse 4-byte aligned.  Violations return an error and launch
@@ -76,11 +78,19 @@ typedef struct {
   int32_t reduction;     /* flce_reduction_t */
 } flce_problem_t;
 
-/* Workspace size in bytes for every call below on problem p (0 if p is invalid).
- * Holds the device status word, per-row partial (max, sum) pairs, target
- * logits, one vocabulary chunk of bf16 G (N x C, C a fixed chunk width) and an
- * fp32 accumulator for dX (N x H).  Independent of V. */
+/* Workspace size in bytes with which every call below takes its fastest path
+ * (0 if p is invalid): the minimum size plus room for flce_fwd_bwd's fused path,
+ * i.e. a chunk of R rows of the bf16 vocabulary gradient (R x V, at most 1 GiB,
+ * at least two chunks once N > 256), one fp32 per (chunk row, 256-wide
+ * vocabulary tile) and an fp32 dW accumulator (V x H). */
 size_t flce_workspace_bytes(const flce_problem_t* p);
+
+/* Smallest workspace every call below accepts (0 if p is invalid): the device
+ * status word, per-row partial (max, sum) pairs, target logits, one vocabulary
+ * chunk of bf16 G (N x C, C a fixed chunk width) and an fp32 dX accumulator
+ * (N x H).  Independent of V.  With it, flce_fwd_bwd recomputes the logits in
+ * the backward pass instead of keeping them for a row chunk. */
+size_t flce_workspace_bytes_min(const flce_problem_t* p);
 
 /* Forward ("What-Each-Parallelism-Actually-Shards" §7.4: online log-sum-exp over
  * vocabulary tiles, target logit only).  Writes *loss (device fp32 scalar) and
@@ -96,7 +106,13 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
                             const int32_t* labels, const float* lse, const float* grad_loss,
                             void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
 
-/* Forward then backward with g = 1: loss, lse, dX, dW in one call. */
+/* Forward then backward with g = 1: loss, lse, dX, dW in one call.  With
+ * ws_bytes >= flce_workspace_bytes(p) it runs fused over row chunks (the logits
+ * are computed once: forward ("What-Each-Parallelism-Actually-Shards" §7.4,
+ * chunked CE) keeps each chunk's tile-max-scaled softmax in bf16, a fix-up turns it
+ * into G once the chunk's lse is known, then dX and dW are contracted from it);
+ * with less (but at least flce_workspace_bytes_min(p)) it runs flce_forward then
+ * flce_backward (logits recomputed, bounded V-independent workspace). */
 flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W,
                            const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
                            void* ws, size_t ws_bytes, flce_stream_t stream);

@@ -18,7 +18,7 @@ FLCE_ERR_LABEL_OUT_OF_RANGE = 5
 FLCE_ERR_TIMEOUT = 6
 REDUCTIONS = {"mean": 0, "sum": 1}
 
-EXPORTED = ("flce_workspace_bytes", "flce_forward", "flce_backward", "flce_fwd_bwd",
+EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
             "flce_forward_noalloc", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
@@ -54,6 +54,10 @@ def lib():
     P = ctypes.POINTER(Problem)
     L.flce_workspace_bytes.argtypes = [P]
     L.flce_workspace_bytes.restype = sz
+    L.flce_workspace_bytes_min.argtypes = [P]
+    L.flce_workspace_bytes_min.restype = sz
+    L.flce_forward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp]
+    L.flce_forward_noalloc.restype = ctypes.c_int
     L.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_forward.restype = ctypes.c_int
     L.flce_backward.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -91,8 +95,15 @@ def _problem(n, h, v, ignore_index, reduction) -> Problem:
 
 
 def workspace_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
+    """Workspace for the fastest path of every call (fused flce_fwd_bwd)."""
     p = _problem(n, h, v, ignore_index, reduction)
     return int(lib().flce_workspace_bytes(ctypes.byref(p)))
+
+
+def workspace_bytes_min(n, h, v, ignore_index=-100, reduction="mean") -> int:
+    """Smallest workspace every call accepts (independent of V)."""
+    p = _problem(n, h, v, ignore_index, reduction)
+    return int(lib().flce_workspace_bytes_min(ctypes.byref(p)))
 
 
 def _torch():
@@ -122,9 +133,9 @@ def _check_inputs(x, w, labels):
         raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}, labels {tuple(labels.shape)}")
 
 
-def _alloc_ws(n, h, v, ignore_index, reduction, device):
+def _alloc_ws(n, h, v, ignore_index, reduction, device, minimal=False):
     torch = _torch()
-    nbytes = workspace_bytes(n, h, v, ignore_index, reduction)
+    nbytes = (workspace_bytes_min if minimal else workspace_bytes)(n, h, v, ignore_index, reduction)
     if nbytes == 0:
         raise FlceError(1, "workspace_bytes")
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -180,15 +191,17 @@ def backward(x, w, labels, lse, grad_loss=None, ignore_index=-100, reduction="me
     return dX, dW, ws
 
 
-def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, out=None, check=False):
-    """Returns (loss, lse, dX, dW, ws).  ``out`` may pass preallocated (loss, lse, dX, dW)."""
+def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, out=None, check=False,
+            minimal_workspace=False):
+    """Returns (loss, lse, dX, dW, ws).  ``out`` may pass preallocated (loss, lse, dX, dW).
+    ``minimal_workspace`` allocates flce_workspace_bytes_min (the recompute path)."""
     torch = _torch()
     _check_inputs(x, w, labels)
     n, h = x.shape
     v = w.shape[0]
     p = _problem(n, h, v, ignore_index, reduction)
     if ws is None:
-        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
+        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device, minimal=minimal_workspace)
     if out is None:
         out = (torch.empty(1, dtype=torch.float32, device=x.device), torch.empty(n, dtype=torch.float32, device=x.device),
                torch.empty_like(x), torch.empty_like(w))

@@ -27,17 +27,36 @@ struct Layout {
   size_t counter;                 // tile counter of the dynamically scheduled launches
   size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
   size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
-  size_t g;                       // backward: one vocabulary chunk of G, bf16 [N, chunk]
-  size_t dx_acc;                  // backward: fp32 dX accumulator [N, H]
+  size_t g;                       // one chunk buffer: recompute path G [N, chunk]; fused path p~/G [rows, Vp]
+  size_t dx_acc;                  // fp32 accumulator: recompute path dX [N, H]; fused path dW [V, H]
+  size_t mtile;                   // fused path: per (chunk row, vocabulary tile) max
   size_t total;
   int nblk, chunk;
+  int rows;                       // fused path: rows per chunk (0: layout without the fused path)
+  int64_t vp;                     // fused path: row pitch of the chunk buffer (V rounded up to 8)
 };
 
-Layout make_layout(const flce_problem_t& p) {
+// Rows per chunk of the fused path: the p~/G buffer [rows, V] stays within
+// kFusedChunkBytes, there are at least two chunks once N > 256, and rows is a
+// multiple of 256 (the finalize block size).
+constexpr size_t kFusedChunkBytes = size_t{1} << 30;
+
+int fused_rows(int64_t n, int64_t v) {
+  const int64_t vp = (v + 7) / 8 * 8;
+  int64_t rows = static_cast<int64_t>(kFusedChunkBytes / (2 * static_cast<size_t>(vp))) / 256 * 256;
+  const int64_t half = ((n + 1) / 2 + 255) / 256 * 256;
+  rows = std::min(rows, std::max<int64_t>(256, half));
+  return static_cast<int>(std::max<int64_t>(256, rows));
+}
+
+Layout make_layout(const flce_problem_t& p, bool fused) {
   Layout L{};
-  const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h);
+  const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
   L.nblk = static_cast<int>((p.n + kFinalizeThreads - 1) / kFinalizeThreads);
   L.chunk = chunk_width(p.n);
+  L.rows = fused ? fused_rows(p.n, p.v) : 0;
+  L.vp = (p.v + 7) / 8 * 8;
+  const size_t vtiles = (v + kBN - 1) / kBN;
   size_t off = 0;
   L.status = off;
   L.n_valid = off + 4;
@@ -55,9 +74,15 @@ Layout make_layout(const flce_problem_t& p) {
   L.tgt = off;
   off = align_up(off + sizeof(float) * n);
   L.g = off;
-  off = align_up(off + 2 * n * static_cast<size_t>(L.chunk));
+  size_t gbytes = 2 * n * static_cast<size_t>(L.chunk);
+  if (fused) gbytes = std::max(gbytes, 2 * static_cast<size_t>(L.rows) * static_cast<size_t>(L.vp));
+  off = align_up(off + gbytes);
   L.dx_acc = off;
-  off = align_up(off + 4 * n * h);
+  size_t accbytes = 4 * n * h;
+  if (fused) accbytes = std::max(accbytes, 4 * v * h);
+  off = align_up(off + accbytes);
+  L.mtile = off;
+  if (fused) off = align_up(off + sizeof(float) * static_cast<size_t>(L.rows) * vtiles);
   L.total = off;
   return L;
 }
@@ -195,6 +220,7 @@ struct Ctx {
   float* tgt() const { return reinterpret_cast<float*>(ws + L.tgt); }
   void* g() const { return ws + L.g; }
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
+  float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
 };
 
 flce_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
@@ -292,8 +318,10 @@ flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes
   if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
   c->p = p;
-  c->L = make_layout(*p);
+  c->L = make_layout(*p, false);
   if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  const Layout full = make_layout(*p, true);
+  if (ws_bytes >= full.total) c->L = full;  // room for the fused path
   c->ws = static_cast<uint8_t*>(ws);
   c->stream = reinterpret_cast<cudaStream_t>(stream);
   st = device_info(&c->dev);
@@ -325,6 +353,8 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
   tp.labels = labels;
+  tp.r0 = 0;
+  tp.row_end = tp.n;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = static_cast<int>(std::min<long long>(c.dev.sms, units));
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
@@ -392,7 +422,11 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     tp.dw_m_tiles = (cw + kBM - 1) / kBM;
     tp.dw_tiles = tp.dw_m_tiles * tp.h_tiles;
     tp.dx_tiles = tp.row_tiles * tp.h_tiles;
-    tp.dx_accumulate = c0 > 0 ? 1 : 0;
+    tp.dx_out = c0 > 0 ? kOutF32Add : kOutF32Store;
+    tp.dw_out = kOutBF16;
+    tp.dx_k = cw;
+    tp.dw_k = tp.n;
+    tp.dx_first = 0;
     tp.tile_counter = c.counter();
     st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
     if (st != FLCE_OK) return st;
@@ -403,6 +437,111 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     if (st != FLCE_OK) return st;
   }
   return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dX, p.n * p.h, c.stream); }));
+}
+
+// Fused forward + backward over row chunks (6NHV executed, no recompute):
+// per chunk, the forward-store pass writes p~ = 2^(S - tile max) and the
+// chunk's lse; the fix-up turns p~ into G in place; one launch then computes
+// dX for the chunk's rows (K = V, bf16 out) and adds G^T X into the fp32 dW
+// accumulator (K = chunk rows).
+flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
+                        void* dX, void* dW) {
+  const flce_problem_t& p = *c.p;
+  const int n = static_cast<int>(p.n), h = static_cast<int>(p.h), v = static_cast<int>(p.v);
+  const int vtiles = (v + kBN - 1) / kBN;
+  const int h_tiles = (h + kBN - 1) / kBN;
+  flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_label_scan(n, v, p.ignore_index, labels, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, nullptr, c.n_valid(),
+                               c.scale(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+
+  TcMaps fm;  // forward-store: X, W K-major; p~ store
+  if (!make_map(&fm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
+  if (!make_map(&fm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  TcMaps bm;  // bwd: G K-major (dX A), W MN-major (dX B), dX bf16 out; G MN-major (dW A), X MN-major (dW B), dW fp32
+  if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.out2, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
+  const uint64_t pitch = static_cast<uint64_t>(c.L.vp) * 2;
+
+  for (int r0 = 0; r0 < n; r0 += c.L.rows) {
+    const int cr = std::min(c.L.rows, n - r0);
+    if (!make_map(&fm.out, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, 64, 32)) return FLCE_ERR_CUDA;
+    fm.a2 = fm.b2 = fm.out2 = fm.a;  // unused in this mode
+    TcParams tp{};
+    tp.n = n;
+    tp.h = h;
+    tp.v = v;
+    tp.ignore_index = p.ignore_index;
+    tp.timeout_ns = timeout_ns();
+    tp.status = c.status();
+    tp.labels = labels;
+    tp.r0 = r0;
+    tp.row_end = r0 + cr;
+    tp.row_tiles = (cr + kBM - 1) / kBM;
+    tp.vocab_tiles = vtiles;
+    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms);
+    tp.part_m = c.part_m();
+    tp.part_l = c.part_l();
+    tp.tgt = c.tgt();
+    tp.mtile = c.mtile();
+    const double fflops = 2.0 * cr * static_cast<double>(v) * h;
+    const int fgrid = static_cast<int>(std::min<long long>(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit));
+    st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
+    if (st != FLCE_OK) return st;
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels,
+                                      lse, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, p.ignore_index, lse, labels, c.scale(),
+                          c.mtile(), c.g(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
+
+    if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, kBK, kBM)) return FLCE_ERR_CUDA;
+    if (!make_map(&bm.a2, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, 64, kBK)) return FLCE_ERR_CUDA;
+    TcParams bp{};
+    bp.n = n;
+    bp.h = h;
+    bp.v = v;
+    bp.ignore_index = p.ignore_index;
+    bp.timeout_ns = timeout_ns();
+    bp.status = c.status();
+    bp.r0 = r0;
+    bp.row_end = r0 + cr;
+    bp.c0 = 0;
+    bp.cw = v;
+    bp.h_tiles = h_tiles;
+    bp.dx_tiles = ((cr + kBM - 1) / kBM) * h_tiles;
+    bp.dw_tiles = ((v + kBM - 1) / kBM) * h_tiles;
+    bp.dx_k = v;
+    bp.dw_k = cr;
+    bp.dx_first = 1;
+    bp.dx_out = kOutBF16;
+    bp.dw_out = r0 == 0 ? kOutF32Store : kOutF32Add;
+    bp.tile_counter = c.counter();
+    st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
+    if (st != FLCE_OK) return st;
+    const long long btiles = static_cast<long long>(bp.dx_tiles) + bp.dw_tiles;
+    const int bgrid = static_cast<int>(std::min<long long>(c.dev.sms, btiles));
+    st = cuda_status(
+        timed(2, 2.0 * fflops, c.stream, [&] { return launch_tc(kModeBwd, bm, bp, bgrid, c.stream); }));
+    if (st != FLCE_OK) return st;
+  }
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, loss, c.n_valid(),
+                               c.scale(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dW, p.v * p.h, c.stream); }));
 }
 
 }  // namespace
@@ -417,7 +556,12 @@ extern "C" {
 
 size_t flce_workspace_bytes(const flce_problem_t* p) {
   if (check_problem(p) != FLCE_OK) return 0;
-  return make_layout(*p).total;
+  return make_layout(*p, true).total;
+}
+
+size_t flce_workspace_bytes_min(const flce_problem_t* p) {
+  if (check_problem(p) != FLCE_OK) return 0;
+  return make_layout(*p, false).total;
 }
 
 flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
@@ -463,6 +607,7 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   Ctx c;
   flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
+  if (c.L.rows > 0) return run_fused(c, X, W, labels, loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
   if (st != FLCE_OK) return st;
   return run_backward(c, X, W, labels, lse, dX, dW);

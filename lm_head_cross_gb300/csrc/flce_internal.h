@@ -22,7 +22,10 @@ constexpr int kMaxSplit = 32;  // most vocabulary splits of the forward pass
 // workspace holds one chunk of G, N x chunk bf16.
 int chunk_width(int64_t n);
 
-enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2 };
+enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3 };
+
+// Output format of the dX / dW tiles of a kModeBwd launch.
+enum OutMode : int { kOutF32Store = 0, kOutF32Add = 1, kOutBF16 = 2 };
 
 // Everything a tensor-core launch needs besides its tensor maps.
 struct TcParams {
@@ -45,8 +48,13 @@ struct TcParams {
   int dx_tiles, dw_tiles;
   int h_tiles;          // ceil(h / kBN)
   int dw_m_tiles;       // ceil(cw / kBM)
-  int dx_accumulate;    // 0: first chunk stores, 1: later chunks add
+  int dx_out, dw_out;   // OutMode of the dX and dW tiles
+  int dx_k, dw_k;       // K extents: dX tiles run over dx_k vocabulary ids, dW tiles over dw_k rows
+  int dx_first;         // 1: dX tiles are listed first (they are the long ones)
   int* tile_counter;    // bwd: global tile counter, zero at launch
+  // row chunk of the forward-store pass: rows [r0, row_end) (row_end 0 means n)
+  int r0, row_end;
+  float* mtile;         // forward-store: per (chunk row, vocabulary tile) max, log2 units
 };
 
 struct TcMaps {
@@ -63,6 +71,11 @@ cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid,
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m,
                                 const float* part_l, const float* tgt, const int32_t* labels, float* lse,
                                 double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
+cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, int ignore_index,
+                                     const float* part_m, const float* part_l, const float* tgt, const int32_t* labels,
+                                     float* lse, double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
+cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, int ignore_index, const float* lse,
+                         const int32_t* labels, const float* scale, const float* mtile, void* P, cudaStream_t stream);
 cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss,
                               int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,

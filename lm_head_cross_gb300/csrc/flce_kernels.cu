@@ -74,6 +74,9 @@ struct TileRing {
 template <int MODE>
 constexpr bool kDynamic = (MODE == kModeBwd);
 
+template <int MODE>
+constexpr bool kUnits = (MODE == kModeForward || MODE == kModeFwdStore);
+
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
@@ -91,7 +94,7 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
 template <int MODE>
 __device__ __forceinline__ void sched_init(const TcParams& p, Sched& s) {
   s.done = false;
-  if (MODE == kModeForward) {
+  if (kUnits<MODE>) {
     s.unit = blockIdx.x;
     fwd_unit_begin(p, s);
   } else {
@@ -101,13 +104,13 @@ __device__ __forceinline__ void sched_init(const TcParams& p, Sched& s) {
 
 template <int MODE>
 __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Tile& t) {
-  if (MODE == kModeForward) {
+  if (kUnits<MODE>) {
     if (s.done) return false;
     const int vb = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
-    t.m0 = s.rt * kBM;
+    t.m0 = s.rt * kBM;  // row inside the chunk [r0, row_end)
     t.n0 = s.vt * kBN;
     t.kblocks = ceil_div(p.h, kBK);
-    t.kind = 0;
+    t.kind = (MODE == kModeFwdStore) ? 4 : 0;
     t.first = (s.vt == vb);
     t.last = (s.vt == s.ve - 1);
     t.split = s.sp;
@@ -123,17 +126,17 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Til
     return true;
   } else {
     if (s.t >= p.dw_tiles + p.dx_tiles) return false;
-    if (s.t < p.dw_tiles) {  // dW tiles first: they are the long ones (K = N)
-      t.m0 = (s.t / p.h_tiles) * kBM;  // chunk-local vocabulary row
-      t.n0 = (s.t % p.h_tiles) * kBN;  // hidden column
-      t.kblocks = ceil_div(p.n, kBK);
-      t.kind = 3;
-    } else {
-      const int u = s.t - p.dw_tiles;
-      t.m0 = (u / p.h_tiles) * kBM;  // token row
-      t.n0 = (u % p.h_tiles) * kBN;  // hidden column
-      t.kblocks = ceil_div(p.cw, kBK);
+    // the long tiles come first (dW when K = N, dX when K = V)
+    const bool is_dx = p.dx_first ? (s.t < p.dx_tiles) : (s.t >= p.dw_tiles);
+    const int u = p.dx_first ? (is_dx ? s.t : s.t - p.dx_tiles) : (is_dx ? s.t - p.dw_tiles : s.t);
+    t.m0 = (u / p.h_tiles) * kBM;  // dX: row of the G buffer; dW: column (vocabulary id) of the G buffer
+    t.n0 = (u % p.h_tiles) * kBN;  // hidden column
+    if (is_dx) {
+      t.kblocks = ceil_div(p.dx_k, kBK);
       t.kind = 2;
+    } else {
+      t.kblocks = ceil_div(p.dw_k, kBK);
+      t.kind = 3;
     }
     t.first = t.last = 0;
     t.split = 0;
@@ -143,7 +146,7 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Til
 
 template <int MODE>
 __device__ __forceinline__ void sched_next(const TcParams& p, Sched& s) {
-  if (MODE == kModeForward) {
+  if (kUnits<MODE>) {
     if (++s.vt >= s.ve) {
       s.unit += gridDim.x;
       fwd_unit_begin(p, s);
@@ -221,9 +224,9 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* sme
       uint64_t* bar = &full[stage];
       mbar_arrive_expect_tx(bar, kStageBytes);
       const int k0 = kb * kBK;
-      if (t.kind <= 1) {  // A = X [N,H] K-major, B = W [V,H] K-major
+      if (t.kind <= 1 || t.kind == 4) {  // A = X [N,H] K-major, B = W [V,H] K-major
         const int vcol = (t.kind == 1) ? p.c0 + t.n0 : t.n0;
-        tma_load_2d(sa, &maps.a, bar, k0, t.m0);
+        tma_load_2d(sa, &maps.a, bar, k0, p.r0 + t.m0);
         tma_load_2d(sb, &maps.b, bar, k0, vcol);
       } else if (t.kind == 2) {  // dX: A = G [N, cw] K-major, B = W rows of the chunk, MN-major
         tma_load_2d(sa, &maps.a, bar, k0, t.m0);
@@ -233,7 +236,7 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* sme
 #pragma unroll
         for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
 #pragma unroll
-        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b2, bar, t.n0 + 64 * j, k0);
+        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b2, bar, t.n0 + 64 * j, p.r0 + k0);
       }
       if (++stage == kStages) {
         stage = 0;
@@ -272,7 +275,7 @@ __device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64
   uint32_t acc_phase = 0;
   while (sched_get<MODE>(p, s, t)) {
     const bool a_mn = (t.kind == 3);
-    const bool b_mn = (t.kind >= 2);
+    const bool b_mn = (t.kind == 2 || t.kind == 3);
     const uint32_t idesc = instr_desc_bf16(kBM, kBN, a_mn, b_mn);
     if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
       record_timeout(p, abort_flag);
@@ -380,6 +383,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
   bool found = false;
   int y_fwd = p.ignore_index;
   const float scale = (MODE == kModeGrad) ? *p.scale : 0.f;
+  const int row_end = p.row_end > 0 ? p.row_end : p.n;
 
   while (sched_get<MODE>(p, s, t)) {
     if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag)) {
@@ -390,49 +394,101 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
     tc_fence_after_sync();
     const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * kBN);
 
-    if (MODE == kModeForward) {
-      const int row = t.m0 + r;
+    if (kUnits<MODE>) {
+      const int lrow = t.m0 + r;   // row inside the chunk
+      const int row = p.r0 + lrow;  // row of X
       if (t.first) {
         run_m = -INFINITY;
         run_l = 0.f;
         found = false;
-        y_fwd = (row < p.n) ? p.labels[row] : p.ignore_index;
+        y_fwd = (row < row_end) ? p.labels[row] : p.ignore_index;
       }
+      if (MODE == kModeForward) {
 #pragma unroll 1
-      for (int c = 0; c < kBN / 32; ++c) {
-        const int col0 = t.n0 + c * 32;
-        if (col0 >= p.v) break;  // same for the whole warp
-        __syncwarp();
-        uint32_t v[32];
-        tmem_ld_32x32(tbase + c * 32, v);
-        const int yi = y_fwd - col0;
-        if (static_cast<unsigned>(yi) < 32u) {
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = t.n0 + c * 32;
+          if (col0 >= p.v) break;  // same for the whole warp
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32(tbase + c * 32, v);
+          const int yi = y_fwd - col0;
+          if (static_cast<unsigned>(yi) < 32u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == yi) z_tgt = __uint_as_float(v[j]);
+            found = true;
+          }
+          const int nv = min(32, p.v - col0);
+          float cmax = -INFINITY;
+          if (nv == 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, __uint_as_float(v[j]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              if (j >= nv) v[j] = __float_as_uint(-INFINITY);
+              cmax = fmaxf(cmax, __uint_as_float(v[j]));
+            }
+          }
+          const float new_m = fmaxf(run_m, cmax * kLog2e);
+          float sum = 0.f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
+          run_l = run_l * fast_exp2(run_m - new_m) + sum;
+          run_m = new_m;
+        }
+        release_accumulator(&tempty[acc], lane);
+      } else {
+        // forward-store: the tile's row max first, then p~ = 2^(t - max) as
+        // bf16 into the chunk buffer (exactly 1 at the max, relative error
+        // 2^-9 everywhere), its fp32 sum into the running log-sum-exp.
+        float tmax = -INFINITY;
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          const int col0 = t.n0 + c * 32;
+          if (col0 >= p.v) break;
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32(tbase + c * 32, v);
+          const int yi = y_fwd - col0;
+          if (static_cast<unsigned>(yi) < 32u) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j == yi) z_tgt = __uint_as_float(v[j]);
+            found = true;
+          }
+          const int nv = min(32, p.v - col0);
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            if (j == yi) z_tgt = __uint_as_float(v[j]);
-          found = true;
+            if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
         }
-        const int nv = min(32, p.v - col0);
-        float cmax = -INFINITY;
-        if (nv == 32) {
-#pragma unroll
-          for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, __uint_as_float(v[j]));
-        } else {
+        const float tmax2 = tmax * kLog2e;
+        float sum = 0.f;
+#pragma unroll 1
+        for (int g = 0; g < kBN / 64; ++g) {
+          const int col0 = t.n0 + g * 64;
+          if (col0 >= p.v) break;
+          __syncwarp();
+          uint32_t v[64];
+          tmem_ld_32x64(tbase + g * 64, v);
+          const int nv = p.v - col0;
+          uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            if (j >= nv) v[j] = __float_as_uint(-INFINITY);
-            cmax = fmaxf(cmax, __uint_as_float(v[j]));
+            const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -tmax2)) : 0.f;
+            const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -tmax2)) : 0.f;
+            sum += a + b;
+            w[j] = pack_bf16x2(a, b);
           }
+          stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
         }
-        const float new_m = fmaxf(run_m, cmax * kLog2e);
-        float sum = 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
-        run_l = run_l * fast_exp2(run_m - new_m) + sum;
+        release_accumulator(&tempty[acc], lane);
+        if (row < row_end) p.mtile[static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN] = tmax2;
+        const float new_m = fmaxf(run_m, tmax2);
+        run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(tmax2 - new_m);
         run_m = new_m;
       }
-      release_accumulator(&tempty[acc], lane);
-      if (t.last && row < p.n) {
+      if (t.last && row < row_end) {
         p.part_m[static_cast<int64_t>(t.split) * p.n + row] = run_m;
         p.part_l[static_cast<int64_t>(t.split) * p.n + row] = run_l;
         if (found) p.tgt[row] = z_tgt;
@@ -465,16 +521,13 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
       }
       release_accumulator(&tempty[acc], lane);
     } else {
-      if (t.kind == 2) {  // dX partial: fp32, stored (first chunk) or added at L2
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          if (t.n0 + c * 32 >= p.h) break;
-          __syncwarp();
-          uint32_t v[32];
-          tmem_ld_32x32(tbase + c * 32, v);
-          stage_and_store(&maps.out, stg, sbuf, lane, v, t.n0 + c * 32, t.m0 + quarter * 32, p.dx_accumulate != 0);
-        }
-      } else {  // dW rows of the chunk: complete sums over all tokens, bf16
+      // dX tile: rows of X (offset r0), written to maps.out; dW tile: vocabulary
+      // rows (offset c0), written to maps.out2.
+      const bool is_dx = (t.kind == 2);
+      const CUtensorMap* omap = is_dx ? &maps.out : &maps.out2;
+      const int omode = is_dx ? p.dx_out : p.dw_out;
+      const int y0 = (is_dx ? p.r0 : p.c0) + t.m0 + quarter * 32;
+      if (omode == kOutBF16) {
 #pragma unroll 1
         for (int g = 0; g < kBN / 64; ++g) {
           if (t.n0 + g * 64 >= p.h) break;
@@ -484,7 +537,16 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
           uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
-          stage_and_store(&maps.out2, stg, sbuf, lane, w, t.n0 + g * 64, p.c0 + t.m0 + quarter * 32, false);
+          stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, false);
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < kBN / 32; ++c) {
+          if (t.n0 + c * 32 >= p.h) break;
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32(tbase + c * 32, v);
+          stage_and_store(omap, stg, sbuf, lane, v, t.n0 + c * 32, y0, omode == kOutF32Add);
         }
       }
       release_accumulator(&tempty[acc], lane);
@@ -543,7 +605,7 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     fence_proxy_async_smem();
     tma_prefetch_map(&maps.a);
     tma_prefetch_map(&maps.b);
-    if (MODE != kModeForward) tma_prefetch_map(&maps.out);
+    if (MODE != kModeForward) tma_prefetch_map(&maps.out);  // grad / forward-store / bwd
     if (MODE == kModeBwd) {
       tma_prefetch_map(&maps.a2);
       tma_prefetch_map(&maps.b2);
@@ -586,16 +648,19 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 
 // Merge the per-split (max, sum) pairs of each row into lse, check its label,
 // and reduce the per-row losses of the block in a fixed order.
+// Rows [r0, r0 + rows) of an n-row problem; r0 is a multiple of the block size,
+// and block b writes partial r0 / kFinalizeThreads + b.
 __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
-    int n, int v, int vsplit, int ignore_index, const float* __restrict__ part_m, const float* __restrict__ part_l,
-    const float* __restrict__ tgt, const int32_t* __restrict__ labels, float* __restrict__ lse_out,
-    double* __restrict__ blk_loss, int* __restrict__ blk_valid, int* __restrict__ status) {
+    int r0, int rows, int n, int v, int vsplit, int ignore_index, const float* __restrict__ part_m,
+    const float* __restrict__ part_l, const float* __restrict__ tgt, const int32_t* __restrict__ labels,
+    float* __restrict__ lse_out, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
+    int* __restrict__ status) {
   __shared__ double s_loss[kFinalizeThreads];
   __shared__ int s_valid[kFinalizeThreads];
-  const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  const int row = r0 + blockIdx.x * kFinalizeThreads + threadIdx.x;
   double li = 0.0;
   int valid = 0;
-  if (row < n) {
+  if (row < r0 + rows) {
     float m = -INFINITY;
     for (int s = 0; s < vsplit; ++s) m = fmaxf(m, part_m[static_cast<int64_t>(s) * n + row]);
     float l = 0.f;
@@ -624,8 +689,43 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     __syncthreads();
   }
   if (threadIdx.x == 0) {
-    blk_loss[blockIdx.x] = s_loss[0];
-    blk_valid[blockIdx.x] = s_valid[0];
+    blk_loss[r0 / kFinalizeThreads + blockIdx.x] = s_loss[0];
+    blk_valid[r0 / kFinalizeThreads + blockIdx.x] = s_valid[0];
+  }
+}
+
+// In place over one row chunk of the forward-store buffer:
+//   G = s * valid * (p~ * 2^(m_tile - lse*log2e) - [j = y])
+// turning the stored, tile-max-scaled probabilities into the gradient of the
+// logits once the row's log-sum-exp is known.  One block per row.
+__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, int ignore_index,
+                                                    const float* __restrict__ lse, const int32_t* __restrict__ labels,
+                                                    const float* __restrict__ scale, const float* __restrict__ mtile,
+                                                    __nv_bfloat16* __restrict__ P) {
+  const int lrow = blockIdx.x;
+  const int row = r0 + lrow;
+  const int y = labels[row];
+  const float coef = (y != ignore_index) ? *scale : 0.f;
+  const float lse2 = lse[row] * kLog2e;
+  uint4* prow = reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp);
+  const float* mt = mtile + static_cast<int64_t>(lrow) * vtiles;
+  const int nvec = (v + 7) / 8;
+  for (int q = threadIdx.x; q < nvec; q += blockDim.x) {
+    const int j0 = q * 8;
+    const float c = coef * fast_exp2(mt[j0 / kBN] - lse2);
+    const uint4 u = prow[q];
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+    uint32_t out[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int j = j0 + 2 * e;
+      const float lo = __uint_as_float(in[e] << 16);
+      const float hi = __uint_as_float(in[e] & 0xFFFF0000u);
+      const float g0 = (j < v) ? fmaf(lo, c, (j == y) ? -coef : 0.f) : 0.f;
+      const float g1 = (j + 1 < v) ? fmaf(hi, c, (j + 1 == y) ? -coef : 0.f) : 0.f;
+      out[e] = pack_bf16x2(g0, g1);
+    }
+    prow[q] = make_uint4(out[0], out[1], out[2], out[3]);
   }
 }
 
@@ -756,16 +856,31 @@ cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid,
     case kModeForward: return launch_mode<kModeForward>(maps, p, grid, stream);
     case kModeGrad: return launch_mode<kModeGrad>(maps, p, grid, stream);
     case kModeBwd: return launch_mode<kModeBwd>(maps, p, grid, stream);
+    case kModeFwdStore: return launch_mode<kModeFwdStore>(maps, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
+}
+
+cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, int ignore_index,
+                                     const float* part_m, const float* part_l, const float* tgt, const int32_t* labels,
+                                     float* lse, double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
+  const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
+  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, ignore_index, part_m, part_l,
+                                                               tgt, labels, lse, blk_loss, blk_valid, status);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
                                 const float* tgt, const int32_t* labels, float* lse, double* blk_loss, int* blk_valid,
                                 int* status, cudaStream_t stream) {
-  const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
-  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, vsplit, ignore_index, part_m, part_l, tgt, labels,
-                                                               lse, blk_loss, blk_valid, status);
+  return launch_fwd_finalize_rows(0, n, n, v, vsplit, ignore_index, part_m, part_l, tgt, labels, lse, blk_loss,
+                                  blk_valid, status, stream);
+}
+
+cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, int ignore_index, const float* lse,
+                         const int32_t* labels, const float* scale, const float* mtile, void* P, cudaStream_t stream) {
+  fixup_kernel<<<rows, 256, 0, stream>>>(r0, v, vp, vtiles, ignore_index, lse, labels, scale, mtile,
+                                         static_cast<__nv_bfloat16*>(P));
   return cudaGetLastError();
 }
 

@@ -32,16 +32,22 @@ def test_status_strings():
 
 
 def test_workspace_size_rules():
-    ws = flce.workspace_bytes
-    assert ws(256, 128, 1024) > 0
-    # independent of V (the logits are never stored)
-    assert ws(8192, 2048, 32000) == ws(8192, 2048, 128256) == ws(8192, 2048, 7)
+    ws, wmin = flce.workspace_bytes, flce.workspace_bytes_min
+    assert wmin(256, 128, 1024) > 0
+    # the minimum is independent of V (the logits are never stored)
+    assert wmin(8192, 2048, 32000) == wmin(8192, 2048, 128256) == wmin(8192, 2048, 7)
     # grows with N
-    assert ws(16384, 2048, 32000) > ws(8192, 2048, 32000)
+    assert wmin(16384, 2048, 32000) > wmin(8192, 2048, 32000)
+    # the fused path's size is at least the minimum
+    for n, h, v in ((256, 128, 1024), (8192, 2048, 32000), (32768, 4096, 151936)):
+        assert ws(n, h, v) >= wmin(n, h, v)
+    # its row-chunk buffer never holds more than half of the [N, V] logits
+    assert ws(8192, 2048, 32000) - wmin(8192, 2048, 32000) <= 8192 * 32000 + 4 * 32000 * 2048 + 8192 * 125 * 4
     # invalid problems give 0
-    assert ws(0, 128, 10) == 0 and ws(10, 12, 10) == 0 and ws(10, 4, 10) == 0 and ws(10, 128, 0) == 0
-    # the largest workload stays under 4 GB of extra device memory
-    assert ws(131072, 4096, 131072) < 4e9
+    for f in (ws, wmin):
+        assert f(0, 128, 10) == 0 and f(10, 12, 10) == 0 and f(10, 4, 10) == 0 and f(10, 128, 0) == 0
+    # the largest workload stays under 4 GB of extra device memory on either path
+    assert ws(131072, 4096, 131072) < 4e9 and wmin(131072, 4096, 131072) < 4e9
 
 
 def _call_forward(p, X=0x1000, W=0x2000, lab=0x3000, loss=0x4000, lse=0x5000, ws=0x100000, nbytes=None):

@@ -71,9 +71,19 @@ def test_workload_full_size(cfg):
     p = synth.config_problem(cfg)
     rng = np.random.default_rng(100 + cfg)
     X, W, y = to_device(p)
+    # the recompute path (minimal workspace) must agree with the fused path
+    loss_m, lse_m, dX_m, dW_m, ws = flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction, minimal_workspace=True)
+    assert flce.read_device_status(ws) == 0
+    del ws
     loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction)
     assert flce.read_device_status(ws) == 0
     del ws
+    assert abs(float(loss_m.item()) - float(loss.item())) <= 1e-4 * abs(float(loss.item()))
+    assert (lse_m - lse).abs().max().item() <= 1e-3
+    for a, b, name in ((dX, dX_m, "dX"), (dW, dW_m, "dW")):
+        err = (a.float() - b.float()).abs().max().item()
+        assert err <= 1e-2 * b.float().abs().max().item(), (name, err)
+    del loss_m, lse_m, dX_m, dW_m
     loss = float(loss.item())
     lse_g = lse.cpu().numpy()
     valid = p.labels != p.ignore_index

@@ -25,8 +25,8 @@ def run(problem, **kw):
                 dW=dW.float().cpu().numpy(), status=st)
 
 
-def check_full(problem):
-    got = run(problem)
+def check_full(problem, minimal_workspace=False):
+    got = run(problem, minimal_workspace=minimal_workspace)
     assert got["status"] == 0, flce.status_string(got["status"])
     ref = oracle.full_bf16(problem)
     assert_loss(got["loss"], ref["loss"])
@@ -38,9 +38,13 @@ def check_full(problem):
     return got, ref
 
 
+PATHS = pytest.mark.parametrize("minimal", [False, True], ids=["fused", "recompute"])
+
+
+@PATHS
 @pytest.mark.parametrize("cfg", [1])
-def test_config_full(cfg):
-    check_full(synth.config_problem(cfg))
+def test_config_full(cfg, minimal):
+    check_full(synth.config_problem(cfg), minimal)
 
 
 @pytest.mark.parametrize("n,h,v,red,labels", [
@@ -50,22 +54,36 @@ def test_config_full(cfg):
     (77, 72, 2, "sum", "uniform"),            # V = 2
     (640, 256, 17000, "mean", "zipf"),        # three backward vocabulary chunks, ragged last chunk
     (1000, 520, 8200, "sum", "uniform"),      # chunk boundary + 8 past it; H not a tile multiple
+    (1500, 128, 4001, "mean", "zipf"),        # fused path: two row chunks, the last one ragged; odd V
 ])
-def test_ragged_shapes(n, h, v, red, labels):
+@PATHS
+def test_ragged_shapes(n, h, v, red, labels, minimal):
     p = synth.make_problem(n, h, v, seed=n + h + v, labels=labels, ignore_frac=0.1, reduction=red,
                            w_std=0.05)
-    check_full(p)
+    check_full(p, minimal)
 
 
-def test_outlier_rows_sum_reduction():
+@PATHS
+def test_outlier_rows_sum_reduction(minimal):
     p = synth.make_problem(512, 256, 3000, seed=44, labels="zipf", ignore_frac=0.05, reduction="sum",
                            outlier_rows=16, outlier_scale=10.0)
-    check_full(p)
+    check_full(p, minimal)
 
 
-def test_all_rows_ignored_mean_gives_zero():
+def test_fused_and_recompute_paths_agree():
+    p = synth.make_problem(2048, 256, 6000, seed=45, labels="zipf", ignore_frac=0.05)
+    a = run(p)
+    b = run(p, minimal_workspace=True)
+    assert abs(a["loss"] - b["loss"]) <= 1e-4 * abs(b["loss"])
+    assert np.abs(a["lse"] - b["lse"]).max() <= 1e-4
+    assert_grad(a["dX"], b["dX"], frac=1e-2, name="dX")
+    assert_grad(a["dW"], b["dW"], frac=1e-2, name="dW")
+
+
+@PATHS
+def test_all_rows_ignored_mean_gives_zero(minimal):
     p = synth.make_problem(200, 64, 500, seed=3, ignore_frac=1.0, reduction="mean")
-    got = run(p)
+    got = run(p, minimal_workspace=minimal)
     assert got["status"] == 0
     assert got["loss"] == 0.0
     assert np.all(got["dX"] == 0) and np.all(got["dW"] == 0)
@@ -73,11 +91,12 @@ def test_all_rows_ignored_mean_gives_zero():
     assert_lse(got["lse"], ref["lse"])
 
 
-def test_w_zero_closed_form():
+@PATHS
+def test_w_zero_closed_form(minimal):
     """W = 0: loss = ln V exactly in the definition; dX = 0; dW from its closed form."""
     p = synth.make_problem(384, 128, 3000, seed=5, ignore_frac=0.1)
     p.W[:] = 0
-    got = run(p)
+    got = run(p, minimal_workspace=minimal)
     assert abs(got["loss"] - math.log(3000)) <= 1e-3 * math.log(3000)
     assert np.all(got["dX"] == 0)
     X = oracle.widen_bf16(p.X)
@@ -89,18 +108,20 @@ def test_w_zero_closed_form():
     assert_grad(got["dW"], dW / nv, name="dW")
 
 
-def test_equal_rows_give_zero_dx_and_log_v():
+@PATHS
+def test_equal_rows_give_zero_dx_and_log_v(minimal):
     p = synth.make_problem(256, 128, 700, seed=6, ignore_frac=0.0)
     p.W[:] = p.W[3]
-    got = run(p)
+    got = run(p, minimal_workspace=minimal)
     assert abs(got["loss"] - math.log(700)) <= 1e-3 * math.log(700)
     # every softmax row is uniform: dX_i = s (mean_j W_j - W_{y_i}) = 0
     assert np.abs(got["dX"]).max() <= 1e-6
 
 
-def test_dw_vocab_sum_is_zero():
+@PATHS
+def test_dw_vocab_sum_is_zero(minimal):
     p = synth.make_problem(512, 256, 5000, seed=8, ignore_frac=0.05, reduction="sum")
-    got = run(p)
+    got = run(p, minimal_workspace=minimal)
     dW = got["dW"]
     # each row of G sums to zero, so the vocabulary sum of dW vanishes up to bf16 rounding of dW
     resid = np.abs(dW.astype(np.float64).sum(axis=0)).max()
@@ -151,10 +172,11 @@ def test_autograd_wrapper():
     assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")
 
 
-def test_repeat_calls_are_deterministic():
+@PATHS
+def test_repeat_calls_are_deterministic(minimal):
     p = synth.make_problem(512, 256, 9000, seed=13, ignore_frac=0.05)
-    a = run(p)
-    b = run(p)
+    a = run(p, minimal_workspace=minimal)
+    b = run(p, minimal_workspace=minimal)
     assert a["loss"] == b["loss"]
     assert np.array_equal(a["lse"], b["lse"])
     assert np.array_equal(a["dW"], b["dW"])
