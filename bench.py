@@ -357,7 +357,8 @@ def run_flce(args, rank, world, local_rank):
         "config": workload_config(args.config, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
                                                      "outside the per-step events)", world),
         "frac_of_peak": value / world / peak_burst, "peak_src": f"{peak_src} bf16_tflops (burst)",
-        "executed_tflops": world * 8.0 * n * h * v * args.steps / (total_ms / 1e3) / 1e12,
+        "executed_tflops": world * sum(x[2] for x in prof.values()) / (total_ms / 1e3) / 1e12,
+        "path": "fused row chunks (6NHV executed)" if ws_bytes >= flce.workspace_bytes(n, h, v) else "recompute (8NHV)",
         "extra_hbm_bytes": ws_bytes, "peak_alloc_delta_bytes": int(peak_delta),
         "materialised_logits_bytes": {"bf16": flce.logits_footprint_bytes(n, v, 2),
                                       "fp32": flce.logits_footprint_bytes(n, v, 4)},

@@ -702,6 +702,7 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
                                                     const float* __restrict__ lse, const int32_t* __restrict__ labels,
                                                     const float* __restrict__ scale, const float* __restrict__ mtile,
                                                     __nv_bfloat16* __restrict__ P) {
+  constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
   const int lrow = blockIdx.x;
   const int row = r0 + lrow;
   const int y = labels[row];
@@ -710,22 +711,32 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
   uint4* prow = reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp);
   const float* mt = mtile + static_cast<int64_t>(lrow) * vtiles;
   const int nvec = (v + 7) / 8;
-  for (int q = threadIdx.x; q < nvec; q += blockDim.x) {
-    const int j0 = q * 8;
-    const float c = coef * fast_exp2(mt[j0 / kBN] - lse2);
-    const uint4 u = prow[q];
-    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-    uint32_t out[4];
+  for (int base = threadIdx.x; base < nvec; base += blockDim.x * kUnroll) {
+    uint4 u[kUnroll];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int j = j0 + 2 * e;
-      const float lo = __uint_as_float(in[e] << 16);
-      const float hi = __uint_as_float(in[e] & 0xFFFF0000u);
-      const float g0 = (j < v) ? fmaf(lo, c, (j == y) ? -coef : 0.f) : 0.f;
-      const float g1 = (j + 1 < v) ? fmaf(hi, c, (j + 1 == y) ? -coef : 0.f) : 0.f;
-      out[e] = pack_bf16x2(g0, g1);
+    for (int k = 0; k < kUnroll; ++k) {
+      const int q = base + k * blockDim.x;
+      if (q < nvec) u[k] = prow[q];
     }
-    prow[q] = make_uint4(out[0], out[1], out[2], out[3]);
+#pragma unroll
+    for (int k = 0; k < kUnroll; ++k) {
+      const int q = base + k * blockDim.x;
+      if (q >= nvec) break;
+      const int j0 = q * 8;
+      const float c = coef * fast_exp2(mt[j0 / kBN] - lse2);
+      const uint32_t in[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+      uint32_t out[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int j = j0 + 2 * e;
+        const float lo = __uint_as_float(in[e] << 16);
+        const float hi = __uint_as_float(in[e] & 0xFFFF0000u);
+        const float g0 = (j < v) ? fmaf(lo, c, (j == y) ? -coef : 0.f) : 0.f;
+        const float g1 = (j + 1 < v) ? fmaf(hi, c, (j + 1 == y) ? -coef : 0.f) : 0.f;
+        out[e] = pack_bf16x2(g0, g1);
+      }
+      prow[q] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
   }
 }
 
