@@ -336,7 +336,7 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   const flce_problem_t& p = *c.p;
   TcMaps maps;
   if (!make_map(&maps.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
-  if (!make_map(&maps.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  if (!make_map(&maps.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
   maps.out = maps.a2 = maps.b2 = maps.out2 = maps.a;  // unused in this mode
 
   TcParams tp{};
@@ -346,9 +346,9 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.ignore_index = p.ignore_index;
   tp.timeout_ns = timeout_ns();
   tp.status = c.status();
-  tp.row_tiles = static_cast<int>((p.n + kBM - 1) / kBM);
+  tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
@@ -356,7 +356,7 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.r0 = 0;
   tp.row_end = tp.n;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
-  const int grid = static_cast<int>(std::min<long long>(c.dev.sms, units));
+  const int grid = pair_grid(c.dev.sms, units);
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
   flce_status_t st = cuda_status(
       timed(0, flops, c.stream, [&] { return launch_tc(kModeForward, maps, tp, grid, c.stream); }));
@@ -387,12 +387,12 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   tp.labels = labels;
   tp.lse = lse;
   tp.scale = c.scale();
-  tp.row_tiles = static_cast<int>((p.n + kBM - 1) / kBM);
+  tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.h_tiles = static_cast<int>((p.h + kBN - 1) / kBN);
 
   TcMaps gm;  // grad: X, W K-major; G store
   if (!make_map(&gm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
-  if (!make_map(&gm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  if (!make_map(&gm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
   TcMaps bm;  // bwd: W MN-major (dX B operand), X MN-major (dW B operand), dX fp32 acc, dW store
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
@@ -411,7 +411,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     const long long gtiles = static_cast<long long>(tp.row_tiles) * tp.grad_n_tiles;
     const double gflops = 2.0 * static_cast<double>(p.n) * cw * static_cast<double>(p.h);
     flce_status_t st = cuda_status(timed(1, gflops, c.stream, [&] {
-      return launch_tc(kModeGrad, gm, tp, static_cast<int>(std::min<long long>(c.dev.sms, gtiles)), c.stream);
+      return launch_tc(kModeGrad, gm, tp, pair_grid(c.dev.sms, gtiles), c.stream);
     }));
     if (st != FLCE_OK) return st;
 
@@ -419,7 +419,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
       return FLCE_ERR_CUDA;
     if (!make_map(&bm.a2, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, 64, kBK))
       return FLCE_ERR_CUDA;
-    tp.dw_m_tiles = (cw + kBM - 1) / kBM;
+    tp.dw_m_tiles = (cw + kPairRows - 1) / kPairRows;
     tp.dw_tiles = tp.dw_m_tiles * tp.h_tiles;
     tp.dx_tiles = tp.row_tiles * tp.h_tiles;
     tp.dx_out = c0 > 0 ? kOutF32Add : kOutF32Store;
@@ -432,7 +432,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     if (st != FLCE_OK) return st;
     const long long btiles = static_cast<long long>(tp.dw_tiles) + tp.dx_tiles;
     st = cuda_status(timed(2, 2.0 * gflops, c.stream, [&] {
-      return launch_tc(kModeBwd, bm, tp, static_cast<int>(std::min<long long>(c.dev.sms, btiles)), c.stream);
+      return launch_tc(kModeBwd, bm, tp, pair_grid(c.dev.sms, btiles), c.stream);
     }));
     if (st != FLCE_OK) return st;
   }
@@ -462,7 +462,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
 
   TcMaps fm;  // forward-store: X, W K-major; p~ store
   if (!make_map(&fm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
-  if (!make_map(&fm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBN)) return FLCE_ERR_CUDA;
+  if (!make_map(&fm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
   TcMaps bm;  // bwd: G K-major (dX A), W MN-major (dX B), dX bf16 out; G MN-major (dW A), X MN-major (dW B), dW fp32
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
@@ -484,15 +484,15 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     tp.labels = labels;
     tp.r0 = r0;
     tp.row_end = r0 + cr;
-    tp.row_tiles = (cr + kBM - 1) / kBM;
+    tp.row_tiles = (cr + kPairRows - 1) / kPairRows;
     tp.vocab_tiles = vtiles;
-    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms);
+    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms / 2);
     tp.part_m = c.part_m();
     tp.part_l = c.part_l();
     tp.tgt = c.tgt();
     tp.mtile = c.mtile();
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
-    const int fgrid = static_cast<int>(std::min<long long>(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit));
+    const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
@@ -520,8 +520,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     bp.c0 = 0;
     bp.cw = v;
     bp.h_tiles = h_tiles;
-    bp.dx_tiles = ((cr + kBM - 1) / kBM) * h_tiles;
-    bp.dw_tiles = ((v + kBM - 1) / kBM) * h_tiles;
+    bp.dx_tiles = ((cr + kPairRows - 1) / kPairRows) * h_tiles;
+    bp.dw_tiles = ((v + kPairRows - 1) / kPairRows) * h_tiles;
     bp.dx_k = v;
     bp.dw_k = cr;
     bp.dx_first = 1;
@@ -531,7 +531,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
     if (st != FLCE_OK) return st;
     const long long btiles = static_cast<long long>(bp.dx_tiles) + bp.dw_tiles;
-    const int bgrid = static_cast<int>(std::min<long long>(c.dev.sms, btiles));
+    const int bgrid = pair_grid(c.dev.sms, btiles);
     st = cuda_status(
         timed(2, 2.0 * fflops, c.stream, [&] { return launch_tc(kModeBwd, bm, bp, bgrid, c.stream); }));
     if (st != FLCE_OK) return st;

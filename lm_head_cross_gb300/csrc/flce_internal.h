@@ -14,9 +14,19 @@ namespace flce {
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 64;
-constexpr int kStages = 4;
+constexpr int kStages = 6;    // 32 KiB per stage and CTA (own A rows + own half of B)
 constexpr int kThreads = 192;  // warp 0: TMA producer, warp 1: MMA issuer, warps 2-5: epilogue
 constexpr int kMaxSplit = 32;  // most vocabulary splits of the forward pass
+constexpr int kPairRows = 2 * kBM;  // every launch runs on CTA pairs: a pair tile has 256 rows
+constexpr int kBoxB = kBN / 2;      // rows of the B operand each CTA of a pair stages (K-major box)
+
+// Grid of a tensor-core launch: CTA pairs, at most one CTA per SM.
+inline int pair_grid(int sms, long long pair_work) {
+  long long pairs = sms / 2;
+  if (pair_work < pairs) pairs = pair_work;
+  if (pairs < 1) pairs = 1;
+  return static_cast<int>(2 * pairs);
+}
 
 // Vocabulary chunk width of the backward pass (a multiple of kBN).  The
 // workspace holds one chunk of G, N x chunk bf16.
@@ -33,7 +43,7 @@ struct TcParams {
   int ignore_index;
   uint64_t timeout_ns;
   int* status;
-  // forward: row tiles x vocabulary splits
+  // forward: row pair tiles (256 rows) x vocabulary splits
   int row_tiles, vocab_tiles, vsplit;
   float* part_m;  // [vsplit][n] running max, log2 units
   float* part_l;  // [vsplit][n] running sum of 2^(t - m)
@@ -47,7 +57,7 @@ struct TcParams {
   // bwd: dX tiles then dW tiles
   int dx_tiles, dw_tiles;
   int h_tiles;          // ceil(h / kBN)
-  int dw_m_tiles;       // ceil(cw / kBM)
+  int dw_m_tiles;       // ceil(cw / kPairRows)
   int dx_out, dw_out;   // OutMode of the dX and dW tiles
   int dx_k, dw_k;       // K extents: dX tiles run over dx_k vocabulary ids, dW tiles over dw_k rows
   int dx_first;         // 1: dX tiles are listed first (they are the long ones)

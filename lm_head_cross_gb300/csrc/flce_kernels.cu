@@ -3,25 +3,30 @@
 // One persistent, warp-specialised tcgen05 kernel template does all the dense
 // work ("What-Each-Parallelism-Actually-Shards" §7.4: fuse the projection, the
 // log-sum-exp, the target-logit read and the backward, so the [N,V] logits are
-// never written to global memory):
+// never written to global memory).  Modes:
 //
-//   kModeForward  S = X W^T tile by tile (K = H) into TMEM; the epilogue keeps
-//                 a running (max, sum-of-exp) per row over the vocabulary tiles
-//                 of its split and picks out the target logit.  Nothing of S
-//                 leaves the SM.
-//   kModeGrad     recomputes S for one vocabulary chunk and writes
-//                 G = s (exp(S - lse) - onehot) valid as bf16 into the chunk
-//                 buffer (N x chunk, the only O(N x tile) scratch).
-//   kModeBwd      two contractions on that chunk in one launch:
-//                 dW[chunk] = G^T X (K = N, written once as bf16) and
-//                 dX += G W[chunk] (K = chunk, fp32 accumulated with TMA
-//                 reduce-add at L2).
+//   kModeForward   S = X W^T tile by tile (K = H) into TMEM; the epilogue keeps
+//                  a running (max, sum-of-exp) per row over the vocabulary tiles
+//                  of its split and picks out the target logit.
+//   kModeFwdStore  the same, and it also writes p~ = 2^(S - tile max) as bf16
+//                  for one row chunk (fused forward + backward).
+//   kModeGrad      recomputes S for one vocabulary chunk and writes
+//                  G = s (exp(S - lse) - onehot) valid as bf16.
+//   kModeBwd       dX and dW tiles of one chunk of G in one launch, handed out
+//                  longest-first by a global counter.
 //
-// Warp roles: warp 0 lane 0 issues TMA loads into a 4-stage shared-memory ring;
-// warp 1 lane 0 issues tcgen05.mma (128 x 256 x 16, bf16 -> fp32) into one of
-// two TMEM accumulators (2 x 256 columns); warps 2-5 drain the other
-// accumulator with tcgen05.ld (one TMEM lane = one row per thread), so row
-// reductions need no shuffles.  Every wait is bounded (see mbar_wait).
+// CTA pairs: every launch is a grid of 2-CTA clusters.  A pair owns a 256 x 256
+// output tile; each CTA stages its own 128 rows of A and its own half (128 rows)
+// of B, and one thread of the even CTA issues tcgen05.mma.cta_group::2
+// (256 x 256 x 16, bf16 -> fp32), which writes each CTA's 128 rows of D into
+// that CTA's TMEM.  Per SM this halves the B operand traffic of a 128 x 256
+// tile, so six 32 KiB stages fit in shared memory.
+//
+// Warp roles in each CTA: warp 0 lane 0 issues TMA loads (completion counted on
+// the even CTA's barrier); warp 1 owns TMEM, and in the even CTA lane 0 issues
+// the MMAs; warps 2-5 drain the other of two TMEM accumulators (2 x 256
+// columns) with tcgen05.ld, one row per thread, so row reductions need no
+// shuffles.  Every wait is bounded (see mbar_wait).
 #include "flce_device.cuh"
 #include "flce_internal.h"
 
@@ -32,9 +37,11 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 
-constexpr int kAStage = kBM * kBK * 2;             // 16 KiB
-constexpr int kBStage = kBN * kBK * 2;             // 32 KiB
-constexpr int kStageBytes = kAStage + kBStage;     // 48 KiB
+constexpr int kPairM = 2 * kBM;                    // rows of a pair tile
+constexpr int kHalfN = kBN / 2;                    // B rows staged by each CTA
+constexpr int kAStage = kBM * kBK * 2;             // 16 KiB: this CTA's 128 rows of A
+constexpr int kBStage = kHalfN * kBK * 2;          // 16 KiB: this CTA's half of B
+constexpr int kStageBytes = kAStage + kBStage;     // 32 KiB
 constexpr int kMnBlock = 64 * kBK * 2;             // one 64-wide MN block of 64 K rows: 8 KiB
 constexpr int kStagingBuf = 32 * 128;              // 32 rows x 128 B
 constexpr int kStagingPerWarp = 2 * kStagingBuf;
@@ -43,32 +50,40 @@ constexpr int kSmemStagingOff = kSmemStages;
 constexpr int kSmemBarOff = kSmemStagingOff + 4 * kStagingPerWarp;
 constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;  // barriers, ring, slot, flag; 1 KiB alignment slack
 constexpr uint32_t kTmemCols = 2 * kBN;
+constexpr uint16_t kPairMask = 0x3;
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Tile {
-  int m0, n0;   // origin in the output index space of this tile's GEMM
+  int m0, n0;   // m0: this CTA's first row (pair base + 128 * rank); n0: first column of the 256-wide tile
   int kblocks;  // K steps of kBK
-  int kind;     // 0 forward, 1 grad, 2 dX, 3 dW
+  int kind;     // 0 forward, 1 grad, 2 dX, 3 dW, 4 forward-store
   int first, last, split;
 };
 
 struct Sched {
-  int unit, rt, sp, vt, ve;  // forward
-  int t;                     // grad / bwd
+  int unit, rt, sp, vt, ve;  // forward units
+  int t;                     // grad / bwd tile index
   bool done;
-  // bwd: tiles handed out by a global counter; the producer publishes each
-  // tile index into a shared-memory ring that the MMA and epilogue warps read.
-  int ridx;
+  int ridx;                  // bwd: position in the tile ring
   uint32_t rphase;
 };
 
 constexpr int kRing = 8;
+// Readers of each ring slot: the even CTA's MMA thread and 4 epilogue warps,
+// the odd CTA's producer and 4 epilogue warps.
+constexpr int kRingReaders = 10;
 
 struct TileRing {
   volatile int* slot;  // [kRing]
-  uint64_t* full;      // [kRing], one arrival (producer)
-  uint64_t* empty;     // [kRing], five arrivals (MMA thread + 4 epilogue warps)
+  uint64_t* full;      // [kRing], one arrival (the even CTA's producer)
+  uint64_t* empty;     // [kRing], kRingReaders arrivals, used in the even CTA
+};
+
+struct Pair {
+  uint32_t rank;        // 0: even CTA (issues the MMAs), 1: odd CTA
+  uint32_t peer;        // 1 - rank
+  int id, count;        // pair index and number of pairs in the grid
 };
 
 template <int MODE>
@@ -92,22 +107,26 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
 }
 
 template <int MODE>
-__device__ __forceinline__ void sched_init(const TcParams& p, Sched& s) {
+__device__ __forceinline__ void sched_init(const TcParams& p, const Pair& pr, Sched& s) {
   s.done = false;
+  s.ridx = 0;
+  s.rphase = 0;
   if (kUnits<MODE>) {
-    s.unit = blockIdx.x;
+    s.unit = pr.id;
     fwd_unit_begin(p, s);
   } else {
-    s.t = blockIdx.x;
+    s.t = pr.id;
   }
 }
 
+// Tile of the current schedule position; m0 is this CTA's half of the pair tile.
 template <int MODE>
-__device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Tile& t) {
+__device__ __forceinline__ bool sched_get(const TcParams& p, const Pair& pr, const Sched& s, Tile& t) {
+  const int half = static_cast<int>(pr.rank) * kBM;
   if (kUnits<MODE>) {
     if (s.done) return false;
     const int vb = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
-    t.m0 = s.rt * kBM;  // row inside the chunk [r0, row_end)
+    t.m0 = s.rt * kPairM + half;  // row inside the chunk [r0, row_end)
     t.n0 = s.vt * kBN;
     t.kblocks = ceil_div(p.h, kBK);
     t.kind = (MODE == kModeFwdStore) ? 4 : 0;
@@ -117,7 +136,7 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Til
     return true;
   } else if (MODE == kModeGrad) {
     if (s.t >= p.row_tiles * p.grad_n_tiles) return false;
-    t.m0 = (s.t / p.grad_n_tiles) * kBM;
+    t.m0 = (s.t / p.grad_n_tiles) * kPairM + half;
     t.n0 = (s.t % p.grad_n_tiles) * kBN;  // chunk-local vocabulary column
     t.kblocks = ceil_div(p.h, kBK);
     t.kind = 1;
@@ -129,8 +148,8 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Til
     // the long tiles come first (dW when K = N, dX when K = V)
     const bool is_dx = p.dx_first ? (s.t < p.dx_tiles) : (s.t >= p.dw_tiles);
     const int u = p.dx_first ? (is_dx ? s.t : s.t - p.dx_tiles) : (is_dx ? s.t - p.dw_tiles : s.t);
-    t.m0 = (u / p.h_tiles) * kBM;  // dX: row of the G buffer; dW: column (vocabulary id) of the G buffer
-    t.n0 = (u % p.h_tiles) * kBN;  // hidden column
+    t.m0 = (u / p.h_tiles) * kPairM + half;  // dX: row of the G buffer; dW: column (vocabulary id) of the G buffer
+    t.n0 = (u % p.h_tiles) * kBN;            // hidden column
     if (is_dx) {
       t.kblocks = ceil_div(p.dx_k, kBK);
       t.kind = 2;
@@ -145,29 +164,33 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Sched& s, Til
 }
 
 template <int MODE>
-__device__ __forceinline__ void sched_next(const TcParams& p, Sched& s) {
+__device__ __forceinline__ void sched_next(const TcParams& p, const Pair& pr, Sched& s) {
   if (kUnits<MODE>) {
     if (++s.vt >= s.ve) {
-      s.unit += gridDim.x;
+      s.unit += pr.count;
       fwd_unit_begin(p, s);
     }
   } else {
-    s.t += gridDim.x;
+    s.t += pr.count;
   }
 }
 
-__device__ __forceinline__ void record_timeout(const TcParams& p, volatile int* abort_flag) {
+// A wait gave up: record it, and stop both CTAs of the pair.
+__device__ __forceinline__ void record_timeout(const TcParams& p, const Pair& pr, volatile int* abort_flag) {
   *abort_flag = 1;
+  st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(abort_flag)), pr.peer), 1u);
   atomicCAS(p.status, 0, kErrTimeout);
 }
 
-// Producer side of the dynamic schedule: publish tile index `t` (a value past
-// the last tile tells the readers to stop).
-__device__ __forceinline__ bool ring_publish(const TcParams& p, TileRing& ring, Sched& s, int t,
+// Even CTA's producer: publish tile index `t` to both CTAs (a value past the
+// last tile tells the readers to stop).
+__device__ __forceinline__ bool ring_publish(const TcParams& p, const Pair& pr, TileRing& ring, Sched& s, int t,
                                              volatile int* abort_flag) {
   if (!mbar_wait(&ring.empty[s.ridx], s.rphase ^ 1u, p.timeout_ns, abort_flag)) return false;
   ring.slot[s.ridx] = t;
+  st_shared_cluster_u32(mapa_shared(smem_u32(const_cast<int*>(&ring.slot[s.ridx])), pr.peer), static_cast<uint32_t>(t));
   mbar_arrive(&ring.full[s.ridx]);
+  mbar_arrive_cluster(mapa_shared(smem_u32(&ring.full[s.ridx]), pr.peer));
   if (++s.ridx == kRing) {
     s.ridx = 0;
     s.rphase ^= 1u;
@@ -176,14 +199,14 @@ __device__ __forceinline__ bool ring_publish(const TcParams& p, TileRing& ring, 
 }
 
 // Reader side: the next published tile index.  `arrive` is true for the one
-// thread per reader group that releases the slot.
+// thread per reader group that releases the slot (on the even CTA's barrier).
 template <bool WHOLE_WARP>
 __device__ __forceinline__ bool ring_read(const TcParams& p, TileRing& ring, Sched& s, bool arrive,
                                           volatile int* abort_flag) {
   if (!mbar_wait(&ring.full[s.ridx], s.rphase, p.timeout_ns, abort_flag)) return false;
   s.t = ring.slot[s.ridx];
   if (WHOLE_WARP) __syncwarp();  // every lane has read the slot before it is released
-  if (arrive) mbar_arrive(&ring.empty[s.ridx]);
+  if (arrive) mbar_arrive_cluster(mapa_shared(smem_u32(&ring.empty[s.ridx]), 0));
   if (++s.ridx == kRing) {
     s.ridx = 0;
     s.rphase ^= 1u;
@@ -191,52 +214,58 @@ __device__ __forceinline__ bool ring_read(const TcParams& p, TileRing& ring, Sch
   return true;
 }
 
-// Next tile index for the producer: its first tile is its block index, the
-// rest come from the global counter in the order the tiles are listed.
-__device__ __forceinline__ int dynamic_next_index(const TcParams& p) {
-  return static_cast<int>(gridDim.x) + atomicAdd(p.tile_counter, 1);
+// Next tile index of the dynamic schedule: a pair's first tile is its pair
+// index, the rest come from the global counter in the order tiles are listed.
+__device__ __forceinline__ int dynamic_next_index(const TcParams& p, const Pair& pr) {
+  return pr.count + atomicAdd(p.tile_counter, 1);
 }
 
 // ----------------------------------------------------------------------------- producer (TMA)
 
 template <int MODE>
-__device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                             TileRing ring, volatile int* abort_flag) {
+__device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& pr, uint8_t* smem, uint64_t* full,
+                             uint64_t* empty, TileRing ring, volatile int* abort_flag) {
   Sched s;
-  sched_init<MODE>(p, s);
-  s.ridx = 0;
-  s.rphase = 0;
-  if (kDynamic<MODE> && !ring_publish(p, ring, s, s.t, abort_flag)) {
-    record_timeout(p, abort_flag);
-    return;
+  sched_init<MODE>(p, pr, s);
+  if (kDynamic<MODE>) {
+    const bool ok = pr.rank == 0 ? ring_publish(p, pr, ring, s, s.t, abort_flag)
+                                 : ring_read<false>(p, ring, s, true, abort_flag);
+    if (!ok) {
+      record_timeout(p, pr, abort_flag);
+      return;
+    }
   }
+  const uint32_t full_even = mapa_shared(smem_u32(full), 0);  // completion is counted in the even CTA
+  const int bhalf = static_cast<int>(pr.rank) * kHalfN;
   Tile t;
   int stage = 0;
   uint32_t phase = 0;
-  while (sched_get<MODE>(p, s, t)) {
+  while (sched_get<MODE>(p, pr, s, t)) {
     for (int kb = 0; kb < t.kblocks; ++kb) {
       if (!mbar_wait(&empty[stage], phase ^ 1u, p.timeout_ns, abort_flag)) {
-        record_timeout(p, abort_flag);
+        record_timeout(p, pr, abort_flag);
         return;
       }
       uint8_t* sa = smem + stage * kStageBytes;
       uint8_t* sb = sa + kAStage;
-      uint64_t* bar = &full[stage];
-      mbar_arrive_expect_tx(bar, kStageBytes);
+      const uint32_t bar = full_even + 8u * stage;
+      if (pr.rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
       const int k0 = kb * kBK;
       if (t.kind <= 1 || t.kind == 4) {  // A = X [N,H] K-major, B = W [V,H] K-major
         const int vcol = (t.kind == 1) ? p.c0 + t.n0 : t.n0;
-        tma_load_2d(sa, &maps.a, bar, k0, p.r0 + t.m0);
-        tma_load_2d(sb, &maps.b, bar, k0, vcol);
-      } else if (t.kind == 2) {  // dX: A = G [N, cw] K-major, B = W rows of the chunk, MN-major
-        tma_load_2d(sa, &maps.a, bar, k0, t.m0);
+        tma_load_2d_pair(sa, &maps.a, bar, k0, p.r0 + t.m0);
+        tma_load_2d_pair(sb, &maps.b, bar, k0, vcol + bhalf);
+      } else if (t.kind == 2) {  // dX: A = G K-major, B = W rows of the chunk, MN-major
+        tma_load_2d_pair(sa, &maps.a, bar, k0, t.m0);
 #pragma unroll
-        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b, bar, t.n0 + 64 * j, p.c0 + k0);
+        for (int j = 0; j < kHalfN / 64; ++j)
+          tma_load_2d_pair(sb + j * kMnBlock, &maps.b, bar, t.n0 + bhalf + 64 * j, p.c0 + k0);
       } else {  // dW: A = G^T (G MN-major), B = X MN-major; K runs over token rows
 #pragma unroll
-        for (int j = 0; j < kBM / 64; ++j) tma_load_2d(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
+        for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
 #pragma unroll
-        for (int j = 0; j < kBN / 64; ++j) tma_load_2d(sb + j * kMnBlock, &maps.b2, bar, t.n0 + 64 * j, p.r0 + k0);
+        for (int j = 0; j < kHalfN / 64; ++j)
+          tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.r0 + k0);
       }
       if (++stage == kStages) {
         stage = 0;
@@ -244,28 +273,33 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, uint8_t* sme
       }
     }
     if (kDynamic<MODE>) {
-      s.t = dynamic_next_index(p);
-      if (!ring_publish(p, ring, s, s.t, abort_flag)) {
-        record_timeout(p, abort_flag);
+      bool ok;
+      if (pr.rank == 0) {
+        s.t = dynamic_next_index(p, pr);
+        ok = ring_publish(p, pr, ring, s, s.t, abort_flag);
+      } else {
+        ok = ring_read<false>(p, ring, s, true, abort_flag);
+      }
+      if (!ok) {
+        record_timeout(p, pr, abort_flag);
         return;
       }
     } else {
-      sched_next<MODE>(p, s);
+      sched_next<MODE>(p, pr, s);
     }
   }
 }
 
-// ----------------------------------------------------------------------------- MMA issuer
+// ----------------------------------------------------------------------------- MMA issuer (even CTA)
 
 template <int MODE>
-__device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64_t* empty, uint64_t* tfull,
-                        uint64_t* tempty, uint32_t tmem_base, TileRing ring, volatile int* abort_flag) {
+__device__ void run_mma(const TcParams& p, const Pair& pr, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                        uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base, TileRing ring,
+                        volatile int* abort_flag) {
   Sched s;
-  sched_init<MODE>(p, s);
-  s.ridx = 0;
-  s.rphase = 0;
+  sched_init<MODE>(p, pr, s);
   if (kDynamic<MODE> && !ring_read<false>(p, ring, s, true, abort_flag)) {
-    record_timeout(p, abort_flag);
+    record_timeout(p, pr, abort_flag);
     return;
   }
   Tile t;
@@ -273,19 +307,19 @@ __device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64
   uint32_t phase = 0;
   int acc = 0;
   uint32_t acc_phase = 0;
-  while (sched_get<MODE>(p, s, t)) {
+  while (sched_get<MODE>(p, pr, s, t)) {
     const bool a_mn = (t.kind == 3);
     const bool b_mn = (t.kind == 2 || t.kind == 3);
-    const uint32_t idesc = instr_desc_bf16(kBM, kBN, a_mn, b_mn);
+    const uint32_t idesc = instr_desc_bf16(kPairM, kBN, a_mn, b_mn);
     if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, p.timeout_ns, abort_flag)) {
-      record_timeout(p, abort_flag);
+      record_timeout(p, pr, abort_flag);
       return;
     }
     tc_fence_after_sync();
     const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * kBN);
     for (int kb = 0; kb < t.kblocks; ++kb) {
       if (!mbar_wait(&full[stage], phase, p.timeout_ns, abort_flag)) {
-        record_timeout(p, abort_flag);
+        record_timeout(p, pr, abort_flag);
         return;
       }
       tc_fence_after_sync();
@@ -295,24 +329,24 @@ __device__ void run_mma(const TcParams& p, uint8_t* smem, uint64_t* full, uint64
       for (int k = 0; k < kBK / 16; ++k) {
         const uint64_t ad = a_mn ? smem_desc_sw128(sa + k * 2048, kMnBlock, 1024) : smem_desc_sw128(sa + k * 32, 16, 1024);
         const uint64_t bd = b_mn ? smem_desc_sw128(sb + k * 2048, kMnBlock, 1024) : smem_desc_sw128(sb + k * 32, 16, 1024);
-        umma_bf16(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
+        umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
       }
-      umma_commit(&empty[stage]);  // frees this stage once the MMAs above have read it
+      umma_commit_pair(&empty[stage], kPairMask);  // frees this stage in both CTAs once read
       if (++stage == kStages) {
         stage = 0;
         phase ^= 1u;
       }
     }
-    umma_commit(&tfull[acc]);  // accumulator ready for the epilogue
+    umma_commit_pair(&tfull[acc], kPairMask);  // both CTAs' accumulators ready for their epilogues
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
     if (kDynamic<MODE>) {
       if (!ring_read<false>(p, ring, s, true, abort_flag)) {
-        record_timeout(p, abort_flag);
+        record_timeout(p, pr, abort_flag);
         return;
       }
     } else {
-      sched_next<MODE>(p, s);
+      sched_next<MODE>(p, pr, s);
     }
   }
 }
@@ -348,16 +382,17 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t*
   sbuf ^= 1;
 }
 
+// The even CTA's MMA waits for all 8 epilogue warps of the pair.
 __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int lane) {
   tc_fence_before_sync();
   __syncwarp();
-  if (lane == 0) mbar_arrive(tempty_acc);
+  if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty_acc), 0));
 }
 
 // ----------------------------------------------------------------------------- epilogue
 
 template <int MODE>
-__device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* staging, uint64_t* tfull,
+__device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& pr, uint8_t* staging, uint64_t* tfull,
                              uint64_t* tempty, uint32_t tmem_base, TileRing ring, volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -367,11 +402,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
   int sbuf = 0;
 
   Sched s;
-  sched_init<MODE>(p, s);
-  s.ridx = 0;
-  s.rphase = 0;
+  sched_init<MODE>(p, pr, s);
   if (kDynamic<MODE> && !ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
-    record_timeout(p, abort_flag);
+    record_timeout(p, pr, abort_flag);
     return;
   }
   Tile t;
@@ -385,9 +418,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
   const float scale = (MODE == kModeGrad) ? *p.scale : 0.f;
   const int row_end = p.row_end > 0 ? p.row_end : p.n;
 
-  while (sched_get<MODE>(p, s, t)) {
+  while (sched_get<MODE>(p, pr, s, t)) {
     if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag)) {
-      record_timeout(p, abort_flag);
+      record_timeout(p, pr, abort_flag);
       break;
     }
     __syncwarp();
@@ -555,11 +588,11 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
     if (acc == 0) acc_phase ^= 1u;
     if (kDynamic<MODE>) {
       if (!ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
-        record_timeout(p, abort_flag);
+        record_timeout(p, pr, abort_flag);
         break;
       }
     } else {
-      sched_next<MODE>(p, s);
+      sched_next<MODE>(p, pr, s);
     }
   }
   if (lane == 0) bulk_wait_group_all();
@@ -569,7 +602,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, uint8_t* sta
 // ----------------------------------------------------------------------------- the kernel
 
 template <int MODE>
-__global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
@@ -586,6 +620,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  Pair pr;
+  pr.rank = cluster_ctarank();
+  pr.peer = pr.rank ^ 1u;
+  pr.id = static_cast<int>(blockIdx.x >> 1);
+  pr.count = static_cast<int>(gridDim.x >> 1);
 
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < kStages; ++i) {
@@ -594,11 +633,11 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 4);  // one arrival per epilogue warp
+      mbar_init(&tempty[i], 8);  // one arrival per epilogue warp of the pair
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&ring.full[i], 1);
-      mbar_init(&ring.empty[i], 5);
+      mbar_init(&ring.empty[i], kRingReaders);
     }
     *abort_flag = 0;
     mbar_fence_init();
@@ -613,20 +652,20 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     }
   }
   if (warp == 1) {
-    tmem_alloc(tmem_slot, kTmemCols);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
   }
   tc_fence_before_sync();
-  __syncthreads();
+  cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA arrival
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) run_producer<MODE>(maps, p, smem, full, empty, ring, abort_flag);
+    if (lane == 0) run_producer<MODE>(maps, p, pr, smem, full, empty, ring, abort_flag);
   } else if (warp == 1) {
-    if (lane == 0) run_mma<MODE>(p, smem, full, empty, tfull, tempty, tmem_base, ring, abort_flag);
+    if (lane == 0 && pr.rank == 0) run_mma<MODE>(p, pr, smem, full, empty, tfull, tempty, tmem_base, ring, abort_flag);
   } else {
-    run_epilogue<MODE>(maps, p, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, abort_flag);
+    run_epilogue<MODE>(maps, p, pr, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, abort_flag);
   }
 
   tc_fence_before_sync();
@@ -638,9 +677,10 @@ __global__ void __launch_bounds__(kThreads, 1) tc_kernel(const __grid_constant__
     while (global_timer_ns() - t0 < 2000000ull) {
     }
   }
+  cluster_sync_all();  // no CTA leaves while its peer may still signal it
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, kTmemCols);
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 

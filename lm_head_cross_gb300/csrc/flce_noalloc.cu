@@ -132,7 +132,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
 
   TcMaps maps;
   if (!map_2d(&maps.a, X, p->h, p->n, kBK, kBM)) return FLCE_ERR_CUDA;
-  if (!map_2d(&maps.b, W, p->h, p->v, kBK, kBN)) return FLCE_ERR_CUDA;
+  if (!map_2d(&maps.b, W, p->h, p->v, kBK, kBoxB)) return FLCE_ERR_CUDA;
   maps.out = maps.a2 = maps.b2 = maps.out2 = maps.a;
 
   TcParams tp{};
@@ -142,7 +142,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.ignore_index = p->ignore_index;
   tp.timeout_ns = 4000000000ull;
   tp.status = status;
-  tp.row_tiles = static_cast<int>((p->n + kBM - 1) / kBM);
+  tp.row_tiles = static_cast<int>((p->n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p->v + kBN - 1) / kBN);
   tp.vsplit = std::min(kNoAllocSplit, tp.vocab_tiles);
   tp.part_m = part_m;
@@ -150,7 +150,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.tgt = tgt;
   tp.labels = labels;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
-  const int grid = static_cast<int>(std::min<long long>(sms, units));
+  const int grid = pair_grid(sms, units);
 
   // Only the status word must start at zero; every other region the kernels
   // read is written earlier in the same call.
