@@ -280,6 +280,9 @@ def run_flce(args, rank, world, local_rank):
 
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in starts + ends:      # create the driver events now, not inside the timed loop
+        e.record(stream)
+    torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
     if dist is not None:
         dist.barrier()

@@ -637,6 +637,13 @@ flce_status_t flce_profile_enable(int on) {
   std::lock_guard<std::mutex> lock(P.mu);
   P.clear();
   P.on = on != 0;
+  // Create the events up front so that recording them costs no driver
+  // allocation inside the region being timed.
+  while (P.on && P.pool.size() < 4096) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) break;
+    P.pool.push_back(e);
+  }
   return FLCE_OK;
 }
 
