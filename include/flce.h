@@ -117,6 +117,13 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
                            const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
                            void* ws, size_t ws_bytes, flce_stream_t stream);
 
+/* dX *= g and dW *= g in place (bf16, g a device fp32 scalar): turns the
+ * gradients flce_fwd_bwd computed for g = 1 into those of g * loss, so an
+ * autograd wrapper can run the fused pass in its forward and apply the
+ * upstream gradient in its backward. */
+flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, void* dX, void* dW,
+                               flce_stream_t stream);
+
 /* Synchronises `stream`, then returns the status word recorded in ws by the
  * kernels of earlier calls (FLCE_OK if none) and clears it. */
 flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);

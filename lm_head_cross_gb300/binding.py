@@ -20,7 +20,7 @@ REDUCTIONS = {"mean": 0, "sum": 1}
 
 EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
-            "flce_forward_noalloc", "flce_status_string")
+            "flce_forward_noalloc", "flce_scale_grads", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
@@ -64,6 +64,8 @@ def lib():
     L.flce_backward.restype = ctypes.c_int
     L.flce_fwd_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_fwd_bwd.restype = ctypes.c_int
+    L.flce_scale_grads.argtypes = [P, vp, vp, vp, vp]
+    L.flce_scale_grads.restype = ctypes.c_int
     L.flce_read_device_status.argtypes = [vp, vp]
     L.flce_read_device_status.restype = ctypes.c_int
     L.flce_selftest_timeout.argtypes = [vp, sz, ctypes.c_uint64, vp]
@@ -234,8 +236,22 @@ def profile_read() -> dict:
     return out
 
 
+def scale_grads(dX, dW, grad_loss, stream=None):
+    """dX *= g, dW *= g in place (g: one-element fp32 CUDA tensor)."""
+    n, h = dX.shape
+    v = dW.shape[0]
+    p = _problem(n, h, v, -100, "mean")
+    _call("flce_scale_grads", lib().flce_scale_grads(ctypes.byref(p), grad_loss.data_ptr(), dX.data_ptr(),
+                                                     dW.data_ptr(), _stream_ptr(stream)))
+
+
 class _LinearCrossEntropy:
-    """torch.autograd.Function wrapper, built lazily so importing needs no torch."""
+    """torch.autograd.Function wrapper, built lazily so importing needs no torch.
+
+    When a gradient is needed, the forward runs the fused forward + backward
+    (flce_fwd_bwd, upstream gradient 1) and keeps dX and dW; the backward then
+    only multiplies them by the upstream gradient.  Otherwise the forward runs
+    the forward pass alone."""
     fn = None
 
     @classmethod
@@ -246,19 +262,18 @@ class _LinearCrossEntropy:
             class Fn(torch.autograd.Function):
                 @staticmethod
                 def forward(ctx, x2, w, labels, ignore_index, reduction):
-                    loss, lse, ws = forward(x2, w, labels, ignore_index, reduction)
-                    ctx.save_for_backward(x2, w, labels, lse)
-                    ctx.ignore_index = ignore_index
-                    ctx.reduction = reduction
-                    ctx.ws = ws
+                    if ctx.needs_input_grad[0] or ctx.needs_input_grad[1]:
+                        loss, _, dX, dW, _ = fwd_bwd(x2, w, labels, ignore_index, reduction)
+                        ctx.save_for_backward(dX, dW)
+                    else:
+                        loss, _, _ = forward(x2, w, labels, ignore_index, reduction)
                     return loss.reshape(())
 
                 @staticmethod
                 def backward(ctx, grad):
-                    x2, w, labels, lse = ctx.saved_tensors
+                    dX, dW = ctx.saved_tensors
                     g = grad.detach().to(torch.float32).reshape(1).contiguous()
-                    dX, dW, _ = backward(x2, w, labels, lse, g, ctx.ignore_index, ctx.reduction, ws=ctx.ws)
-                    ctx.ws = None
+                    scale_grads(dX, dW, g)
                     return dX, dW, None, None, None
 
             cls.fn = Fn

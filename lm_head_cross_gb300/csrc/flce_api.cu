@@ -613,6 +613,18 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   return run_backward(c, X, W, labels, lse, dX, dW);
 }
 
+flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, void* dX, void* dW,
+                               flce_stream_t stream) {
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (!grad_loss || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(dX, 16) || !aligned(dW, 16) || !aligned(grad_loss, 4)) return FLCE_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  st = cuda_status(timed(3, 0.0, s, [&] { return launch_scale_bf16(dX, p->n * p->h, grad_loss, s); }));
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, s, [&] { return launch_scale_bf16(dW, p->v * p->h, grad_loss, s); }));
+}
+
 flce_status_t flce_read_device_status(void* ws, flce_stream_t stream) {
   if (!ws || !aligned(ws, kAlign)) return FLCE_ERR_INVALID_ARGUMENT;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

@@ -92,6 +92,7 @@ cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk
                                 const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
                                 cudaStream_t stream);
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
+cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream);
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 int tc_smem_bytes();

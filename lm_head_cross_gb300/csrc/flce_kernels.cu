@@ -867,6 +867,20 @@ __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16
   }
 }
 
+// x *= g for bf16 data (8 elements per thread-iteration), g a device scalar.
+__global__ void scale_bf16_kernel(__nv_bfloat16* __restrict__ x, int64_t count8, const float* __restrict__ g) {
+  const float s = *g;
+  for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count8;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    uint4 u = reinterpret_cast<uint4*>(x)[i];
+    uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      w[e] = pack_bf16x2(__uint_as_float(w[e] << 16) * s, __uint_as_float(w[e] & 0xFFFF0000u) * s);
+    reinterpret_cast<uint4*>(x)[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
 // Waits on a barrier that nothing completes; the bounded wait gives up and the
 // timeout lands in the status word.
 __global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
@@ -959,6 +973,18 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
   convert_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), count8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream) {
+  const int64_t count8 = count / 8;
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (count8 + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  scale_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<__nv_bfloat16*>(x), count8, g);
   return cudaGetLastError();
 }
 

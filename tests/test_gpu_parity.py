@@ -159,17 +159,21 @@ def test_separate_forward_backward_with_upstream_gradient():
     assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
 
 
-def test_autograd_wrapper():
+@pytest.mark.parametrize("upstream", [1.0, 2.5])
+def test_autograd_wrapper(upstream):
     p = synth.make_problem(2 * 150, 128, 1500, seed=12, labels="zipf", ignore_frac=0.1)
     X, W, y = to_device(p)
     x3 = X.reshape(2, 150, 128).clone().requires_grad_(True)
     w = W.clone().requires_grad_(True)
     loss = flce.linear_cross_entropy(x3, w, y.reshape(2, 150).long())
-    loss.backward()
-    ref = oracle.full_bf16(p)
+    (loss * upstream).backward()
+    ref = oracle.full_bf16(p, grad_output=upstream)
     assert_loss(float(loss.item()), ref["loss"])
     assert_grad(x3.grad.reshape(300, 128).float().cpu().numpy(), ref["dX"], name="dX")
     assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")
+    with torch.no_grad():
+        l2 = flce.linear_cross_entropy(X.reshape(2, 150, 128), W, y.reshape(2, 150).long())
+    assert_loss(float(l2.item()), ref["loss"])
 
 
 @PATHS
