@@ -16,8 +16,13 @@
  *   loss_i = (lse_i - z_{i,y_i}) * valid_i,   valid_i = [y_i != ignore_index]
  *   loss   = sum_i loss_i / n_valid  (FLCE_REDUCTION_MEAN; 0 when n_valid = 0)
  *          = sum_i loss_i            (FLCE_REDUCTION_SUM)
+ *          = loss_i per row          (FLCE_REDUCTION_NONE; then `loss` points to N floats
+ *                                     and the upstream gradient is one g_i per row)
  *   G_ij   = s * (exp(z_ij - lse_i) - [j = y_i]) * valid_i,
- *            s = g / n_valid (mean) or g (sum), g = upstream gradient of loss
+ *            s = g / n_valid (mean), g (sum) or g_i (none), g = upstream gradient of loss
+ *   With shift = 1 (the causal next-token shift of §7.4's call), the label of
+ *   row i is labels[i + 1], and the last row of each sequence of seq_len rows
+ *   is ignored: position t of a sequence predicts the token at t + 1.
  *   dX = G W   (bf16 [N,H]),   dW = G^T X   (bf16 [V,H])
  *
  * Conventions for every call:
@@ -68,7 +73,7 @@ typedef enum {
   FLCE_ERR_EXCEEDS_STATIC_SCRATCH = 9 /* flce_forward_noalloc: n above its fixed maximum */
 } flce_status_t;
 
-typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1 } flce_reduction_t;
+typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1, FLCE_REDUCTION_NONE = 2 } flce_reduction_t;
 
 typedef struct {
   int64_t n;             /* rows (tokens), N = B*S */
@@ -76,6 +81,8 @@ typedef struct {
   int64_t v;             /* vocabulary size */
   int32_t ignore_index;  /* label value that marks a row as ignored (commonly -100) */
   int32_t reduction;     /* flce_reduction_t */
+  int32_t shift;         /* 0, or 1: row i is scored against labels[i + 1] (see above) */
+  int32_t seq_len;       /* rows per sequence when shift = 1 (n must be a multiple); ignored otherwise */
 } flce_problem_t;
 
 /* Workspace size in bytes with which every call below takes its fastest path
@@ -93,20 +100,23 @@ size_t flce_workspace_bytes(const flce_problem_t* p);
 size_t flce_workspace_bytes_min(const flce_problem_t* p);
 
 /* Forward ("What-Each-Parallelism-Actually-Shards" §7.4: online log-sum-exp over
- * vocabulary tiles, target logit only).  Writes *loss (device fp32 scalar) and
- * lse[N] (fp32).  Reads X, W, labels.  Never stores logits. */
+ * vocabulary tiles, target logit only).  Writes the loss (device fp32 scalar,
+ * or N per-row losses under FLCE_REDUCTION_NONE) and lse[N] (fp32).  Reads X,
+ * W, labels.  Never stores logits. */
 flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W,
                            const int32_t* labels, float* loss, float* lse,
                            void* ws, size_t ws_bytes, flce_stream_t stream);
 
 /* Backward (§7.4: recompute logits instead of saving them).  Given lse from
  * flce_forward on the same X, W, labels, writes dX [N,H] and dW [V,H] (bf16,
- * fp32 accumulation).  grad_loss: device fp32 scalar g, or NULL for g = 1. */
+ * fp32 accumulation).  grad_loss: device fp32 scalar g, or NULL for g = 1;
+ * under FLCE_REDUCTION_NONE, N per-row gradients g_i (required). */
 flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* W,
                             const int32_t* labels, const float* lse, const float* grad_loss,
                             void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
 
-/* Forward then backward with g = 1: loss, lse, dX, dW in one call.  With
+/* Forward then backward with g = 1 (under FLCE_REDUCTION_NONE: the gradients
+ * of the sum of the per-row losses): loss, lse, dX, dW in one call.  With
  * ws_bytes >= flce_workspace_bytes(p) it runs fused over row chunks (the logits
  * are computed once: forward ("What-Each-Parallelism-Actually-Shards" §7.4,
  * chunked CE) keeps each chunk's tile-max-scaled softmax in bf16, a fix-up turns it

@@ -16,7 +16,7 @@ _LIB = None
 FLCE_OK = 0
 FLCE_ERR_LABEL_OUT_OF_RANGE = 5
 FLCE_ERR_TIMEOUT = 6
-REDUCTIONS = {"mean": 0, "sum": 1}
+REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
@@ -33,7 +33,8 @@ class FlceError(RuntimeError):
 
 class Problem(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("h", ctypes.c_int64), ("v", ctypes.c_int64),
-                ("ignore_index", ctypes.c_int32), ("reduction", ctypes.c_int32)]
+                ("ignore_index", ctypes.c_int32), ("reduction", ctypes.c_int32),
+                ("shift", ctypes.c_int32), ("seq_len", ctypes.c_int32)]
 
 
 def lib_path() -> str:
@@ -90,10 +91,15 @@ def logits_footprint_bytes(n_rows: int, v: int, elem_bytes: int) -> int:
     return int(n_rows) * int(v) * int(elem_bytes)
 
 
-def _problem(n, h, v, ignore_index, reduction) -> Problem:
+def _problem(n, h, v, ignore_index, reduction, shift=0, seq_len=0) -> Problem:
     if reduction not in REDUCTIONS:
-        raise ValueError(f"reduction must be 'mean' or 'sum', got {reduction!r}")
-    return Problem(int(n), int(h), int(v), int(ignore_index), REDUCTIONS[reduction])
+        raise ValueError(f"reduction must be 'mean', 'sum' or 'none', got {reduction!r}")
+    if shift not in (0, 1):
+        raise ValueError("shift must be 0 or 1")
+    if shift and (seq_len < 1 or n % seq_len):
+        raise ValueError("shift=1 needs seq_len dividing the number of rows")
+    return Problem(int(n), int(h), int(v), int(ignore_index), REDUCTIONS[reduction], int(shift),
+                   int(seq_len) if shift else 0)
 
 
 def workspace_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
@@ -148,16 +154,17 @@ def _call(name, code):
         raise FlceError(code, name)
 
 
-def forward(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, check=False):
-    """Returns (loss [1] fp32, lse [N] fp32, ws)."""
+def forward(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, check=False, shift=0,
+            seq_len=0):
+    """Returns (loss fp32 ([1], or [N] per row for reduction 'none'), lse [N] fp32, ws)."""
     torch = _torch()
     _check_inputs(x, w, labels)
     n, h = x.shape
     v = w.shape[0]
-    p = _problem(n, h, v, ignore_index, reduction)
+    p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
     if ws is None:
         ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
-    loss = torch.empty(1, dtype=torch.float32, device=x.device)
+    loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device)
     lse = torch.empty(n, dtype=torch.float32, device=x.device)
     s = _stream_ptr(stream)
     _call("flce_forward", lib().flce_forward(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
@@ -168,17 +175,22 @@ def forward(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
 
 
 def backward(x, w, labels, lse, grad_loss=None, ignore_index=-100, reduction="mean", ws=None, stream=None,
-             check=False):
-    """Returns (dX [N,H] bf16, dW [V,H] bf16, ws).  grad_loss: None or a 1-element fp32 CUDA tensor."""
+             check=False, shift=0, seq_len=0):
+    """Returns (dX [N,H] bf16, dW [V,H] bf16, ws).  grad_loss: None or a 1-element fp32 CUDA
+    tensor; for reduction 'none', an [N] fp32 CUDA tensor of per-row gradients (required)."""
     torch = _torch()
     _check_inputs(x, w, labels)
     n, h = x.shape
     v = w.shape[0]
     if lse.dtype != torch.float32 or lse.shape != (n,) or not lse.is_contiguous():
         raise ValueError("lse must be contiguous fp32 [N]")
-    if grad_loss is not None and (grad_loss.dtype != torch.float32 or grad_loss.numel() != 1 or not grad_loss.is_cuda):
-        raise ValueError("grad_loss must be a one-element fp32 CUDA tensor")
-    p = _problem(n, h, v, ignore_index, reduction)
+    want = n if reduction == "none" else 1
+    if reduction == "none" and grad_loss is None:
+        raise ValueError("reduction 'none' needs per-row gradients")
+    if grad_loss is not None and (grad_loss.dtype != torch.float32 or grad_loss.numel() != want or not grad_loss.is_cuda
+                                  or not grad_loss.is_contiguous()):
+        raise ValueError(f"grad_loss must be a contiguous {want}-element fp32 CUDA tensor")
+    p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
     if ws is None:
         ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device)
     dX = torch.empty_like(x)
@@ -194,19 +206,20 @@ def backward(x, w, labels, lse, grad_loss=None, ignore_index=-100, reduction="me
 
 
 def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, out=None, check=False,
-            minimal_workspace=False):
+            minimal_workspace=False, shift=0, seq_len=0):
     """Returns (loss, lse, dX, dW, ws).  ``out`` may pass preallocated (loss, lse, dX, dW).
-    ``minimal_workspace`` allocates flce_workspace_bytes_min (the recompute path)."""
+    ``minimal_workspace`` allocates flce_workspace_bytes_min (the recompute path).  For
+    reduction 'none' the loss is per row and the gradients are those of its sum."""
     torch = _torch()
     _check_inputs(x, w, labels)
     n, h = x.shape
     v = w.shape[0]
-    p = _problem(n, h, v, ignore_index, reduction)
+    p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
     if ws is None:
         ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device, minimal=minimal_workspace)
     if out is None:
-        out = (torch.empty(1, dtype=torch.float32, device=x.device), torch.empty(n, dtype=torch.float32, device=x.device),
-               torch.empty_like(x), torch.empty_like(w))
+        out = (torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device),
+               torch.empty(n, dtype=torch.float32, device=x.device), torch.empty_like(x), torch.empty_like(w))
     loss, lse, dX, dW = out
     s = _stream_ptr(stream)
     _call("flce_fwd_bwd", lib().flce_fwd_bwd(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
@@ -261,34 +274,55 @@ class _LinearCrossEntropy:
 
             class Fn(torch.autograd.Function):
                 @staticmethod
-                def forward(ctx, x2, w, labels, ignore_index, reduction):
-                    if ctx.needs_input_grad[0] or ctx.needs_input_grad[1]:
-                        loss, _, dX, dW, _ = fwd_bwd(x2, w, labels, ignore_index, reduction)
+                def forward(ctx, x2, w, labels, ignore_index, reduction, shift, seq_len):
+                    ctx.reduction = reduction
+                    kw = dict(shift=shift, seq_len=seq_len)
+                    needs = ctx.needs_input_grad[0] or ctx.needs_input_grad[1]
+                    if needs and reduction != "none":
+                        loss, _, dX, dW, _ = fwd_bwd(x2, w, labels, ignore_index, reduction, **kw)
                         ctx.save_for_backward(dX, dW)
-                    else:
-                        loss, _, _ = forward(x2, w, labels, ignore_index, reduction)
-                    return loss.reshape(())
+                        return loss.reshape(())
+                    loss, lse, _ = forward(x2, w, labels, ignore_index, reduction, **kw)
+                    if needs:  # per-row upstream gradients are only known in backward: recompute there
+                        ctx.save_for_backward(x2, w, labels, lse)
+                        ctx.args = (ignore_index, kw)
+                    return loss if reduction == "none" else loss.reshape(())
 
                 @staticmethod
                 def backward(ctx, grad):
+                    if ctx.reduction == "none":
+                        x2, w, labels, lse = ctx.saved_tensors
+                        ignore_index, kw = ctx.args
+                        g = grad.detach().to(torch.float32).reshape(-1).contiguous()
+                        dX, dW, _ = backward(x2, w, labels, lse, g, ignore_index, "none", **kw)
+                        return dX, dW, None, None, None, None, None
                     dX, dW = ctx.saved_tensors
                     g = grad.detach().to(torch.float32).reshape(1).contiguous()
                     scale_grads(dX, dW, g)
-                    return dX, dW, None, None, None
+                    return dX, dW, None, None, None, None, None
 
             cls.fn = Fn
         return cls.fn
 
 
-def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str = "mean"):
+def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str = "mean", shift: int = 0):
     """Cross-entropy of ``x @ w.T`` against ``labels`` without materialising the logits.
 
     x: [..., H] bf16 CUDA, w: [V, H] bf16, labels: [...] integer (same leading
-    shape as x).  Returns a scalar fp32 loss with autograd to x and w.
+    shape as x).  reduction: 'mean' (over non-ignored rows), 'sum' or 'none'
+    (per-row losses, shaped like labels).  shift=1 scores position t of each
+    sequence against the label at t + 1 (x and labels [B, S, ...]; the last
+    position of each sequence is ignored).  Autograd flows to x and w.
     """
     torch = _torch()
     h = x.shape[-1]
+    seq_len = 0
+    if shift:
+        if x.dim() < 3:
+            raise ValueError("shift=1 needs x shaped [B, S, H]")
+        seq_len = int(x.shape[-2])
     x2 = x.reshape(-1, h).contiguous()
     lab = labels.reshape(-1).to(torch.int32).contiguous()
-    loss = _LinearCrossEntropy.get().apply(x2, w.contiguous(), lab, int(ignore_index), reduction)
-    return loss
+    loss = _LinearCrossEntropy.get().apply(x2, w.contiguous(), lab, int(ignore_index), reduction, int(shift),
+                                           seq_len)
+    return loss.reshape(labels.shape) if reduction == "none" else loss

@@ -133,7 +133,11 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 flce_status_t check_problem(const flce_problem_t* p) {
   if (!p) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->n < 1 || p->h < 1 || p->v < 1) return FLCE_ERR_INVALID_ARGUMENT;
-  if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM &&
+      p->reduction != FLCE_REDUCTION_NONE)
+    return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->shift != 0 && p->shift != 1) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->shift && (p->seq_len < 1 || p->n % p->seq_len != 0)) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->h < 8 || p->h % 8 != 0) return FLCE_ERR_UNSUPPORTED_SHAPE;
   // TMA coordinates and the kernels' tile indices are 32-bit.
   if (p->n > (int64_t{1} << 30) || p->v > (int64_t{1} << 30) || p->h > (int64_t{1} << 20))
@@ -221,6 +225,10 @@ struct Ctx {
   void* g() const { return ws + L.g; }
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
   float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
+  LabelView labels_of(const int32_t* labels) const {
+    return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1};
+  }
+  bool per_row() const { return p->reduction == FLCE_REDUCTION_NONE; }
 };
 
 flce_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
@@ -353,6 +361,8 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
   tp.labels = labels;
+  tp.shift = p.shift;
+  tp.seq_len = p.shift ? p.seq_len : 1;
   tp.r0 = 0;
   tp.row_end = tp.n;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
@@ -362,19 +372,21 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
       timed(0, flops, c.stream, [&] { return launch_tc(kModeForward, maps, tp, grid, c.stream); }));
   if (st != FLCE_OK) return st;
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_fwd_finalize(tp.n, tp.v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels, lse,
-                               c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+    return launch_fwd_finalize_rows(0, tp.n, tp.n, tp.v, tp.vsplit, c.labels_of(labels), c.part_m(), c.part_l(),
+                                    c.tgt(), lse, c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(),
+                                    c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
   return cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, grad_loss, loss, c.n_valid(),
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, grad_loss,
+                               c.per_row() ? nullptr : loss, c.n_valid(),
                                c.scale(), c.stream);
   }));
 }
 
 // Backward given lse and the scale already in the workspace.
 flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int32_t* labels, const float* lse,
-                           void* dX, void* dW) {
+                           const float* grad_rows, void* dX, void* dW) {
   const flce_problem_t& p = *c.p;
   const int chunk = c.L.chunk;
   TcParams tp{};
@@ -385,6 +397,9 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   tp.timeout_ns = timeout_ns();
   tp.status = c.status();
   tp.labels = labels;
+  tp.shift = p.shift;
+  tp.seq_len = p.shift ? p.seq_len : 1;
+  tp.grad_rows = grad_rows;
   tp.lse = lse;
   tp.scale = c.scale();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
@@ -451,7 +466,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
   const int vtiles = (v + kBN - 1) / kBN;
   const int h_tiles = (h + kBN - 1) / kBN;
   flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_label_scan(n, v, p.ignore_index, labels, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+    return launch_label_scan_view(n, v, c.labels_of(labels), c.blk_loss(), c.blk_valid(), c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
@@ -482,6 +497,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     tp.timeout_ns = timeout_ns();
     tp.status = c.status();
     tp.labels = labels;
+    tp.shift = p.shift;
+    tp.seq_len = p.shift ? p.seq_len : 1;
     tp.r0 = r0;
     tp.row_end = r0 + cr;
     tp.row_tiles = (cr + kPairRows - 1) / kPairRows;
@@ -496,13 +513,14 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, p.ignore_index, c.part_m(), c.part_l(), c.tgt(), labels,
-                                      lse, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, c.labels_of(labels), c.part_m(), c.part_l(), c.tgt(),
+                                      lse, c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(),
+                                      c.stream);
     }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, p.ignore_index, lse, labels, c.scale(),
-                          c.mtile(), c.g(), c.stream);
+      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, c.labels_of(labels), lse, c.scale(), c.mtile(),
+                          c.g(), c.stream);
     }));
     if (st != FLCE_OK) return st;
 
@@ -537,8 +555,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     if (st != FLCE_OK) return st;
   }
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, loss, c.n_valid(),
-                               c.scale(), c.stream);
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr,
+                               c.per_row() ? nullptr : loss, c.n_valid(), c.scale(), c.stream);
   }));
   if (st != FLCE_OK) return st;
   return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dW, p.v * p.h, c.stream); }));
@@ -585,17 +603,19 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
   Ctx c;
   flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
+  if (c.per_row() && !grad_loss) return FLCE_ERR_INVALID_ARGUMENT;  // reduction none needs the per-row gradient
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_label_scan(static_cast<int>(p->n), static_cast<int>(p->v), p->ignore_index, labels, c.blk_loss(),
+    return launch_label_scan_view(static_cast<int>(p->n), static_cast<int>(p->v), c.labels_of(labels), c.blk_loss(),
                              c.blk_valid(), c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction, grad_loss, nullptr, c.n_valid(),
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction, c.per_row() ? nullptr : grad_loss,
+                               nullptr, c.n_valid(),
                                c.scale(), c.stream);
   }));
   if (st != FLCE_OK) return st;
-  return run_backward(c, X, W, labels, lse, dX, dW);
+  return run_backward(c, X, W, labels, lse, c.per_row() ? grad_loss : nullptr, dX, dW);
 }
 
 flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
@@ -610,7 +630,7 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   if (c.L.rows > 0) return run_fused(c, X, W, labels, loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
   if (st != FLCE_OK) return st;
-  return run_backward(c, X, W, labels, lse, dX, dW);
+  return run_backward(c, X, W, labels, lse, nullptr, dX, dW);
 }
 
 flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, void* dX, void* dW,

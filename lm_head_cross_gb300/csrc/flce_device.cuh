@@ -17,6 +17,13 @@ enum : int {
   kErrTimeout = 6,
 };
 
+// Label of `row`: labels[row], or with shift labels[row + 1] and ignore_index
+// for the last row of each sequence of seq_len rows.
+__device__ __forceinline__ int label_at(const int32_t* labels, int row, int shift, int seq_len, int ignore_index) {
+  if (!shift) return labels[row];
+  return ((row + 1) % seq_len == 0) ? ignore_index : labels[row + 1];
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -49,6 +49,8 @@ struct TcParams {
   float* part_l;  // [vsplit][n] running sum of 2^(t - m)
   float* tgt;     // [n] target logit z_{i, y_i}
   const int32_t* labels;
+  int shift, seq_len;   // shift = 1: row i is scored against labels[i + 1]; each sequence's last row is ignored
+  const float* grad_rows;  // grad (reduction none): per-row upstream gradient, or null
   // grad / bwd: one vocabulary chunk [c0, c0 + cw)
   int c0, cw;
   const float* lse;
@@ -81,11 +83,21 @@ cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid,
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m,
                                 const float* part_l, const float* tgt, const int32_t* labels, float* lse,
                                 double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
-cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, int ignore_index,
-                                     const float* part_m, const float* part_l, const float* tgt, const int32_t* labels,
-                                     float* lse, double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
-cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, int ignore_index, const float* lse,
-                         const int32_t* labels, const float* scale, const float* mtile, void* P, cudaStream_t stream);
+// Labels as the kernels read them: with shift, row i takes labels[i + 1] and
+// the last row of each sequence of seq_len rows is ignored.
+struct LabelView {
+  const int32_t* labels;
+  int ignore_index;
+  int shift, seq_len;
+};
+
+cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
+                                     const float* part_l, const float* tgt, float* lse, float* loss_rows,
+                                     double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
+cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
+                         const float* scale, const float* mtile, void* P, cudaStream_t stream);
+cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
+                                   cudaStream_t stream);
 cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss,
                               int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,

@@ -434,7 +434,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_m = -INFINITY;
         run_l = 0.f;
         found = false;
-        y_fwd = (row < row_end) ? p.labels[row] : p.ignore_index;
+        y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
       }
       if (MODE == kModeForward) {
 #pragma unroll 1
@@ -528,9 +528,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       }
     } else if (MODE == kModeGrad) {
       const int row = t.m0 + r;
-      const int y = (row < p.n) ? p.labels[row] : p.ignore_index;
+      const int y = (row < p.n) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
       const bool valid = (row < p.n) && (y != p.ignore_index);
-      const float coef = valid ? scale : 0.f;
+      const float coef = valid ? (p.grad_rows ? p.grad_rows[row] : scale) : 0.f;
       const float lse2 = (row < p.n) ? p.lse[row] * kLog2e : 0.f;
       const int ycol = y - (p.c0 + t.n0);  // label position inside this tile (if any)
 #pragma unroll 1
@@ -691,10 +691,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // Rows [r0, r0 + rows) of an n-row problem; r0 is a multiple of the block size,
 // and block b writes partial r0 / kFinalizeThreads + b.
 __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
-    int r0, int rows, int n, int v, int vsplit, int ignore_index, const float* __restrict__ part_m,
-    const float* __restrict__ part_l, const float* __restrict__ tgt, const int32_t* __restrict__ labels,
-    float* __restrict__ lse_out, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
+    int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* __restrict__ part_m,
+    const float* __restrict__ part_l, const float* __restrict__ tgt, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
     int* __restrict__ status) {
+  const int ignore_index = lv.ignore_index;
   __shared__ double s_loss[kFinalizeThreads];
   __shared__ int s_valid[kFinalizeThreads];
   const int row = r0 + blockIdx.x * kFinalizeThreads + threadIdx.x;
@@ -708,7 +709,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
       l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
     const float lse = (m + log2f(l)) * kLn2;
     lse_out[row] = lse;
-    const int y = labels[row];
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
     if (y != ignore_index) {
       if (y >= 0 && y < v) {
         valid = 1;
@@ -717,6 +718,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
         atomicCAS(status, 0, kErrLabel);
       }
     }
+    if (loss_rows) loss_rows[row] = static_cast<float>(li);
   }
   s_loss[threadIdx.x] = li;
   s_valid[threadIdx.x] = valid;
@@ -738,15 +740,14 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
 //   G = s * valid * (p~ * 2^(m_tile - lse*log2e) - [j = y])
 // turning the stored, tile-max-scaled probabilities into the gradient of the
 // logits once the row's log-sum-exp is known.  One block per row.
-__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, int ignore_index,
-                                                    const float* __restrict__ lse, const int32_t* __restrict__ labels,
-                                                    const float* __restrict__ scale, const float* __restrict__ mtile,
-                                                    __nv_bfloat16* __restrict__ P) {
+__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, LabelView lv,
+                                                    const float* __restrict__ lse, const float* __restrict__ scale,
+                                                    const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
   constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
   const int lrow = blockIdx.x;
   const int row = r0 + lrow;
-  const int y = labels[row];
-  const float coef = (y != ignore_index) ? *scale : 0.f;
+  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+  const float coef = (y != lv.ignore_index) ? *scale : 0.f;
   const float lse2 = lse[row] * kLog2e;
   uint4* prow = reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp);
   const float* mt = mtile + static_cast<int64_t>(lrow) * vtiles;
@@ -781,16 +782,16 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
 }
 
 // Label scan: range check and valid count, for a backward call on its own.
-__global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int v, int ignore_index,
-                                                                       const int32_t* __restrict__ labels,
+__global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int v, LabelView lv,
                                                                        double* __restrict__ blk_loss,
                                                                        int* __restrict__ blk_valid,
                                                                        int* __restrict__ status) {
   __shared__ int s_valid[kFinalizeThreads];
+  const int ignore_index = lv.ignore_index;
   const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
   int valid = 0;
   if (row < n) {
-    const int y = labels[row];
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
     if (y != ignore_index) {
       if (y >= 0 && y < v)
         valid = 1;
@@ -840,7 +841,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
     const long long nv = s_valid[0];
     const double g = grad_loss ? static_cast<double>(*grad_loss) : 1.0;
     double loss, scale;
-    if (reduction == 0) {  // mean over valid rows; no valid row gives 0
+    if (reduction == 0) {  // mean over valid rows; no valid row gives 0 (sum / none: scale g)
       loss = nv > 0 ? total / static_cast<double>(nv) : 0.0;
       scale = nv > 0 ? g / static_cast<double>(nv) : 0.0;
     } else {
@@ -926,34 +927,39 @@ cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid,
   }
 }
 
-cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, int ignore_index,
-                                     const float* part_m, const float* part_l, const float* tgt, const int32_t* labels,
-                                     float* lse, double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
+cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
+                                     const float* part_l, const float* tgt, float* lse, float* loss_rows,
+                                     double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
   const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
-  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, ignore_index, part_m, part_l,
-                                                               tgt, labels, lse, blk_loss, blk_valid, status);
+  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse,
+                                                               loss_rows, blk_loss, blk_valid, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
                                 const float* tgt, const int32_t* labels, float* lse, double* blk_loss, int* blk_valid,
                                 int* status, cudaStream_t stream) {
-  return launch_fwd_finalize_rows(0, n, n, v, vsplit, ignore_index, part_m, part_l, tgt, labels, lse, blk_loss,
-                                  blk_valid, status, stream);
+  const LabelView lv{labels, ignore_index, 0, 1};
+  return launch_fwd_finalize_rows(0, n, n, v, vsplit, lv, part_m, part_l, tgt, lse, nullptr, blk_loss, blk_valid,
+                                  status, stream);
 }
 
-cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, int ignore_index, const float* lse,
-                         const int32_t* labels, const float* scale, const float* mtile, void* P, cudaStream_t stream) {
-  fixup_kernel<<<rows, 256, 0, stream>>>(r0, v, vp, vtiles, ignore_index, lse, labels, scale, mtile,
-                                         static_cast<__nv_bfloat16*>(P));
+cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
+                         const float* scale, const float* mtile, void* P, cudaStream_t stream) {
+  fixup_kernel<<<rows, 256, 0, stream>>>(r0, v, vp, vtiles, lv, lse, scale, mtile, static_cast<__nv_bfloat16*>(P));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
+                                   cudaStream_t stream) {
+  const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
+  label_scan_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, lv, blk_loss, blk_valid, status);
   return cudaGetLastError();
 }
 
 cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss, int* blk_valid,
                               int* status, cudaStream_t stream) {
-  const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
-  label_scan_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, ignore_index, labels, blk_loss, blk_valid, status);
-  return cudaGetLastError();
+  return launch_label_scan_view(n, v, LabelView{labels, ignore_index, 0, 1}, blk_loss, blk_valid, status, stream);
 }
 
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,

@@ -102,7 +102,11 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
                                               const int32_t* labels, float* loss, float* lse, flce_stream_t stream) {
   if (!p || !X || !W || !labels || !loss || !lse) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->n < 1 || p->h < 1 || p->v < 1) return FLCE_ERR_INVALID_ARGUMENT;
-  if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM &&
+      p->reduction != FLCE_REDUCTION_NONE)
+    return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->shift != 0 && p->shift != 1) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->shift && (p->seq_len < 1 || p->n % p->seq_len != 0)) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->h < 8 || p->h % 8 != 0 || p->h > (int64_t{1} << 20) || p->v > (int64_t{1} << 30))
     return FLCE_ERR_UNSUPPORTED_SHAPE;
   if (p->n > kNoAllocMaxRows) return FLCE_ERR_EXCEEDS_STATIC_SCRATCH;
@@ -149,6 +153,8 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.part_l = part_l;
   tp.tgt = tgt;
   tp.labels = labels;
+  tp.shift = p->shift;
+  tp.seq_len = p->shift ? p->seq_len : 1;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = pair_grid(sms, units);
 
@@ -156,11 +162,14 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   // read is written earlier in the same call.
   if (cudaMemsetAsync(status, 0, sizeof(int), cs) != cudaSuccess) return FLCE_ERR_CUDA;
   if (launch_tc(kModeForward, maps, tp, grid, cs) != cudaSuccess) return FLCE_ERR_CUDA;
-  if (launch_fwd_finalize(tp.n, tp.v, tp.vsplit, p->ignore_index, part_m, part_l, tgt, labels, lse, blk_loss, blk_valid,
-                          status, cs) != cudaSuccess)
+  const bool per_row = p->reduction == FLCE_REDUCTION_NONE;
+  const LabelView lv{labels, p->ignore_index, tp.shift, tp.seq_len};
+  if (launch_fwd_finalize_rows(0, tp.n, tp.n, tp.v, tp.vsplit, lv, part_m, part_l, tgt, lse, per_row ? loss : nullptr,
+                               blk_loss, blk_valid, status, cs) != cudaSuccess)
     return FLCE_ERR_CUDA;
   const int nblk = static_cast<int>((p->n + kFinalizeThreads - 1) / kFinalizeThreads);
-  if (launch_reduce_final(nblk, blk_loss, blk_valid, p->reduction, nullptr, loss, n_valid, scale, cs) != cudaSuccess)
+  if (launch_reduce_final(nblk, blk_loss, blk_valid, p->reduction, nullptr, per_row ? nullptr : loss, n_valid, scale,
+                          cs) != cudaSuccess)
     return FLCE_ERR_CUDA;
   poison_loss_on_error<<<1, 32, 0, cs>>>(status, loss);
   return cudaGetLastError() == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;

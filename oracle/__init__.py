@@ -22,7 +22,11 @@ while never storing the logits.  So, for rows ``i`` and vocabulary ids ``j``:
 
 Readings where the pages are silent: under ``mean`` with no valid row the loss
 is 0 and both gradients are 0; ``lse`` is reported for ignored rows too; a label
-that is neither ``ignore_index`` nor in ``[0, V)`` is an error.
+that is neither ``ignore_index`` nor in ``[0, V)`` is an error.  ``none``
+returns the per-row losses, and the gradient then takes one upstream value per
+row.  §7.4's call passes ``shift=1`` (causal next-token shift): position t of a
+sequence is scored against the token at t + 1, and the last position has no
+target; ``shift_labels`` writes that out.
 
 Everything is float64.  bf16 inputs widen exactly.  Matrix products use numpy's
 ``matmul`` (a library primitive); rows are processed in blocks only to bound
@@ -51,11 +55,20 @@ def valid_rows(labels: np.ndarray, ignore_index: int) -> np.ndarray:
     return np.asarray(labels, dtype=np.int64) != ignore_index
 
 
-def grad_scale(n_valid: int, reduction: str, grad_output: float = 1.0) -> float:
-    """``s``: d(loss)/d(loss_i) times the upstream gradient."""
+def shift_labels(labels: np.ndarray, seq_len: int, ignore_index: int) -> np.ndarray:
+    """Next-token targets: row i of a flattened [B, S] batch takes labels[i + 1];
+    the last position of each sequence gets ``ignore_index``."""
+    lab = np.asarray(labels).reshape(-1, seq_len)
+    out = np.full_like(lab, ignore_index)
+    out[:, :-1] = lab[:, 1:]
+    return out.reshape(-1)
+
+
+def grad_scale(n_valid: int, reduction: str, grad_output=1.0):
+    """``s``: d(loss)/d(loss_i) times the upstream gradient (per row for ``none``)."""
     if reduction == "mean":
         return 0.0 if n_valid == 0 else grad_output / n_valid
-    if reduction == "sum":
+    if reduction in ("sum", "none"):
         return grad_output
     raise ValueError(reduction)
 
@@ -108,13 +121,16 @@ def forward(X, W, labels, ignore_index: int = -100, reduction: str = "mean"):
         loss = 0.0 if n_valid == 0 else total / n_valid
     elif reduction == "sum":
         loss = total
+    elif reduction == "none":
+        loss = loss_rows.copy()
     else:
         raise ValueError(reduction)
     return dict(loss=loss, lse=lse, loss_rows=loss_rows, n_valid=n_valid)
 
 
-def grad_logits_rows(X, W, labels, rows, lse_rows, scale: float, ignore_index: int = -100):
-    """``G[rows, :] = s * (exp(z - lse) - onehot(y)) * valid`` for selected rows."""
+def grad_logits_rows(X, W, labels, rows, lse_rows, scale, ignore_index: int = -100):
+    """``G[rows, :] = s * (exp(z - lse) - onehot(y)) * valid`` for selected rows
+    (``scale``: a number, or one value per selected row)."""
     X = np.asarray(X, np.float64)
     W = np.asarray(W, np.float64)
     rows = np.asarray(rows, dtype=np.int64)
@@ -124,7 +140,7 @@ def grad_logits_rows(X, W, labels, rows, lse_rows, scale: float, ignore_index: i
     ok = lab != ignore_index
     p[np.nonzero(ok)[0], lab[ok]] -= 1.0
     p[~ok, :] = 0.0
-    return scale * p
+    return np.reshape(scale, (-1, 1)) * p if np.ndim(scale) else scale * p
 
 
 def backward_dx_rows(X, W, labels, rows, scale: float, ignore_index: int = -100, lse_rows=None):
@@ -136,8 +152,8 @@ def backward_dx_rows(X, W, labels, rows, scale: float, ignore_index: int = -100,
     return G @ np.asarray(W, np.float64)
 
 
-def backward_dw_ids(X, W, labels, lse_all, ids, scale: float, ignore_index: int = -100):
-    """``dW[ids] = G[:, ids]^T X``; needs every row's lse."""
+def backward_dw_ids(X, W, labels, lse_all, ids, scale, ignore_index: int = -100):
+    """``dW[ids] = G[:, ids]^T X``; needs every row's lse (``scale``: number or per row)."""
     X = np.asarray(X, np.float64)
     W = np.asarray(W, np.float64)
     ids = np.asarray(ids, dtype=np.int64)
@@ -146,11 +162,15 @@ def backward_dw_ids(X, W, labels, lse_all, ids, scale: float, ignore_index: int 
     p = np.exp(z - np.asarray(lse_all, np.float64)[:, None])
     p -= (lab[:, None] == ids[None, :]).astype(np.float64)
     p[lab == ignore_index, :] = 0.0
+    if np.ndim(scale):
+        p = p * np.reshape(scale, (-1, 1))
+        return p.T @ X
     return scale * (p.T @ X)
 
 
-def full(X, W, labels, ignore_index: int = -100, reduction: str = "mean", grad_output: float = 1.0):
-    """Loss, lse, dX and dW for a whole (small) problem, in float64."""
+def full(X, W, labels, ignore_index: int = -100, reduction: str = "mean", grad_output=1.0):
+    """Loss, lse, dX and dW for a whole (small) problem, in float64
+    (``grad_output``: one number, or one per row for ``none``)."""
     X = np.asarray(X, np.float64)
     W = np.asarray(W, np.float64)
     f = forward(X, W, labels, ignore_index, reduction)

@@ -67,6 +67,8 @@ def test_host_side_validation_without_gpu():
     assert _call_forward(ok, nbytes=16) == 4         # workspace too small
     assert _call_forward(P(256, 12, 1024, -100, 0)) == 2   # h % 8 != 0
     assert _call_forward(P(256, 128, 1024, -100, 7)) == 1  # bad reduction
+    assert _call_forward(P(256, 128, 1024, -100, 0, 2, 0)) == 1  # bad shift
+    assert _call_forward(P(256, 128, 1024, -100, 0, 1, 100)) == 1  # n not a multiple of seq_len
     assert _call_forward(P(0, 128, 1024, -100, 0)) == 1    # empty
     L = flce.lib()
     assert L.flce_selftest_timeout(None, 256, 1000, None) == 1
@@ -76,7 +78,7 @@ def test_host_side_validation_without_gpu():
 
 def test_python_binding_rejects_bad_reduction():
     with pytest.raises(ValueError):
-        flce.workspace_bytes(10, 16, 10, reduction="none")
+        flce.workspace_bytes(10, 16, 10, reduction="avg")
 
 
 def test_footprint_golden():

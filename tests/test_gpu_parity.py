@@ -196,3 +196,67 @@ def test_timeout_path_returns_status():
     p = synth.make_problem(128, 64, 256, seed=1)
     got = run(p)
     assert got["status"] == 0
+
+
+@PATHS
+def test_reduction_none_fwd_bwd(minimal):
+    """Per-row losses; the fused call's gradients are those of their sum."""
+    p = synth.make_problem(600, 128, 3000, seed=61, labels="zipf", ignore_frac=0.1, reduction="none")
+    X, W, y = to_device(p)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, "none", minimal_workspace=minimal)
+    assert flce.read_device_status(ws) == 0
+    ref = oracle.full_bf16(p)
+    rows = loss.cpu().numpy()
+    assert rows.shape == (600,)
+    assert np.abs(rows - ref["loss"]).max() <= 2e-3 + 1e-3 * np.abs(ref["loss"]).max()
+    valid = p.labels != p.ignore_index
+    assert np.all(rows[~valid] == 0.0)
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+def test_reduction_none_backward_per_row_gradients():
+    p = synth.make_problem(500, 136, 2200, seed=62, labels="uniform", ignore_frac=0.1, reduction="none")
+    X, W, y = to_device(p)
+    loss, lse, ws = flce.forward(X, W, y, p.ignore_index, "none")
+    g = np.random.default_rng(5).standard_normal(500).astype(np.float32)
+    dX, dW, _ = flce.backward(X, W, y, lse, torch.from_numpy(g).cuda(), p.ignore_index, "none", ws=ws)
+    assert flce.read_device_status(ws) == 0
+    ref = oracle.full_bf16(p, grad_output=g.astype(np.float64))
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+@PATHS
+@pytest.mark.parametrize("red", ["mean", "sum"])
+def test_shift_one(minimal, red):
+    """Causal next-token shift inside the kernels: row i is scored against labels[i + 1]."""
+    B, S = 3, 200
+    p = synth.make_problem(B * S, 128, 2500, seed=63, labels="zipf", ignore_frac=0.05, reduction=red)
+    X, W, y = to_device(p)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, minimal_workspace=minimal, shift=1, seq_len=S)
+    assert flce.read_device_status(ws) == 0
+    shifted = oracle.shift_labels(p.labels, S, p.ignore_index)
+    ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), shifted, p.ignore_index, red)
+    assert_loss(float(loss.item()), ref["loss"])
+    assert_lse(lse.cpu().numpy(), ref["lse"])
+    assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+def test_autograd_none_and_shift():
+    B, S, H, V = 2, 160, 128, 1800
+    p = synth.make_problem(B * S, H, V, seed=64, labels="zipf", ignore_frac=0.1)
+    X, W, y = to_device(p)
+    x3 = X.reshape(B, S, H).clone().requires_grad_(True)
+    w = W.clone().requires_grad_(True)
+    rows = flce.linear_cross_entropy(x3, w, y.reshape(B, S).long(), reduction="none", shift=1)
+    assert rows.shape == (B, S)
+    g = torch.linspace(0.5, 1.5, B * S, device="cuda").reshape(B, S)
+    (rows * g).sum().backward()
+    shifted = oracle.shift_labels(p.labels, S, p.ignore_index)
+    ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), shifted, p.ignore_index, "none",
+                      grad_output=g.reshape(-1).cpu().numpy().astype(np.float64))
+    assert np.abs(rows.detach().reshape(-1).cpu().numpy() - ref["loss"]).max() <= 2e-3 + 1e-3 * np.abs(ref["loss"]).max()
+    assert_grad(x3.grad.reshape(B * S, H).float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")

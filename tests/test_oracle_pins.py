@@ -250,6 +250,47 @@ def test_oracle_pin(pin):
     pin(oracle)
 
 
+def test_reduction_none_matches_torch():
+    """Per-row losses and the gradient of sum_i g_i loss_i against torch's reduction='none'."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(31)
+    X, W, y = _rand_problem(rng, 23, 9, 14, ignore_frac=0.2)
+    g = rng.standard_normal(23)
+    f = oracle.full(X, W, y, IGN, "none", grad_output=g)
+    tX = torch.tensor(X, requires_grad=True)
+    tW = torch.tensor(W, requires_grad=True)
+    rows = F.cross_entropy(tX @ tW.T, torch.tensor(y), ignore_index=IGN, reduction="none")
+    (rows * torch.tensor(g)).sum().backward()
+    np.testing.assert_allclose(f["loss"], rows.detach().numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(f["dX"], tX.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(f["dW"], tW.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
+def test_shift_matches_causal_lm_loss():
+    """shift=1 on flattened [B, S] rows equals the usual causal-LM loss: logits of
+    positions 0..S-2 against labels of positions 1..S-1 (torch, float64)."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(32)
+    B, S, H, V = 3, 7, 6, 11
+    X = rng.standard_normal((B * S, H))
+    W = rng.standard_normal((V, H)) * 0.5
+    lab = rng.integers(0, V, size=(B, S))
+    lab[0, 3] = IGN
+    y = oracle.shift_labels(lab, S, IGN)
+    assert list(y[:S]) == list(lab[0, 1:]) + [IGN]
+    f = oracle.full(X, W, y, IGN, "mean")
+    tX = torch.tensor(X.reshape(B, S, H), requires_grad=True)
+    tW = torch.tensor(W, requires_grad=True)
+    logits = tX @ tW.T
+    loss = F.cross_entropy(logits[:, :-1].reshape(-1, V), torch.tensor(lab[:, 1:]).reshape(-1), ignore_index=IGN)
+    loss.backward()
+    assert abs(f["loss"] - loss.item()) < 1e-12
+    np.testing.assert_allclose(f["dX"], tX.grad.numpy().reshape(B * S, H), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(f["dW"], tW.grad.numpy(), rtol=1e-10, atol=1e-13)
+
+
 def test_mean_with_no_valid_row():
     """Reading taken where the pages are silent: no valid row under mean gives 0, not NaN."""
     rng = np.random.default_rng(23)
