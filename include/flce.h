@@ -134,6 +134,32 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
 flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, void* dX, void* dW,
                                flce_stream_t stream);
 
+/* Distillation without full logits ("What-Each-Parallelism-Actually-Shards"
+ * §7.6: in distillation keep to top-k logits or chunked KL instead of returning
+ * the [B,S,V] logits).
+ *
+ * flce_topk: for each row the k largest logits z_ij = x_i . w_j (1 <= k <= 16),
+ * high to low (ties: lower id first), their vocabulary ids and the row's lse,
+ * e.g. the teacher side of a distillation step.  topk_idx, topk_logit: [N, k];
+ * lse: [N].  Needs flce_topk_workspace_bytes(p, k) of workspace.  Labels,
+ * reduction and shift in p are not used. */
+size_t flce_topk_workspace_bytes(const flce_problem_t* p, int32_t k);
+flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const void* W, int32_t* topk_idx,
+                        float* topk_logit, float* lse, void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* flce_soft_fwd_bwd: loss and gradients against sparse soft targets, the student
+ * side of a distillation step.  Row i has k target ids tgt_idx[i, :] with
+ * probabilities q = tgt_prob[i, :] ([N, k], 1 <= k <= 16; entries with q <= 0
+ * are unused; ids distinct).  With p = softmax(x_i W^T):
+ *   loss_i = sum_k q_k log q_k - sum_k q_k log p_{id_k}      (KL(q || p) on the ids)
+ *   G_ij   = s * (Q_i p_ij - sum_k q_k [j = id_k]),  Q_i = sum_k q_k
+ * A row with Q_i = 0 is ignored; mean divides by the rows that are not.  k = 1,
+ * q = 1 is the hard-label cross-entropy.  g = 1 as in flce_fwd_bwd; needs
+ * flce_workspace_bytes(p) (the fused path).  shift must be 0; labels unused. */
+flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                                const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
+                                void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
+
 /* Synchronises `stream`, then returns the status word recorded in ws by the
  * kernels of earlier calls (FLCE_OK if none) and clears it. */
 flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);

@@ -20,7 +20,8 @@ REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
 EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
-            "flce_forward_noalloc", "flce_scale_grads", "flce_status_string")
+            "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
+            "flce_soft_fwd_bwd", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
@@ -65,6 +66,12 @@ def lib():
     L.flce_backward.restype = ctypes.c_int
     L.flce_fwd_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_fwd_bwd.restype = ctypes.c_int
+    L.flce_topk_workspace_bytes.argtypes = [P, ctypes.c_int32]
+    L.flce_topk_workspace_bytes.restype = sz
+    L.flce_topk.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_topk.restype = ctypes.c_int
+    L.flce_soft_fwd_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_soft_fwd_bwd.restype = ctypes.c_int
     L.flce_scale_grads.argtypes = [P, vp, vp, vp, vp]
     L.flce_scale_grads.restype = ctypes.c_int
     L.flce_read_device_status.argtypes = [vp, vp]
@@ -227,6 +234,53 @@ def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
                                              ws.data_ptr(), ws.numel(), s))
     if check:
         _call("device", read_device_status(ws, stream))
+    return loss, lse, dX, dW, ws
+
+
+def topk(x, w, k, ws=None, stream=None):
+    """Per row, the k largest logits of x @ w.T (high to low), their ids and the row's lse.
+    Returns (idx [N,k] int32, logit [N,k] fp32, lse [N] fp32, ws)."""
+    torch = _torch()
+    n, h = x.shape
+    v = w.shape[0]
+    dummy = torch.empty(n, dtype=torch.int32, device=x.device)
+    _check_inputs(x, w, dummy)
+    p = _problem(n, h, v, -100, "mean")
+    if ws is None:
+        nbytes = int(lib().flce_topk_workspace_bytes(ctypes.byref(p), int(k)))
+        if nbytes == 0:
+            raise FlceError(1, "flce_topk_workspace_bytes")
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+    idx = torch.empty(n, k, dtype=torch.int32, device=x.device)
+    val = torch.empty(n, k, dtype=torch.float32, device=x.device)
+    lse = torch.empty(n, dtype=torch.float32, device=x.device)
+    _call("flce_topk", lib().flce_topk(ctypes.byref(p), int(k), x.data_ptr(), w.data_ptr(), idx.data_ptr(),
+                                       val.data_ptr(), lse.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream)))
+    return idx, val, lse, ws
+
+
+def soft_fwd_bwd(x, w, tgt_idx, tgt_prob, reduction="mean", ws=None, stream=None):
+    """KL of sparse soft targets (k ids and probabilities per row) against softmax(x @ w.T),
+    forward and backward.  Returns (loss, lse, dX, dW, ws)."""
+    torch = _torch()
+    n, h = x.shape
+    v = w.shape[0]
+    k = int(tgt_idx.shape[1])
+    if tgt_idx.shape != (n, k) or tgt_prob.shape != (n, k) or tgt_idx.dtype != torch.int32 or \
+            tgt_prob.dtype != torch.float32 or not (tgt_idx.is_contiguous() and tgt_prob.is_contiguous()):
+        raise ValueError("targets must be contiguous [N, k] int32 ids and fp32 probabilities")
+    _check_inputs(x, w, torch.empty(n, dtype=torch.int32, device=x.device))
+    p = _problem(n, h, v, -100, reduction)
+    if ws is None:
+        ws = _alloc_ws(n, h, v, -100, reduction, x.device)
+    loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device)
+    lse = torch.empty(n, dtype=torch.float32, device=x.device)
+    dX = torch.empty_like(x)
+    dW = torch.empty_like(w)
+    _call("flce_soft_fwd_bwd", lib().flce_soft_fwd_bwd(ctypes.byref(p), k, x.data_ptr(), w.data_ptr(),
+                                                       tgt_idx.data_ptr(), tgt_prob.data_ptr(), loss.data_ptr(),
+                                                       lse.data_ptr(), dX.data_ptr(), dW.data_ptr(), ws.data_ptr(),
+                                                       ws.numel(), _stream_ptr(stream)))
     return loss, lse, dX, dW, ws
 
 

@@ -226,7 +226,7 @@ struct Ctx {
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
   float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
   LabelView labels_of(const int32_t* labels) const {
-    return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1};
+    return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1, nullptr, nullptr, 0};
   }
   bool per_row() const { return p->reduction == FLCE_REDUCTION_NONE; }
 };
@@ -459,16 +459,23 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
 // chunk's lse; the fix-up turns p~ into G in place; one launch then computes
 // dX for the chunk's rows (K = V, bf16 out) and adds G^T X into the fp32 dW
 // accumulator (K = chunk rows).
-flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
+flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelView lv, float* loss, float* lse,
                         void* dX, void* dW) {
   const flce_problem_t& p = *c.p;
   const int n = static_cast<int>(p.n), h = static_cast<int>(p.h), v = static_cast<int>(p.v);
+  const int32_t* labels = lv.labels;
   const int vtiles = (v + kBN - 1) / kBN;
   const int h_tiles = (h + kBN - 1) / kBN;
   flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_label_scan_view(n, v, c.labels_of(labels), c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+    return launch_label_scan_view(n, v, lv, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
+  if (lv.soft_k > 0) {  // soft targets: sum_k q_k z_{i, id_k} per row, before any finalize reads it
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_soft_gather(n, h, v, lv.soft_k, X, W, lv.soft_idx, lv.soft_prob, c.tgt(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
+  }
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
     return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, nullptr, c.n_valid(),
                                c.scale(), c.stream);
@@ -513,13 +520,13 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, c.labels_of(labels), c.part_m(), c.part_l(), c.tgt(),
+      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(),
                                       lse, c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(),
                                       c.stream);
     }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, c.labels_of(labels), lse, c.scale(), c.mtile(),
+      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse, c.scale(), c.mtile(),
                           c.g(), c.stream);
     }));
     if (st != FLCE_OK) return st;
@@ -560,6 +567,52 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const int32_
   }));
   if (st != FLCE_OK) return st;
   return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dW, p.v * p.h, c.stream); }));
+}
+
+// Top-k pass: the forward with a per-row best-k list, then the merge.
+size_t topk_extra_bytes(const flce_problem_t& p) {
+  return align_up(static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * (sizeof(float) + sizeof(int32_t)));
+}
+
+flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_t* out_idx, float* out_val, float* lse) {
+  const flce_problem_t& p = *c.p;
+  const Layout base = make_layout(p, false);
+  float* cand_val = reinterpret_cast<float*>(c.ws + base.total);
+  int32_t* cand_idx = reinterpret_cast<int32_t*>(
+      c.ws + base.total + static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * sizeof(float));
+  TcMaps maps;
+  if (!make_map(&maps.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
+  if (!make_map(&maps.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
+  maps.out = maps.a2 = maps.b2 = maps.out2 = maps.a;
+  TcParams tp{};
+  tp.n = static_cast<int>(p.n);
+  tp.h = static_cast<int>(p.h);
+  tp.v = static_cast<int>(p.v);
+  tp.ignore_index = p.ignore_index;
+  tp.timeout_ns = timeout_ns();
+  tp.status = c.status();
+  tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
+  tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
+  tp.vsplit = std::min(kTopkSplit, std::max(1, std::min(tp.vocab_tiles, choose_vsplit(tp.row_tiles, tp.vocab_tiles,
+                                                                                        c.dev.sms / 2))));
+  tp.part_m = c.part_m();
+  tp.part_l = c.part_l();
+  tp.tgt = c.tgt();
+  tp.labels = nullptr;
+  tp.r0 = 0;
+  tp.row_end = tp.n;
+  tp.topk_val = cand_val;
+  tp.topk_idx = cand_idx;
+  tp.topk_k = k;
+  const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
+  const int grid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
+  flce_status_t st =
+      cuda_status(timed(0, flops, c.stream, [&] { return launch_tc(kModeTopk, maps, tp, grid, c.stream); }));
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_topk_finalize(tp.n, tp.vsplit, k, c.part_m(), c.part_l(), cand_val, cand_idx, lse, out_val, out_idx,
+                                c.stream);
+  }));
 }
 
 }  // namespace
@@ -627,7 +680,7 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   Ctx c;
   flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
-  if (c.L.rows > 0) return run_fused(c, X, W, labels, loss, lse, dX, dW);
+  if (c.L.rows > 0) return run_fused(c, X, W, c.labels_of(labels), loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
   if (st != FLCE_OK) return st;
   return run_backward(c, X, W, labels, lse, nullptr, dX, dW);
@@ -662,6 +715,42 @@ flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns
   if (limit_ns == 0 || limit_ns > 10000000000ull) return FLCE_ERR_INVALID_ARGUMENT;
   if (cudaMemsetAsync(ws, 0, sizeof(int), reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess) return FLCE_ERR_CUDA;
   return cuda_status(launch_timeout_selftest(static_cast<int*>(ws), limit_ns, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+size_t flce_topk_workspace_bytes(const flce_problem_t* p, int32_t k) {
+  if (check_problem(p) != FLCE_OK || k < 1 || k > kTopkMax) return 0;
+  return make_layout(*p, false).total + topk_extra_bytes(*p);
+}
+
+flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const void* W, int32_t* topk_idx,
+                        float* topk_logit, float* lse, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!X || !W || !topk_idx || !topk_logit || !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  if (k < 1 || k > kTopkMax) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(topk_idx, 4) || !aligned(topk_logit, 4) || !aligned(lse, 4))
+    return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  if (st != FLCE_OK) return st;
+  if (ws_bytes < flce_topk_workspace_bytes(p, k)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  c.L = make_layout(*p, false);
+  return run_topk(c, k, X, W, topk_idx, topk_logit, lse);
+}
+
+flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                                const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
+                                void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!X || !W || !tgt_idx || !tgt_prob || !loss || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (k < 1 || k > kTopkMax) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p && p->shift) return FLCE_ERR_INVALID_ARGUMENT;  // targets are given per row
+  if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(tgt_idx, 4) ||
+      !aligned(tgt_prob, 4) || !aligned(lse, 4) || !aligned(loss, 4))
+    return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  if (st != FLCE_OK) return st;
+  if (c.L.rows == 0) return FLCE_ERR_WORKSPACE_TOO_SMALL;  // needs flce_workspace_bytes(p)
+  const LabelView lv{nullptr, p->ignore_index, 0, 1, tgt_idx, tgt_prob, k};
+  return run_fused(c, X, W, lv, loss, lse, dX, dW);
 }
 
 flce_status_t flce_profile_enable(int on) {

@@ -20,6 +20,7 @@ enum : int {
 // Label of `row`: labels[row], or with shift labels[row + 1] and ignore_index
 // for the last row of each sequence of seq_len rows.
 __device__ __forceinline__ int label_at(const int32_t* labels, int row, int shift, int seq_len, int ignore_index) {
+  if (!labels) return ignore_index;  // soft targets: no hard label
   if (!shift) return labels[row];
   return ((row + 1) % seq_len == 0) ? ignore_index : labels[row + 1];
 }

@@ -32,7 +32,10 @@ inline int pair_grid(int sms, long long pair_work) {
 // workspace holds one chunk of G, N x chunk bf16.
 int chunk_width(int64_t n);
 
-enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3 };
+enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3, kModeTopk = 4 };
+
+constexpr int kTopkMax = 16;     // largest k of flce_topk / of soft targets per row
+constexpr int kTopkSplit = 8;    // most vocabulary splits of the top-k pass (bounds its partial buffer)
 
 // Output format of the dX / dW tiles of a kModeBwd launch.
 enum OutMode : int { kOutF32Store = 0, kOutF32Add = 1, kOutBF16 = 2 };
@@ -67,6 +70,10 @@ struct TcParams {
   // row chunk of the forward-store pass: rows [r0, row_end) (row_end 0 means n)
   int r0, row_end;
   float* mtile;         // forward-store: per (chunk row, vocabulary tile) max, log2 units
+  // top-k pass: per (split, row) the best topk_k (logit, id) pairs, [vsplit][n][kTopkMax]
+  float* topk_val;
+  int32_t* topk_idx;
+  int topk_k;
 };
 
 struct TcMaps {
@@ -86,9 +93,13 @@ cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, cons
 // Labels as the kernels read them: with shift, row i takes labels[i + 1] and
 // the last row of each sequence of seq_len rows is ignored.
 struct LabelView {
-  const int32_t* labels;
+  const int32_t* labels;   // hard labels (may be null when soft targets are given)
   int ignore_index;
   int shift, seq_len;
+  // soft targets: per row soft_k (vocabulary id, probability) pairs; soft_k = 0 for hard labels
+  const int32_t* soft_idx;
+  const float* soft_prob;
+  int soft_k;
 };
 
 cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
@@ -96,6 +107,11 @@ cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
                          const float* scale, const float* mtile, void* P, cudaStream_t stream);
+cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,
+                               const float* prob, float* tgt, cudaStream_t stream);
+cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
+                                 const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
+                                 int32_t* out_idx, cudaStream_t stream);
 cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
                                    cudaStream_t stream);
 cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss,

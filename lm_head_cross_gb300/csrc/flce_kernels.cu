@@ -90,7 +90,7 @@ template <int MODE>
 constexpr bool kDynamic = (MODE == kModeBwd);
 
 template <int MODE>
-constexpr bool kUnits = (MODE == kModeForward || MODE == kModeFwdStore);
+constexpr bool kUnits = (MODE == kModeForward || MODE == kModeFwdStore || MODE == kModeTopk);
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -412,6 +412,13 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   uint32_t acc_phase = 0;
 
   // forward state (one row per thread)
+  float tk_val[kTopkMax];
+  int tk_idx[kTopkMax];
+#pragma unroll
+  for (int i = 0; i < kTopkMax; ++i) {
+    tk_val[i] = -INFINITY;
+    tk_idx[i] = -1;
+  }
   float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
   bool found = false;
   int y_fwd = p.ignore_index;
@@ -435,8 +442,15 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_l = 0.f;
         found = false;
         y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
+        if (MODE == kModeTopk) {
+#pragma unroll
+          for (int i = 0; i < kTopkMax; ++i) {
+            tk_val[i] = -INFINITY;
+            tk_idx[i] = -1;
+          }
+        }
       }
-      if (MODE == kModeForward) {
+      if (MODE == kModeForward || MODE == kModeTopk) {
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           const int col0 = t.n0 + c * 32;
@@ -469,6 +483,27 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
           run_l = run_l * fast_exp2(run_m - new_m) + sum;
           run_m = new_m;
+          if (MODE == kModeTopk && cmax > tk_val[kTopkMax - 1]) {
+            // keep the row's best kTopkMax (logit, id), sorted high to low
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              float x = __uint_as_float(v[j]);
+              if (x > tk_val[kTopkMax - 1]) {
+                int xi = col0 + j;
+#pragma unroll
+                for (int i = 0; i < kTopkMax; ++i) {
+                  if (x > tk_val[i]) {
+                    const float tv = tk_val[i];
+                    const int ti = tk_idx[i];
+                    tk_val[i] = x;
+                    tk_idx[i] = xi;
+                    x = tv;
+                    xi = ti;
+                  }
+                }
+              }
+            }
+          }
         }
         release_accumulator(&tempty[acc], lane);
       } else {
@@ -525,6 +560,14 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         p.part_m[static_cast<int64_t>(t.split) * p.n + row] = run_m;
         p.part_l[static_cast<int64_t>(t.split) * p.n + row] = run_l;
         if (found) p.tgt[row] = z_tgt;
+        if (MODE == kModeTopk) {
+          const int64_t base = (static_cast<int64_t>(t.split) * p.n + row) * kTopkMax;
+#pragma unroll
+          for (int i = 0; i < kTopkMax; ++i) {
+            p.topk_val[base + i] = tk_val[i];
+            p.topk_idx[base + i] = tk_idx[i];
+          }
+        }
       }
     } else if (MODE == kModeGrad) {
       const int row = t.m0 + r;
@@ -709,13 +752,31 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
       l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
     const float lse = (m + log2f(l)) * kLn2;
     lse_out[row] = lse;
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
-    if (y != ignore_index) {
-      if (y >= 0 && y < v) {
+    if (lv.soft_k > 0) {
+      // KL(q || p) over the row's target ids: sum_k q_k log q_k + Q lse - sum_k q_k z_k
+      double Q = 0.0, C = 0.0;
+      for (int k = 0; k < lv.soft_k; ++k) {
+        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + k];
+        const int id = lv.soft_idx[static_cast<int64_t>(row) * lv.soft_k + k];
+        if (q > 0.f) {
+          if (id < 0 || id >= v) atomicCAS(status, 0, kErrLabel);
+          Q += q;
+          C += static_cast<double>(q) * log(static_cast<double>(q));
+        }
+      }
+      if (Q > 0.0) {
         valid = 1;
-        li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
-      } else {
-        atomicCAS(status, 0, kErrLabel);
+        li = C + Q * static_cast<double>(lse) - static_cast<double>(tgt[row]);
+      }
+    } else {
+      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
+      if (y != ignore_index) {
+        if (y >= 0 && y < v) {
+          valid = 1;
+          li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
+        } else {
+          atomicCAS(status, 0, kErrLabel);
+        }
       }
     }
     if (loss_rows) loss_rows[row] = static_cast<float>(li);
@@ -744,10 +805,31 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
                                                     const float* __restrict__ lse, const float* __restrict__ scale,
                                                     const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
   constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
+  __shared__ int s_idx[kTopkMax];
+  __shared__ float s_q[kTopkMax];
+  __shared__ float s_mass;
   const int lrow = blockIdx.x;
   const int row = r0 + lrow;
   const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-  const float coef = (y != lv.ignore_index) ? *scale : 0.f;
+  float coef = (y != lv.ignore_index) ? *scale : 0.f;
+  const int nsoft = lv.soft_k;
+  if (nsoft > 0) {
+    // soft targets: G = s (Q p - sum_k q_k [j = id_k]), Q = sum_k q_k
+    if (threadIdx.x < nsoft) {
+      const float q = lv.soft_prob[static_cast<int64_t>(row) * nsoft + threadIdx.x];
+      s_q[threadIdx.x] = q > 0.f ? q : 0.f;
+      s_idx[threadIdx.x] = lv.soft_idx[static_cast<int64_t>(row) * nsoft + threadIdx.x];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+      for (int k = 0; k < nsoft; ++k) m += s_q[k];
+      s_mass = m;
+    }
+    __syncthreads();
+    coef = s_mass > 0.f ? *scale : 0.f;
+  }
+  const float mass = nsoft > 0 ? s_mass : 1.f;
   const float lse2 = lse[row] * kLog2e;
   uint4* prow = reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp);
   const float* mt = mtile + static_cast<int64_t>(lrow) * vtiles;
@@ -764,16 +846,27 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
       const int q = base + k * blockDim.x;
       if (q >= nvec) break;
       const int j0 = q * 8;
-      const float c = coef * fast_exp2(mt[j0 / kBN] - lse2);
+      const float c = coef * mass * fast_exp2(mt[j0 / kBN] - lse2);
       const uint32_t in[4] = {u[k].x, u[k].y, u[k].z, u[k].w};
+      float sub[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) sub[e] = (j0 + e == y) ? coef : 0.f;
+      for (int t = 0; t < nsoft; ++t) {
+        const int d = s_idx[t] - j0;
+        if (static_cast<unsigned>(d) < 8u) {
+#pragma unroll
+          for (int e = 0; e < 8; ++e)
+            if (e == d) sub[e] += coef * s_q[t];
+        }
+      }
       uint32_t out[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int j = j0 + 2 * e;
         const float lo = __uint_as_float(in[e] << 16);
         const float hi = __uint_as_float(in[e] & 0xFFFF0000u);
-        const float g0 = (j < v) ? fmaf(lo, c, (j == y) ? -coef : 0.f) : 0.f;
-        const float g1 = (j + 1 < v) ? fmaf(hi, c, (j + 1 == y) ? -coef : 0.f) : 0.f;
+        const float g0 = (j < v) ? fmaf(lo, c, -sub[2 * e]) : 0.f;
+        const float g1 = (j + 1 < v) ? fmaf(hi, c, -sub[2 * e + 1]) : 0.f;
         out[e] = pack_bf16x2(g0, g1);
       }
       prow[q] = make_uint4(out[0], out[1], out[2], out[3]);
@@ -791,12 +884,25 @@ __global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int
   const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
   int valid = 0;
   if (row < n) {
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
-    if (y != ignore_index) {
-      if (y >= 0 && y < v)
-        valid = 1;
-      else
-        atomicCAS(status, 0, kErrLabel);
+    if (lv.soft_k > 0) {
+      float Q = 0.f;
+      for (int k = 0; k < lv.soft_k; ++k) {
+        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + k];
+        const int id = lv.soft_idx[static_cast<int64_t>(row) * lv.soft_k + k];
+        if (q > 0.f) {
+          Q += q;
+          if (id < 0 || id >= v) atomicCAS(status, 0, kErrLabel);
+        }
+      }
+      valid = Q > 0.f;
+    } else {
+      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
+      if (y != ignore_index) {
+        if (y >= 0 && y < v)
+          valid = 1;
+        else
+          atomicCAS(status, 0, kErrLabel);
+      }
     }
   }
   s_valid[threadIdx.x] = valid;
@@ -852,6 +958,90 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
     *n_valid_out = static_cast<int>(nv);
     *scale_out = static_cast<float>(scale);
   }
+}
+
+// Soft targets: tgt_i = sum_k q_ik (x_i . w_{id_ik}), one warp per row, fp32
+// accumulation of the bf16 products (ids with q <= 0 or out of range skipped).
+__global__ void __launch_bounds__(256) soft_gather_kernel(int n, int h, int v, int k, const __nv_bfloat16* __restrict__ X,
+                                                          const __nv_bfloat16* __restrict__ W,
+                                                          const int32_t* __restrict__ idx,
+                                                          const float* __restrict__ prob, float* __restrict__ tgt) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (warp >= n) return;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(warp) * h);
+  float acc = 0.f;
+  for (int t = 0; t < k; ++t) {
+    const float q = prob[static_cast<int64_t>(warp) * k + t];
+    const int id = idx[static_cast<int64_t>(warp) * k + t];
+    if (!(q > 0.f) || id < 0 || id >= v) continue;
+    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(id) * h);
+    float dot = 0.f;
+    for (int c = lane; c < h / 8; c += 32) {
+      const uint4 a = xr[c], b = wr[c];
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
+        dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    acc = fmaf(q, dot, acc);
+  }
+  if (lane == 0) tgt[warp] = acc;
+}
+
+// Top-k pass: merge the per-split candidates of each row into its best k
+// (logit, id), high to low, and its log-sum-exp.
+__global__ void __launch_bounds__(128) topk_finalize_kernel(int n, int vsplit, int k, const float* __restrict__ part_m,
+                                                            const float* __restrict__ part_l,
+                                                            const float* __restrict__ cand_val,
+                                                            const int32_t* __restrict__ cand_idx,
+                                                            float* __restrict__ lse_out, float* __restrict__ out_val,
+                                                            int32_t* __restrict__ out_idx) {
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  float m = -INFINITY;
+  for (int s = 0; s < vsplit; ++s) m = fmaxf(m, part_m[static_cast<int64_t>(s) * n + row]);
+  float l = 0.f;
+  for (int s = 0; s < vsplit; ++s)
+    l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
+  lse_out[row] = (m + log2f(l)) * kLn2;
+  float bv[kTopkMax];
+  int bi[kTopkMax];
+#pragma unroll
+  for (int i = 0; i < kTopkMax; ++i) {
+    bv[i] = -INFINITY;
+    bi[i] = -1;
+  }
+  for (int s = 0; s < vsplit; ++s) {
+    const int64_t base = (static_cast<int64_t>(s) * n + row) * kTopkMax;
+    for (int c = 0; c < kTopkMax; ++c) {
+      float x = cand_val[base + c];
+      int xi = cand_idx[base + c];
+      if (!(x > bv[kTopkMax - 1])) continue;
+#pragma unroll
+      for (int i = 0; i < kTopkMax; ++i) {
+        // ties keep the lower vocabulary id first
+        if (x > bv[i] || (x == bv[i] && xi >= 0 && (bi[i] < 0 || xi < bi[i]))) {
+          const float tv = bv[i];
+          const int ti = bi[i];
+          bv[i] = x;
+          bi[i] = xi;
+          x = tv;
+          xi = ti;
+        }
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < kTopkMax; ++i)
+    if (i < k) {
+      out_val[static_cast<int64_t>(row) * k + i] = bv[i];
+      out_idx[static_cast<int64_t>(row) * k + i] = bi[i];
+    }
 }
 
 __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t count8) {
@@ -923,6 +1113,7 @@ cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid,
     case kModeGrad: return launch_mode<kModeGrad>(maps, p, grid, stream);
     case kModeBwd: return launch_mode<kModeBwd>(maps, p, grid, stream);
     case kModeFwdStore: return launch_mode<kModeFwdStore>(maps, p, grid, stream);
+    case kModeTopk: return launch_mode<kModeTopk>(maps, p, grid, stream);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -979,6 +1170,22 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
   convert_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), count8);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,
+                               const float* prob, float* tgt, cudaStream_t stream) {
+  const int blocks = (n + 7) / 8;  // 8 warps per block, one row each
+  soft_gather_kernel<<<blocks, 256, 0, stream>>>(n, h, v, k, static_cast<const __nv_bfloat16*>(X),
+                                                 static_cast<const __nv_bfloat16*>(W), idx, prob, tgt);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
+                                 const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
+                                 int32_t* out_idx, cudaStream_t stream) {
+  topk_finalize_kernel<<<(n + 127) / 128, 128, 0, stream>>>(n, vsplit, k, part_m, part_l, cand_val, cand_idx, lse,
+                                                             out_val, out_idx);
   return cudaGetLastError();
 }
 

@@ -187,3 +187,61 @@ def full_bf16(problem, grad_output: float = 1.0):
     """``full`` on a ``synth.Problem`` (bf16 bits widened exactly)."""
     return full(widen_bf16(problem.X), widen_bf16(problem.W), problem.labels,
                 problem.ignore_index, problem.reduction, grad_output)
+
+
+# ----------------------------------------------------------------------------- distillation without full logits
+# "What-Each-Parallelism-Actually-Shards" §7.6 suggests keeping only top-k logits
+# (or a chunked KL) for distillation instead of returning [B,S,V] logits.
+
+def topk(X, W, k: int):
+    """Per row: the k largest logits (high to low; ties keep the lower id first),
+    their ids, and the row's lse."""
+    X = np.asarray(X, np.float64)
+    W = np.asarray(W, np.float64)
+    n = X.shape[0]
+    idx = np.empty((n, k), dtype=np.int64)
+    val = np.empty((n, k), dtype=np.float64)
+    lse = np.empty(n, dtype=np.float64)
+    for blk in _row_blocks(n, W.shape[0]):
+        z = X[blk] @ W.T
+        order = np.argsort(-z, axis=1, kind="stable")[:, :k]
+        idx[blk] = order
+        val[blk] = np.take_along_axis(z, order, axis=1)
+        m = z.max(axis=1)
+        lse[blk] = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    return idx, val, lse
+
+
+def soft_full(X, W, tgt_idx, tgt_prob, reduction: str = "mean", grad_output=1.0):
+    """KL(q || p) of sparse soft targets per row against p = softmax(X W^T):
+    loss_i = sum_k q_k log q_k - sum_k q_k log p_{id_k} (entries with q <= 0 unused;
+    a row with no positive mass is ignored), and the gradients of g * loss."""
+    X = np.asarray(X, np.float64)
+    W = np.asarray(W, np.float64)
+    idx = np.asarray(tgt_idx, dtype=np.int64)
+    q = np.where(np.asarray(tgt_prob, np.float64) > 0, np.asarray(tgt_prob, np.float64), 0.0)
+    n = X.shape[0]
+    z = X @ W.T
+    m = z.max(axis=1)
+    lse = m + np.log(np.exp(z - m[:, None]).sum(axis=1))
+    logp = z - lse[:, None]
+    Q = q.sum(axis=1)
+    valid = Q > 0
+    ent = np.where(q > 0, q * np.log(np.where(q > 0, q, 1.0)), 0.0).sum(axis=1)
+    cross = (q * np.take_along_axis(logp, idx, axis=1)).sum(axis=1)
+    loss_rows = np.where(valid, ent - cross, 0.0)
+    n_valid = int(valid.sum())
+    if reduction == "mean":
+        loss = 0.0 if n_valid == 0 else float(loss_rows.sum()) / n_valid
+    elif reduction == "sum":
+        loss = float(loss_rows.sum())
+    elif reduction == "none":
+        loss = loss_rows.copy()
+    else:
+        raise ValueError(reduction)
+    s = grad_scale(n_valid, reduction, grad_output)
+    G = np.exp(logp) * Q[:, None]
+    np.add.at(G, (np.repeat(np.arange(n), idx.shape[1]), idx.reshape(-1)), -q.reshape(-1))
+    G[~valid] = 0.0
+    G = (np.reshape(s, (-1, 1)) if np.ndim(s) else s) * G
+    return dict(loss=loss, lse=lse, loss_rows=loss_rows, n_valid=n_valid, dX=G @ W, dW=G.T @ X)

@@ -291,6 +291,58 @@ def test_shift_matches_causal_lm_loss():
     np.testing.assert_allclose(f["dW"], tW.grad.numpy(), rtol=1e-10, atol=1e-13)
 
 
+def test_soft_targets_k1_equals_hard_labels():
+    """One target id with probability 1 per row is the hard-label cross-entropy."""
+    rng = np.random.default_rng(33)
+    X, W, y = _rand_problem(rng, 19, 6, 13, ignore_frac=0.0)
+    for red in ("mean", "sum"):
+        a = oracle.full(X, W, y, IGN, red)
+        b = oracle.soft_full(X, W, y[:, None], np.ones((19, 1)), red)
+        assert abs(a["loss"] - b["loss"]) < 1e-12
+        np.testing.assert_allclose(a["dX"], b["dX"], rtol=0, atol=1e-13)
+        np.testing.assert_allclose(a["dW"], b["dW"], rtol=0, atol=1e-13)
+
+
+def test_soft_targets_match_torch_kl_div():
+    """Sparse soft targets against torch's KL divergence on dense targets (float64, autograd);
+    a row with no positive mass contributes nothing."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(34)
+    n, h, v, k = 17, 8, 21, 5
+    X, W, _ = _rand_problem(rng, n, h, v, ignore_frac=0.0)
+    idx = np.stack([rng.permutation(v)[:k] for _ in range(n)])
+    q = rng.random((n, k))
+    q[:, -1] = 0.0
+    q /= q.sum(axis=1, keepdims=True)
+    q[3] = 0.0                                    # no mass: ignored
+    dense = np.zeros((n, v))
+    np.put_along_axis(dense, idx, q, axis=1)
+    f = oracle.soft_full(X, W, idx, q, "mean")
+    tX = torch.tensor(X, requires_grad=True)
+    tW = torch.tensor(W, requires_grad=True)
+    logp = F.log_softmax(tX @ tW.T, dim=1)
+    total = F.kl_div(logp, torch.tensor(dense), reduction="sum")
+    (total / (n - 1)).backward()
+    assert abs(f["loss"] - total.item() / (n - 1)) < 1e-12
+    np.testing.assert_allclose(f["dX"], tX.grad.numpy(), rtol=1e-10, atol=1e-13)
+    np.testing.assert_allclose(f["dW"], tW.grad.numpy(), rtol=1e-10, atol=1e-13)
+    assert np.all(f["dX"][3] == 0.0) and f["n_valid"] == n - 1
+
+
+def test_topk_matches_torch():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(35)
+    X, W, _ = _rand_problem(rng, 12, 7, 40, ignore_frac=0.0)
+    idx, val, lse = oracle.topk(X, W, 6)
+    z = torch.tensor(X) @ torch.tensor(W).T
+    tv, ti = torch.topk(z, 6, dim=1)
+    np.testing.assert_allclose(val, tv.numpy(), rtol=0, atol=1e-13)
+    assert np.array_equal(idx, ti.numpy())
+    np.testing.assert_allclose(lse, torch.logsumexp(z, dim=1).numpy(), rtol=0, atol=1e-12)
+    assert np.array_equal(oracle.topk(X, W, 1)[0][:, 0], np.argmax(X @ W.T, axis=1))
+
+
 def test_mean_with_no_valid_row():
     """Reading taken where the pages are silent: no valid row under mean gives 0, not NaN."""
     rng = np.random.default_rng(23)
