@@ -47,6 +47,12 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--op", choices=["fwd_bwd", "topk", "soft"], default="fwd_bwd",
+                    help="fwd_bwd: fused loss + gradients (the benchmark); topk: per-row top-k logits; "
+                         "soft: KL against sparse soft targets, forward + backward")
+    ap.add_argument("--k", type=int, default=8, help="k of --op topk / soft")
+    ap.add_argument("--reduction", choices=["mean", "sum", "none"], default=None, help="override the workload's")
+    ap.add_argument("--shift", type=int, default=0, help="1: causal next-token shift inside the kernels")
     return ap.parse_args()
 
 
@@ -258,8 +264,27 @@ def run_flce(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
 
-    def step():
-        flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction, ws=ws, out=out)
+    reduction = args.reduction or problem.reduction
+    if args.op == "fwd_bwd":
+        if reduction == "none":
+            out = (torch.empty(n, dtype=torch.float32, device=dev),) + out[1:]
+        seq = n if args.shift else 0
+
+        def step():
+            flce.fwd_bwd(X, W, y, problem.ignore_index, reduction, ws=ws, out=out, shift=args.shift, seq_len=seq)
+    elif args.op == "topk":
+        tk_ws = torch.empty(flce.topk_workspace_bytes(n, h, v, args.k), dtype=torch.uint8, device=dev)
+
+        def step():
+            flce.topk(X, W, args.k, ws=tk_ws)
+    else:
+        g = torch.Generator(device="cpu").manual_seed(5)
+        sidx = torch.stack([torch.randperm(v, generator=g)[:args.k] for _ in range(min(n, 64))])
+        sidx = sidx.repeat((n + 63) // 64, 1)[:n].to(torch.int32).contiguous().to(dev)
+        sq = torch.softmax(torch.randn(n, args.k, generator=g), dim=1).to(torch.float32).contiguous().to(dev)
+
+        def step():
+            flce.soft_fwd_bwd(X, W, sidx, sq, reduction, ws=ws)
 
     # extra device memory of one call beyond its inputs and outputs
     torch.cuda.synchronize()
@@ -273,6 +298,8 @@ def run_flce(args, rank, world, local_rank):
     del tmp_out
     if st != 0:
         raise RuntimeError(f"device status {flce.status_string(st)}")
+    if args.op != "fwd_bwd" or args.reduction or args.shift:
+        return run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, stream)
 
     for _ in range(max(3, args.warmup)):
         step()
@@ -382,6 +409,49 @@ def run_flce(args, rank, world, local_rank):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(problem, args.cpu_seconds)
     print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, stream):
+    """A non-default operation or option: same timing discipline, its own metric line."""
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in starts + ends:
+        e.record(stream)
+    torch.cuda.synchronize()
+    flce.profile_enable(True)
+    for i in range(args.steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    prof = flce.profile_read()
+    flce.profile_enable(False)
+    total_ms = max_over_ranks(sum(s.elapsed_time(e) for s, e in zip(starts, ends)), dist, dev)
+    credited = (2.0 if args.op == "topk" else 6.0) * n * h * v
+    if dist is not None:
+        dist.destroy_process_group()
+    if int(os.environ.get("RANK", "0")) != 0:
+        return 0
+    peaks, peak_src = load_peaks()
+    value = job_tflops(world, credited, args.steps, total_ms)
+    names = {"fwd_bwd": "fused linear-CE fwd+bwd TFLOP/s (6NHV)", "topk": "per-row top-k logits TFLOP/s (2NHV)",
+             "soft": "fused linear + sparse-target KL fwd+bwd TFLOP/s (6NHV)"}
+    print(json.dumps({
+        "metric": names[args.op], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(args.config, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+                                       world), op=args.op, k=args.k, reduction=args.reduction, shift=args.shift),
+        "frac_of_peak": value / world / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
+        "peak_src": peak_src,
+        "kernels": {k: {"launches": a, "ms": b, "tflop": c / 1e12} for k, (a, b, c) in prof.items()},
+        "gpu_launches": sum(x[0] for x in prof.values()),
+    }), flush=True)
     return 0
 
 

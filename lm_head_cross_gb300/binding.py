@@ -237,6 +237,11 @@ def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
     return loss, lse, dX, dW, ws
 
 
+def topk_workspace_bytes(n, h, v, k) -> int:
+    p = _problem(n, h, v, -100, "mean")
+    return int(lib().flce_topk_workspace_bytes(ctypes.byref(p), int(k)))
+
+
 def topk(x, w, k, ws=None, stream=None):
     """Per row, the k largest logits of x @ w.T (high to low), their ids and the row's lse.
     Returns (idx [N,k] int32, logit [N,k] fp32, lse [N] fp32, ws)."""

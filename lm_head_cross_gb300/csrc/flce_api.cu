@@ -167,9 +167,9 @@ flce_status_t device_info(Device* d) {
 // round-robin assignment of (row tile, range) units to `grid` CTAs gives the
 // smallest largest per-CTA tile count; a wave then holds about grid/vsplit row
 // tiles, which keeps the X panels it reads resident in L2.
-int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid) {
-  const int lo = std::min(4, vocab_tiles);
-  const int hi = std::min(kMaxSplit, vocab_tiles);
+int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
+  const int hi = std::min(cap, vocab_tiles);
+  const int lo = std::min(4, hi);
   int best = lo;
   long long best_cost = -1;
   for (int vs = lo; vs <= hi; ++vs) {
@@ -193,16 +193,17 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid) {
   return best;
 }
 
-int choose_vsplit(int row_tiles, int vocab_tiles, int grid) {
+int choose_vsplit(int row_tiles, int vocab_tiles, int grid, int cap = kMaxSplit) {
   static std::mutex mu;
-  static int key[3] = {-1, -1, -1};
+  static int key[4] = {-1, -1, -1, -1};
   static int val = 1;
   std::lock_guard<std::mutex> lock(mu);
-  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid) {
-    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid);
+  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid || key[3] != cap) {
+    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid, cap);
     key[0] = row_tiles;
     key[1] = vocab_tiles;
     key[2] = grid;
+    key[3] = cap;
   }
   return val;
 }
@@ -593,8 +594,7 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   tp.status = c.status();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.vsplit = std::min(kTopkSplit, std::max(1, std::min(tp.vocab_tiles, choose_vsplit(tp.row_tiles, tp.vocab_tiles,
-                                                                                        c.dev.sms / 2))));
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kTopkSplit);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();

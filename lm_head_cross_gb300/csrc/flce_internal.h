@@ -35,7 +35,7 @@ int chunk_width(int64_t n);
 enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3, kModeTopk = 4 };
 
 constexpr int kTopkMax = 16;     // largest k of flce_topk / of soft targets per row
-constexpr int kTopkSplit = 8;    // most vocabulary splits of the top-k pass (bounds its partial buffer)
+constexpr int kTopkSplit = 16;   // most vocabulary splits of the top-k pass (bounds its partial buffer)
 
 // Output format of the dX / dW tiles of a kModeBwd launch.
 enum OutMode : int { kOutF32Store = 0, kOutF32Add = 1, kOutBF16 = 2 };

@@ -389,6 +389,61 @@ __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int la
   if (lane == 0) mbar_arrive_cluster(mapa_shared(smem_u32(tempty_acc), 0));
 }
 
+// ----------------------------------------------------------------------------- top-k candidates
+// Each epilogue thread (one row) appends (logit, id) candidates that beat its
+// row's threshold to a buffer in the warp's shared-memory staging area (entry e
+// of lane l at [e][l]: no bank conflicts).  Whenever a lane holds more than
+// kTopkMax, the whole warp compacts that lane's buffer with one 32-wide bitonic
+// sort, keeping the best kTopkMax; the threshold becomes the smallest kept.
+
+constexpr int kTopkCand = 32;
+
+struct TopkBuf {
+  float* val;    // [kTopkCand][32]
+  int* idx;      // [kTopkCand][32]
+  int count;
+  float thr;
+};
+
+__device__ __forceinline__ bool topk_better(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && static_cast<unsigned>(ai) < static_cast<unsigned>(bi));
+}
+
+// Compact the buffers of every lane in `mask` (whole-warp call).
+__device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigned mask) {
+  while (mask) {
+    const int L = __ffs(mask) - 1;
+    mask &= mask - 1;
+    const int cnt = __shfl_sync(0xffffffffu, b.count, L);
+    float v = lane < cnt ? b.val[lane * 32 + L] : -INFINITY;
+    int i = lane < cnt ? b.idx[lane * 32 + L] : -1;
+#pragma unroll
+    for (int kk = 2; kk <= 32; kk <<= 1) {
+#pragma unroll
+      for (int j = kk >> 1; j > 0; j >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+        const int oi = __shfl_xor_sync(0xffffffffu, i, j);
+        const bool keep_better = ((lane & j) == 0) == ((lane & kk) == 0);
+        const bool other_better = topk_better(ov, oi, v, i);
+        if (keep_better ? other_better : !other_better) {
+          v = ov;
+          i = oi;
+        }
+      }
+    }
+    // lanes now hold the candidates high to low; keep the best kTopkMax
+    if (lane < kTopkMax) {
+      b.val[lane * 32 + L] = v;
+      b.idx[lane * 32 + L] = i;
+    }
+    const float kth = __shfl_sync(0xffffffffu, v, kTopkMax - 1);
+    if (lane == L) {
+      b.count = min(cnt, kTopkMax);
+      if (cnt >= kTopkMax) b.thr = kth;
+    }
+  }
+}
+
 // ----------------------------------------------------------------------------- epilogue
 
 template <int MODE>
@@ -412,13 +467,12 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   uint32_t acc_phase = 0;
 
   // forward state (one row per thread)
-  float tk_val[kTopkMax];
-  int tk_idx[kTopkMax];
-#pragma unroll
-  for (int i = 0; i < kTopkMax; ++i) {
-    tk_val[i] = -INFINITY;
-    tk_idx[i] = -1;
-  }
+  TopkBuf tk;
+  tk.val = reinterpret_cast<float*>(stg);
+  tk.idx = reinterpret_cast<int*>(stg + kTopkCand * 32 * sizeof(float));
+  tk.count = 0;
+  tk.thr = -INFINITY;
+  static_assert(kTopkCand * 32 * 8 <= kStagingPerWarp, "top-k candidates fit the staging area");
   float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
   bool found = false;
   int y_fwd = p.ignore_index;
@@ -443,11 +497,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         found = false;
         y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
         if (MODE == kModeTopk) {
-#pragma unroll
-          for (int i = 0; i < kTopkMax; ++i) {
-            tk_val[i] = -INFINITY;
-            tk_idx[i] = -1;
-          }
+          tk.count = 0;
+          tk.thr = -INFINITY;
         }
       }
       if (MODE == kModeForward || MODE == kModeTopk) {
@@ -483,25 +534,23 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
           run_l = run_l * fast_exp2(run_m - new_m) + sum;
           run_m = new_m;
-          if (MODE == kModeTopk && cmax > tk_val[kTopkMax - 1]) {
-            // keep the row's best kTopkMax (logit, id), sorted high to low
+          if (MODE == kModeTopk) {
+            // groups of 8: a buffer holding at most kTopkCand - 8 never overflows, and a
+            // lane is compacted only once it has gathered more than that
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              float x = __uint_as_float(v[j]);
-              if (x > tk_val[kTopkMax - 1]) {
-                int xi = col0 + j;
+            for (int hh = 0; hh < 4; ++hh) {
+              if (cmax > tk.thr) {
 #pragma unroll
-                for (int i = 0; i < kTopkMax; ++i) {
-                  if (x > tk_val[i]) {
-                    const float tv = tk_val[i];
-                    const int ti = tk_idx[i];
-                    tk_val[i] = x;
-                    tk_idx[i] = xi;
-                    x = tv;
-                    xi = ti;
+                for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
+                  const float x = __uint_as_float(v[j]);
+                  if (x > tk.thr) {
+                    tk.val[tk.count * 32 + lane] = x;
+                    tk.idx[tk.count * 32 + lane] = col0 + j;
+                    ++tk.count;
                   }
                 }
               }
+              topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8));
             }
           }
         }
@@ -556,16 +605,17 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(tmax2 - new_m);
         run_m = new_m;
       }
+      if (MODE == kModeTopk && t.last) topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkMax));
       if (t.last && row < row_end) {
         p.part_m[static_cast<int64_t>(t.split) * p.n + row] = run_m;
         p.part_l[static_cast<int64_t>(t.split) * p.n + row] = run_l;
         if (found) p.tgt[row] = z_tgt;
         if (MODE == kModeTopk) {
+          const int kept = tk.count;  // at most kTopkMax (the merge does not need them sorted)
           const int64_t base = (static_cast<int64_t>(t.split) * p.n + row) * kTopkMax;
-#pragma unroll
           for (int i = 0; i < kTopkMax; ++i) {
-            p.topk_val[base + i] = tk_val[i];
-            p.topk_idx[base + i] = tk_idx[i];
+            p.topk_val[base + i] = i < kept ? tk.val[i * 32 + lane] : -INFINITY;
+            p.topk_idx[base + i] = i < kept ? tk.idx[i * 32 + lane] : -1;
           }
         }
       }
