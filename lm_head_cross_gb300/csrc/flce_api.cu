@@ -490,8 +490,12 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
-  if (!make_map(&bm.out2, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
+  CUtensorMap dw_acc_map, dw_bf16_map;
+  if (!make_map(&dw_acc_map, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32))
+    return FLCE_ERR_CUDA;
+  if (!make_map(&dw_bf16_map, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
   const uint64_t pitch = static_cast<uint64_t>(c.L.vp) * 2;
+  const int nchunks = (n + c.L.rows - 1) / c.L.rows;
 
   for (int r0 = 0; r0 < n; r0 += c.L.rows) {
     const int cr = std::min(c.L.rows, n - r0);
@@ -552,7 +556,17 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     bp.dw_k = cr;
     bp.dx_first = 1;
     bp.dx_out = kOutBF16;
-    bp.dw_out = r0 == 0 ? kOutF32Store : kOutF32Add;
+    // dW: the first chunk stores the fp32 accumulator, middle chunks add to it,
+    // the last one adds it to its own part and writes bf16 (a single chunk writes bf16)
+    const bool last = r0 + cr >= n;
+    if (nchunks == 1) {
+      bp.dw_out = kOutBF16;
+      bm.out2 = dw_bf16_map;
+    } else {
+      bp.dw_out = last ? kOutF32AccToBF16 : (r0 == 0 ? kOutF32Store : kOutF32Add);
+      bm.out2 = dw_acc_map;
+      bm.out3 = dw_bf16_map;
+    }
     bp.tile_counter = c.counter();
     st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
     if (st != FLCE_OK) return st;
@@ -566,8 +580,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr,
                                c.per_row() ? nullptr : loss, c.n_valid(), c.scale(), c.stream);
   }));
-  if (st != FLCE_OK) return st;
-  return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dW, p.v * p.h, c.stream); }));
+  return st;
 }
 
 // Top-k pass: the forward with a per-row best-k list, then the merge.

@@ -38,7 +38,12 @@ constexpr int kTopkMax = 16;     // largest k of flce_topk / of soft targets per
 constexpr int kTopkSplit = 16;   // most vocabulary splits of the top-k pass (bounds its partial buffer)
 
 // Output format of the dX / dW tiles of a kModeBwd launch.
-enum OutMode : int { kOutF32Store = 0, kOutF32Add = 1, kOutBF16 = 2 };
+enum OutMode : int {
+  kOutF32Store = 0,      // fp32 through `out`/`out2`
+  kOutF32Add = 1,        // fp32 added at L2 through `out`/`out2`
+  kOutBF16 = 2,          // bf16 through `out`/`out2`
+  kOutF32AccToBF16 = 3,  // dW only: read the fp32 accumulator through `out2`, add, write bf16 through `out3`
+};
 
 // Everything a tensor-core launch needs besides its tensor maps.
 struct TcParams {
@@ -82,7 +87,8 @@ struct TcMaps {
   CUtensorMap out; // grad: G store (bf16 box 64x32); bwd: dX fp32 accumulator (box 32x32)
   CUtensorMap a2;  // bwd: G MN-major (dW A operand, box 64x64)
   CUtensorMap b2;  // bwd: X MN-major (dW B operand, box 64x64)
-  CUtensorMap out2;// bwd: dW bf16 store (box 64x32)
+  CUtensorMap out2;// bwd: dW output (bf16 box 64x32, or the fp32 accumulator, box 32x32)
+  CUtensorMap out3;// bwd, kOutF32AccToBF16: dW bf16 store (box 64x32)
 };
 
 // Launchers (asynchronous on `stream`; return the launch error, if any).

@@ -448,13 +448,16 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
 
 template <int MODE>
 __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& pr, uint8_t* staging, uint64_t* tfull,
-                             uint64_t* tempty, uint32_t tmem_base, TileRing ring, volatile int* abort_flag) {
+                             uint64_t* tempty, uint32_t tmem_base, TileRing ring, uint64_t* ebar,
+                             volatile int* abort_flag) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // a warp may only touch TMEM lanes [32*(warp%4), +32)
   const int r = quarter * 32 + lane;
   uint8_t* stg = staging + (warp - 2) * kStagingPerWarp;
   int sbuf = 0;
+  uint64_t* my_ebar = &ebar[warp - 2];  // TMA loads into this warp's staging buffers
+  uint32_t ephase = 0;
 
   Sched s;
   sched_init<MODE>(p, pr, s);
@@ -653,7 +656,48 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       const CUtensorMap* omap = is_dx ? &maps.out : &maps.out2;
       const int omode = is_dx ? p.dx_out : p.dw_out;
       const int y0 = (is_dx ? p.r0 : p.c0) + t.m0 + quarter * 32;
-      if (omode == kOutBF16) {
+      if (omode == kOutF32AccToBF16) {
+        // last row chunk: dW = accumulator (fp32, earlier chunks) + this chunk, written as bf16
+#pragma unroll 1
+        for (int g = 0; g < kBN / 64; ++g) {
+          if (t.n0 + g * 64 >= p.h) break;
+          if (lane == 0) {
+            bulk_wait_group_read<0>();  // earlier stores are done with both staging buffers
+            mbar_arrive_expect_tx(my_ebar, 2 * kStagingBuf);
+            tma_load_2d(stg, &maps.out2, my_ebar, t.n0 + g * 64, y0);
+            tma_load_2d(stg + kStagingBuf, &maps.out2, my_ebar, t.n0 + g * 64 + 32, y0);
+          }
+          __syncwarp();
+          uint32_t v[64];
+          tmem_ld_32x64(tbase + g * 64, v);
+          if (!mbar_wait(my_ebar, ephase, p.timeout_ns, abort_flag)) {
+            record_timeout(p, pr, abort_flag);
+            break;
+          }
+          ephase ^= 1u;
+          uint32_t w[32];
+#pragma unroll
+          for (int hb = 0; hb < 2; ++hb) {
+            const uint8_t* rowp = stg + hb * kStagingBuf + lane * 128;
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const float4 a = *reinterpret_cast<const float4*>(rowp + ((c ^ (lane & 7)) << 4));
+              const int j = hb * 32 + 4 * c;
+              w[j / 2] = pack_bf16x2(__uint_as_float(v[j]) + a.x, __uint_as_float(v[j + 1]) + a.y);
+              w[j / 2 + 1] = pack_bf16x2(__uint_as_float(v[j + 2]) + a.z, __uint_as_float(v[j + 3]) + a.w);
+            }
+          }
+          __syncwarp();  // every lane has read the fp32 rows before buffer 0 is rewritten
+          stage_rows(stg, lane, w);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&maps.out3, stg, t.n0 + g * 64, y0);
+            bulk_commit_group();
+          }
+          sbuf = 1;  // a store may still read buffer 0
+        }
+      } else if (omode == kOutBF16) {
 #pragma unroll 1
         for (int g = 0; g < kBN / 64; ++g) {
           if (t.n0 + g * 64 >= p.h) break;
@@ -710,6 +754,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   ring.full = bars + 2 * kStages + 6;
   ring.empty = ring.full + kRing;
   ring.slot = reinterpret_cast<volatile int*>(ring.empty + kRing);
+  uint64_t* ebar = ring.empty + kRing + kRing / 2;  // after the 8 slot ints: one per epilogue warp
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -732,6 +777,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       mbar_init(&ring.full[i], 1);
       mbar_init(&ring.empty[i], kRingReaders);
     }
+    for (int i = 0; i < 4; ++i) mbar_init(&ebar[i], 1);
     *abort_flag = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -742,6 +788,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
       tma_prefetch_map(&maps.a2);
       tma_prefetch_map(&maps.b2);
       tma_prefetch_map(&maps.out2);
+      if (p.dw_out == kOutF32AccToBF16) tma_prefetch_map(&maps.out3);
     }
   }
   if (warp == 1) {
@@ -758,7 +805,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && pr.rank == 0) run_mma<MODE>(p, pr, smem, full, empty, tfull, tempty, tmem_base, ring, abort_flag);
   } else {
-    run_epilogue<MODE>(maps, p, pr, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, abort_flag);
+    run_epilogue<MODE>(maps, p, pr, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, ebar, abort_flag);
   }
 
   tc_fence_before_sync();
