@@ -25,11 +25,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
   size_t status, n_valid, scale;  // header words
   size_t counter;                 // tile counter of the dynamically scheduled launches
+  size_t fix_count;               // fused path: rows listed for a full fixup in the current chunk
   size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
   size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
   size_t g;                       // one chunk buffer: recompute path G [N, chunk]; fused path p~/G [rows, Vp]
   size_t dx_acc;                  // fp32 accumulator: recompute path dX [N, H]; fused path dW [V, H]
-  size_t mtile;                   // fused path: per (chunk row, vocabulary tile) max
+  size_t mtile;                   // fused path: per (chunk row, vocabulary tile) reference exponent
+  size_t mref;                    // fused path: per row of X its target logit, log2 units
+  size_t rowscale, fix_list;      // fused path: per chunk row factor f_i; rows listed for a full fixup
+  size_t xs;                      // fused path: f_i x_i for the chunk's rows, bf16 [rows, H]
   size_t total;
   int nblk, chunk;
   int rows;                       // fused path: rows per chunk (0: layout without the fused path)
@@ -62,6 +66,7 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   L.n_valid = off + 4;
   L.scale = off + 8;
   L.counter = off + 16;
+  L.fix_count = off + 20;
   off += kAlign;
   L.blk_loss = off;
   off = align_up(off + sizeof(double) * L.nblk);
@@ -83,6 +88,14 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   off = align_up(off + accbytes);
   L.mtile = off;
   if (fused) off = align_up(off + sizeof(float) * static_cast<size_t>(L.rows) * vtiles);
+  L.mref = off;
+  if (fused) off = align_up(off + sizeof(float) * n);
+  L.rowscale = off;
+  if (fused) off = align_up(off + sizeof(float) * static_cast<size_t>(L.rows));
+  L.fix_list = off;
+  if (fused) off = align_up(off + sizeof(int) * static_cast<size_t>(L.rows));
+  L.xs = off;
+  if (fused) off = align_up(off + 2 * static_cast<size_t>(L.rows) * h);
   L.total = off;
   return L;
 }
@@ -226,6 +239,11 @@ struct Ctx {
   void* g() const { return ws + L.g; }
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
   float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
+  int* fix_count() const { return reinterpret_cast<int*>(ws + L.fix_count); }
+  float* mref() const { return reinterpret_cast<float*>(ws + L.mref); }
+  float* rowscale() const { return reinterpret_cast<float*>(ws + L.rowscale); }
+  int* fix_list() const { return reinterpret_cast<int*>(ws + L.fix_list); }
+  void* xs() const { return ws + L.xs; }
   LabelView labels_of(const int32_t* labels) const {
     return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1, nullptr, nullptr, 0};
   }
@@ -471,6 +489,13 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     return launch_label_scan_view(n, v, lv, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
+  // Hard labels: the forward-store references each row to its target logit,
+  // and only the rows where that fails get the full fixup pass.
+  const bool ref_rows = lv.soft_k == 0;
+  if (ref_rows) {
+    st = cuda_status(timed(3, 0.0, c.stream, [&] { return launch_ref_gather(n, h, v, lv, X, W, c.mref(), c.stream); }));
+    if (st != FLCE_OK) return st;
+  }
   if (lv.soft_k > 0) {  // soft targets: sum_k q_k z_{i, id_k} per row, before any finalize reads it
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
       return launch_soft_gather(n, h, v, lv.soft_k, X, W, lv.soft_idx, lv.soft_prob, c.tgt(), c.stream);
@@ -489,7 +514,9 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   TcMaps bm;  // bwd: G K-major (dX A), W MN-major (dX B), dX bf16 out; G MN-major (dW A), X MN-major (dW B), dW fp32
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
-  if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
+  // dW B operand: X itself, or (per chunk, below) f_i x_i of the chunk's rows
+  if (!ref_rows && !make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK))
+    return FLCE_ERR_CUDA;
   CUtensorMap dw_acc_map, dw_bf16_map;
   if (!make_map(&dw_acc_map, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32))
     return FLCE_ERR_CUDA;
@@ -520,24 +547,50 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.part_l = c.part_l();
     tp.tgt = c.tgt();
     tp.mtile = c.mtile();
+    tp.mref = ref_rows ? c.mref() : nullptr;
+    // tile counter of the backward launch and the fixup list count start at zero
+    st = cuda_status(cudaMemsetAsync(c.counter(), 0, 2 * sizeof(int), c.stream));
+    if (st != FLCE_OK) return st;
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(),
-                                      lse, c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(),
-                                      c.stream);
-    }));
-    if (st != FLCE_OK) return st;
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse, c.scale(), c.mtile(),
-                          c.g(), c.stream);
-    }));
-    if (st != FLCE_OK) return st;
+    if (ref_rows) {
+      const RefRows rr{c.mref(), c.rowscale(), c.fix_list(), c.fix_count(), c.g(), c.L.vp};
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_fwd_finalize_ref(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(), lse,
+                                       c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(), rr,
+                                       c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_fixup_list(cr, c.fix_list(), c.fix_count(), r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse,
+                                 c.mtile(), c.g(), c.dev.sms, c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_row_scale(cr, h, c.rowscale(), static_cast<const uint16_t*>(X) + static_cast<int64_t>(r0) * h,
+                                c.xs(), c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+    } else {
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(), lse,
+                                        c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(),
+                                        c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse, c.scale(), c.mtile(), c.g(),
+                            c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+    }
 
     if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, kBK, kBM)) return FLCE_ERR_CUDA;
     if (!make_map(&bm.a2, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, 64, kBK)) return FLCE_ERR_CUDA;
+    if (ref_rows && !make_map(&bm.b2, c.xs(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, cr, p.h * 2, 64, kBK))
+      return FLCE_ERR_CUDA;
     TcParams bp{};
     bp.n = n;
     bp.h = h;
@@ -547,6 +600,9 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     bp.status = c.status();
     bp.r0 = r0;
     bp.row_end = r0 + cr;
+    bp.b2_r0 = ref_rows ? 0 : r0;
+    bp.rowscale = ref_rows ? c.rowscale() : nullptr;
+    bp.scale = c.scale();
     bp.c0 = 0;
     bp.cw = v;
     bp.h_tiles = h_tiles;
@@ -568,8 +624,6 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
       bm.out3 = dw_bf16_map;
     }
     bp.tile_counter = c.counter();
-    st = cuda_status(cudaMemsetAsync(c.counter(), 0, sizeof(int), c.stream));
-    if (st != FLCE_OK) return st;
     const long long btiles = static_cast<long long>(bp.dx_tiles) + bp.dw_tiles;
     const int bgrid = pair_grid(c.dev.sms, btiles);
     st = cuda_status(

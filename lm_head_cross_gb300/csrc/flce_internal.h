@@ -34,6 +34,10 @@ int chunk_width(int64_t n);
 
 enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3, kModeTopk = 4 };
 
+// Forward-store: a row's p~ is stored relative to its target logit (log2
+// units) unless a tile's max lies more than this above it.
+constexpr float kRefSpan = 64.f;
+
 constexpr int kTopkMax = 16;     // largest k of flce_topk / of soft targets per row
 constexpr int kTopkSplit = 16;   // most vocabulary splits of the top-k pass (bounds its partial buffer)
 
@@ -74,7 +78,10 @@ struct TcParams {
   int* tile_counter;    // bwd: global tile counter, zero at launch
   // row chunk of the forward-store pass: rows [r0, row_end) (row_end 0 means n)
   int r0, row_end;
-  float* mtile;         // forward-store: per (chunk row, vocabulary tile) max, log2 units
+  float* mtile;         // forward-store: per (chunk row, vocabulary tile) reference exponent, log2 units
+  const float* mref;    // forward-store: per row of X its target logit, log2 units (null: tile maxima only)
+  const float* rowscale;  // bwd: per chunk row factor f_i of the stored G / (s f_i) (null: the buffer holds G)
+  int b2_r0;            // bwd: first row of the dW B operand's tensor map
   // top-k pass: per (split, row) the best topk_k (logit, id) pairs, [vsplit][n][kTopkMax]
   float* topk_val;
   int32_t* topk_idx;
@@ -111,6 +118,31 @@ struct LabelView {
 cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
                                      const float* part_l, const float* tgt, float* lse, float* loss_rows,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
+// The rows' side of the target-logit-referenced chunk buffer, once lse is known
+// (rows [r0, r0 + rows)): per row the factor f_i = 2^(ref_i - lse_i log2 e)
+// (0 for rows without a gradient, 1 for rows listed for a full fixup), the
+// target entry G_iy / (s f_i), and the list of rows that a tile stored with
+// its own max.
+struct RefRows {
+  const float* mref;
+  float* rowscale;
+  int* fix_list;
+  int* fix_count;
+  void* P;
+  int64_t vp;
+};
+cudaError_t launch_fwd_finalize_ref(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
+                                    const float* part_l, const float* tgt, float* lse, float* loss_rows,
+                                    double* blk_loss, int* blk_valid, int* status, RefRows rr, cudaStream_t stream);
+// mref_i = x_i . w_{y_i} log2 e for every row with a label in range (0 otherwise).
+cudaError_t launch_ref_gather(int n, int h, int v, LabelView lv, const void* X, const void* W, float* mref,
+                              cudaStream_t stream);
+// Listed rows of a chunk buffer: G / s = p~ 2^(ref - lse log2 e) - [j = y].
+cudaError_t launch_fixup_list(int max_rows, const int* fix_list, const int* fix_count, int r0, int v, int vp,
+                              int vtiles, LabelView lv, const float* lse, const float* mtile, void* P, int grid,
+                              cudaStream_t stream);
+// xs[i, :] = f_i x[i, :] (bf16) for the rows of one chunk.
+cudaError_t launch_row_scale(int rows, int h, const float* f, const void* x, void* xs, cudaStream_t stream);
 cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
                          const float* scale, const float* mtile, void* P, cudaStream_t stream);
 cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,

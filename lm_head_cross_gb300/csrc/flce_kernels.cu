@@ -27,6 +27,8 @@
 // the MMAs; warps 2-5 drain the other of two TMEM accumulators (2 x 256
 // columns) with tcgen05.ld, one row per thread, so row reductions need no
 // shuffles.  Every wait is bounded (see mbar_wait).
+#include <algorithm>
+
 #include "flce_device.cuh"
 #include "flce_internal.h"
 
@@ -265,7 +267,7 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& 
         for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
 #pragma unroll
         for (int j = 0; j < kHalfN / 64; ++j)
-          tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.r0 + k0);
+          tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.b2_r0 + k0);
       }
       if (++stage == kStages) {
         stage = 0;
@@ -479,6 +481,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
   bool found = false;
   int y_fwd = p.ignore_index;
+  float ref_row = -INFINITY;  // forward-store: the row's reference exponent (-inf: every tile uses its own max)
+  bool zero_row = false;      // forward-store: the row has no gradient, p~ is written as 0
   const float scale = (MODE == kModeGrad) ? *p.scale : 0.f;
   const int row_end = p.row_end > 0 ? p.row_end : p.n;
 
@@ -499,6 +503,10 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_l = 0.f;
         found = false;
         y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
+        if (MODE == kModeFwdStore && p.mref) {
+          zero_row = (y_fwd == p.ignore_index) || y_fwd < 0 || y_fwd >= p.v;
+          ref_row = zero_row ? -INFINITY : p.mref[row];
+        }
         if (MODE == kModeTopk) {
           tk.count = 0;
           tk.thr = -INFINITY;
@@ -559,9 +567,11 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         }
         release_accumulator(&tempty[acc], lane);
       } else {
-        // forward-store: the tile's row max first, then p~ = 2^(t - max) as
-        // bf16 into the chunk buffer (exactly 1 at the max, relative error
-        // 2^-9 everywhere), its fp32 sum into the running log-sum-exp.
+        // forward-store: the tile's row max first, then p~ = 2^(t - ref) as
+        // bf16 into the chunk buffer (relative error 2^-9), its fp32 sum into
+        // the running log-sum-exp.  ref is the row's reference exponent (its
+        // target logit) unless the tile's max lies more than kRefSpan above
+        // it, or the row has none; then it is the tile's max.
         float tmax = -INFINITY;
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
@@ -583,6 +593,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
         }
         const float tmax2 = tmax * kLog2e;
+        const float ref = (tmax2 - ref_row > kRefSpan) ? tmax2 : ref_row;
         float sum = 0.f;
 #pragma unroll 1
         for (int g = 0; g < kBN / 64; ++g) {
@@ -595,17 +606,17 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           uint32_t w[32];
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -tmax2)) : 0.f;
-            const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -tmax2)) : 0.f;
+            const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref)) : 0.f;
+            const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref)) : 0.f;
             sum += a + b;
-            w[j] = pack_bf16x2(a, b);
+            w[j] = zero_row ? 0u : pack_bf16x2(a, b);
           }
           stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
         }
         release_accumulator(&tempty[acc], lane);
-        if (row < row_end) p.mtile[static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN] = tmax2;
-        const float new_m = fmaxf(run_m, tmax2);
-        run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(tmax2 - new_m);
+        if (row < row_end) p.mtile[static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN] = ref;
+        const float new_m = fmaxf(run_m, ref);
+        run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(ref - new_m);
         run_m = new_m;
       }
       if (MODE == kModeTopk && t.last) topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkMax));
@@ -656,6 +667,16 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       const CUtensorMap* omap = is_dx ? &maps.out : &maps.out2;
       const int omode = is_dx ? p.dx_out : p.dw_out;
       const int y0 = (is_dx ? p.r0 : p.c0) + t.m0 + quarter * 32;
+      // With per-row factors f the buffer holds G / (s f_i) row by row: a dX row
+      // is scaled by s f_i, a dW tile (whose B operand rows are f_i x_i) by s.
+      float osc = 1.f;
+      if (p.rowscale) {
+        osc = *p.scale;
+        if (is_dx) {
+          const int lr = t.m0 + quarter * 32 + lane;
+          osc = (p.r0 + lr < p.row_end) ? osc * p.rowscale[lr] : 0.f;
+        }
+      }
       if (omode == kOutF32AccToBF16) {
         // last row chunk: dW = accumulator (fp32, earlier chunks) + this chunk, written as bf16
 #pragma unroll 1
@@ -683,8 +704,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             for (int c = 0; c < 8; ++c) {
               const float4 a = *reinterpret_cast<const float4*>(rowp + ((c ^ (lane & 7)) << 4));
               const int j = hb * 32 + 4 * c;
-              w[j / 2] = pack_bf16x2(__uint_as_float(v[j]) + a.x, __uint_as_float(v[j + 1]) + a.y);
-              w[j / 2 + 1] = pack_bf16x2(__uint_as_float(v[j + 2]) + a.z, __uint_as_float(v[j + 3]) + a.w);
+              w[j / 2] = pack_bf16x2(fmaf(__uint_as_float(v[j]), osc, a.x), fmaf(__uint_as_float(v[j + 1]), osc, a.y));
+              w[j / 2 + 1] =
+                  pack_bf16x2(fmaf(__uint_as_float(v[j + 2]), osc, a.z), fmaf(__uint_as_float(v[j + 3]), osc, a.w));
             }
           }
           __syncwarp();  // every lane has read the fp32 rows before buffer 0 is rewritten
@@ -706,7 +728,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           tmem_ld_32x64(tbase + g * 64, v);
           uint32_t w[32];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) w[j] = pack_bf16x2(__uint_as_float(v[2 * j]), __uint_as_float(v[2 * j + 1]));
+          for (int j = 0; j < 32; ++j)
+            w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * osc, __uint_as_float(v[2 * j + 1]) * osc);
           stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, false);
         }
       } else {
@@ -716,6 +739,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           __syncwarp();
           uint32_t v[32];
           tmem_ld_32x32(tbase + c * 32, v);
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * osc);
           stage_and_store(omap, stg, sbuf, lane, v, t.n0 + c * 32, y0, omode == kOutF32Add);
         }
       }
@@ -834,7 +859,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* __restrict__ part_m,
     const float* __restrict__ part_l, const float* __restrict__ tgt, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
-    int* __restrict__ status) {
+    int* __restrict__ status, RefRows rr) {
   const int ignore_index = lv.ignore_index;
   __shared__ double s_loss[kFinalizeThreads];
   __shared__ int s_valid[kFinalizeThreads];
@@ -847,7 +872,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     float l = 0.f;
     for (int s = 0; s < vsplit; ++s)
       l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
-    const float lse = (m + log2f(l)) * kLn2;
+    const float lse2 = m + log2f(l);
+    const float lse = lse2 * kLn2;
     lse_out[row] = lse;
     if (lv.soft_k > 0) {
       // KL(q || p) over the row's target ids: sum_k q_k log q_k + Q lse - sum_k q_k z_k
@@ -875,6 +901,25 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
           atomicCAS(status, 0, kErrLabel);
         }
       }
+      if (rr.mref) {
+        // m is the largest reference the row's tiles used: above the row's
+        // target logit only when some tile was stored relative to its own max
+        const int lrow = row - r0;
+        float f = 0.f;
+        if (valid) {
+          const float ref = rr.mref[row];
+          if (m > ref) {
+            f = 1.f;
+            rr.fix_list[atomicAdd(rr.fix_count, 1)] = lrow;
+          } else {
+            // G_iy / (s f_i) = (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
+            f = exp2f(ref - lse2);
+            const float gy = exp2f(fmaf(tgt[row], kLog2e, -ref)) - exp2f(lse2 - ref);
+            static_cast<__nv_bfloat16*>(rr.P)[static_cast<int64_t>(lrow) * rr.vp + y] = __float2bfloat16_rn(gy);
+          }
+        }
+        rr.rowscale[lrow] = f;
+      }
     }
     if (loss_rows) loss_rows[row] = static_cast<float>(li);
   }
@@ -894,42 +939,12 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
   }
 }
 
-// In place over one row chunk of the forward-store buffer:
-//   G = s * valid * (p~ * 2^(m_tile - lse*log2e) - [j = y])
-// turning the stored, tile-max-scaled probabilities into the gradient of the
-// logits once the row's log-sum-exp is known.  One block per row.
-__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, LabelView lv,
-                                                    const float* __restrict__ lse, const float* __restrict__ scale,
-                                                    const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
+// One row of a chunk buffer: p~ 2^(ref_tile - lse2) times c, less c q at the
+// target ids (q = 1 at y for a hard label), as bf16, in place.
+__device__ __forceinline__ void fixup_row(uint4* __restrict__ prow, const float* __restrict__ mt, int v, float lse2,
+                                          float coef, float mass, int y, int nsoft, const int* s_idx,
+                                          const float* s_q) {
   constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
-  __shared__ int s_idx[kTopkMax];
-  __shared__ float s_q[kTopkMax];
-  __shared__ float s_mass;
-  const int lrow = blockIdx.x;
-  const int row = r0 + lrow;
-  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-  float coef = (y != lv.ignore_index) ? *scale : 0.f;
-  const int nsoft = lv.soft_k;
-  if (nsoft > 0) {
-    // soft targets: G = s (Q p - sum_k q_k [j = id_k]), Q = sum_k q_k
-    if (threadIdx.x < nsoft) {
-      const float q = lv.soft_prob[static_cast<int64_t>(row) * nsoft + threadIdx.x];
-      s_q[threadIdx.x] = q > 0.f ? q : 0.f;
-      s_idx[threadIdx.x] = lv.soft_idx[static_cast<int64_t>(row) * nsoft + threadIdx.x];
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float m = 0.f;
-      for (int k = 0; k < nsoft; ++k) m += s_q[k];
-      s_mass = m;
-    }
-    __syncthreads();
-    coef = s_mass > 0.f ? *scale : 0.f;
-  }
-  const float mass = nsoft > 0 ? s_mass : 1.f;
-  const float lse2 = lse[row] * kLog2e;
-  uint4* prow = reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp);
-  const float* mt = mtile + static_cast<int64_t>(lrow) * vtiles;
   const int nvec = (v + 7) / 8;
   for (int base = threadIdx.x; base < nvec; base += blockDim.x * kUnroll) {
     uint4 u[kUnroll];
@@ -968,6 +983,104 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
       }
       prow[q] = make_uint4(out[0], out[1], out[2], out[3]);
     }
+  }
+}
+
+// In place over one row chunk of the forward-store buffer:
+//   G = s * valid * (p~ * 2^(ref_tile - lse*log2e) - [j = y])
+// turning the stored, reference-scaled probabilities into the gradient of the
+// logits once the row's log-sum-exp is known.  One block per row.
+__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, LabelView lv,
+                                                    const float* __restrict__ lse, const float* __restrict__ scale,
+                                                    const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
+  __shared__ int s_idx[kTopkMax];
+  __shared__ float s_q[kTopkMax];
+  __shared__ float s_mass;
+  const int lrow = blockIdx.x;
+  const int row = r0 + lrow;
+  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+  float coef = (y != lv.ignore_index) ? *scale : 0.f;
+  const int nsoft = lv.soft_k;
+  if (nsoft > 0) {
+    // soft targets: G = s (Q p - sum_k q_k [j = id_k]), Q = sum_k q_k
+    if (threadIdx.x < nsoft) {
+      const float q = lv.soft_prob[static_cast<int64_t>(row) * nsoft + threadIdx.x];
+      s_q[threadIdx.x] = q > 0.f ? q : 0.f;
+      s_idx[threadIdx.x] = lv.soft_idx[static_cast<int64_t>(row) * nsoft + threadIdx.x];
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float m = 0.f;
+      for (int k = 0; k < nsoft; ++k) m += s_q[k];
+      s_mass = m;
+    }
+    __syncthreads();
+    coef = s_mass > 0.f ? *scale : 0.f;
+  }
+  const float mass = nsoft > 0 ? s_mass : 1.f;
+  fixup_row(reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp), mtile + static_cast<int64_t>(lrow) * vtiles,
+            v, lse[row] * kLog2e, coef, mass, y, nsoft, s_idx, s_q);
+}
+
+// Rows of a chunk buffer listed by the finalize (stored at least partly
+// relative to their tiles' maxima): G / s = p~ 2^(ref - lse log2 e) - [j = y].
+// Blocks take list entries round-robin; an empty list costs one launch.
+__global__ void __launch_bounds__(256) fixup_list_kernel(const int* __restrict__ fix_list,
+                                                         const int* __restrict__ fix_count, int r0, int v, int vp,
+                                                         int vtiles, LabelView lv, const float* __restrict__ lse,
+                                                         const float* __restrict__ mtile,
+                                                         __nv_bfloat16* __restrict__ P) {
+  const int count = *fix_count;
+  for (int e = blockIdx.x; e < count; e += gridDim.x) {
+    const int lrow = fix_list[e];
+    const int row = r0 + lrow;
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    fixup_row(reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp),
+              mtile + static_cast<int64_t>(lrow) * vtiles, v, lse[row] * kLog2e, 1.f, 1.f, y, 0, nullptr, nullptr);
+  }
+}
+
+// Target logits in log2 units (the forward-store's row references), one warp
+// per row, fp32 accumulation of the bf16 products.
+__global__ void __launch_bounds__(256) ref_gather_kernel(int n, int h, int v, LabelView lv,
+                                                         const __nv_bfloat16* __restrict__ X,
+                                                         const __nv_bfloat16* __restrict__ W, float* __restrict__ mref) {
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= n) return;
+  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+  float dot = 0.f;
+  if (y >= 0 && y < v) {
+    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * h);
+    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(y) * h);
+    for (int c = lane; c < h / 8; c += 32) {
+      const uint4 a = xr[c], b = wr[c];
+      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
+        dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  }
+  if (lane == 0) mref[row] = dot * kLog2e;
+}
+
+// xs = f_i x_i row by row (8 bf16 per thread and step).
+__global__ void __launch_bounds__(256) row_scale_kernel(int64_t count8, int h8, const float* __restrict__ f,
+                                                        const uint4* __restrict__ x, uint4* __restrict__ xs) {
+  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < count8;
+       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const float c = f[q / h8];
+    const uint4 u = x[q];
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_bf16x2(__uint_as_float(in[e] << 16) * c, __uint_as_float(in[e] & 0xFFFF0000u) * c);
+    xs[q] = make_uint4(o[0], o[1], o[2], o[3]);
   }
 }
 
@@ -1220,7 +1333,41 @@ cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
   const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
   fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse,
-                                                               loss_rows, blk_loss, blk_valid, status);
+                                                               loss_rows, blk_loss, blk_valid, status, RefRows{});
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fwd_finalize_ref(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
+                                    const float* part_l, const float* tgt, float* lse, float* loss_rows,
+                                    double* blk_loss, int* blk_valid, int* status, RefRows rr, cudaStream_t stream) {
+  const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
+  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse,
+                                                               loss_rows, blk_loss, blk_valid, status, rr);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_ref_gather(int n, int h, int v, LabelView lv, const void* X, const void* W, float* mref,
+                              cudaStream_t stream) {
+  const int blocks = (n + 7) / 8;  // 8 rows (warps) per block
+  ref_gather_kernel<<<blocks, 256, 0, stream>>>(n, h, v, lv, static_cast<const __nv_bfloat16*>(X),
+                                                static_cast<const __nv_bfloat16*>(W), mref);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fixup_list(int max_rows, const int* fix_list, const int* fix_count, int r0, int v, int vp,
+                              int vtiles, LabelView lv, const float* lse, const float* mtile, void* P, int grid,
+                              cudaStream_t stream) {
+  grid = std::max(1, std::min(grid, max_rows));
+  fixup_list_kernel<<<grid, 256, 0, stream>>>(fix_list, fix_count, r0, v, vp, vtiles, lv, lse, mtile,
+                                              static_cast<__nv_bfloat16*>(P));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_scale(int rows, int h, const float* f, const void* x, void* xs, cudaStream_t stream) {
+  const int64_t count8 = static_cast<int64_t>(rows) * (h / 8);
+  const int64_t want = (count8 + 255) / 256;
+  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 4096)));
+  row_scale_kernel<<<blocks, 256, 0, stream>>>(count8, h / 8, f, static_cast<const uint4*>(x), static_cast<uint4*>(xs));
   return cudaGetLastError();
 }
 

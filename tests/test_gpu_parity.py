@@ -260,3 +260,24 @@ def test_autograd_none_and_shift():
     assert np.abs(rows.detach().reshape(-1).cpu().numpy() - ref["loss"]).max() <= 2e-3 + 1e-3 * np.abs(ref["loss"]).max()
     assert_grad(x3.grad.reshape(B * S, H).float().cpu().numpy(), ref["dX"], name="dX")
     assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+@pytest.mark.parametrize("red", ["mean", "sum"])
+def test_wide_logit_range_rows(red):
+    """Rows whose target logit lies far below the row's max (some tiles, or the
+    whole row, stored relative to the tiles' own maxima) next to ordinary rows,
+    over two row chunks.  The ordinary rows' dX is checked against its own
+    scale, so the large rows cannot hide an error there."""
+    p = synth.make_problem(1500, 128, 4001, seed=46, labels="uniform", ignore_frac=0.1, reduction=red,
+                           w_std=0.05)
+    xf = synth.bf16_bits_to_f32(p.X)
+    group = np.arange(p.n) % 3           # 0: x1, 1: x16, 2: x64 (powers of two: exact in bf16)
+    xf = xf * np.array([1.0, 16.0, 64.0], np.float32)[group][:, None]
+    p.X = synth.f32_to_bf16_bits(xf)
+    got, ref = check_full(p)
+    for g in range(3):
+        rows = group == g
+        assert_grad(got["dX"][rows], ref["dX"][rows], name=f"dX rows x{[1, 16, 64][g]}")
+    # the x64 rows do have logits spread far past the reference span
+    z = xf[group == 2].astype(np.float64) @ synth.bf16_bits_to_f32(p.W).astype(np.float64).T
+    assert (z.max(axis=1) - z.min(axis=1)).max() > 64 / math.log2(math.e)
