@@ -170,8 +170,12 @@ flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);
  * the bounded waits used by every kernel. */
 flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream);
 
-/* Diagnostics: per-launch device timing.  While profiling is on, every kernel
- * the calls above launch is bracketed by two CUDA events on its stream.
+/* Diagnostics: per-launch device timing.  `mask` selects the kernel kinds to
+ * time (bit k for kind k; 0 turns profiling off, -1 times every kind).  Each
+ * launch of a selected kind is bracketed by two CUDA events on its stream; an
+ * event between two launches keeps the second from starting its launch while
+ * the first drains (the library's kernels otherwise overlap that way), so
+ * select only the kinds to be measured.
  * flce_profile_read synchronises the recorded events and reports, for one
  * kernel kind, the launches recorded, their summed device time (ms) and their
  * summed algorithmic flops.  Kinds: 0 forward projection + online
@@ -180,7 +184,7 @@ flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns
  * kernels (label scan, finalize, reductions, dX cast; 0 flops).  Enabling or
  * disabling clears the totals.  Off by default.  Process-wide, not tied to a
  * workspace. */
-flce_status_t flce_profile_enable(int on);
+flce_status_t flce_profile_enable(int mask);
 flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, double* flops);
 
 /* Forward pass that allocates nothing and takes no workspace.  The pages have

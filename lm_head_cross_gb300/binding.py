@@ -294,8 +294,12 @@ def read_device_status(ws, stream=None) -> int:
     return int(lib().flce_read_device_status(ctypes.c_void_p(ws.data_ptr()), _stream_ptr(stream)))
 
 
-def profile_enable(on: bool = True) -> None:
-    _call("flce_profile_enable", lib().flce_profile_enable(1 if on else 0))
+def profile_enable(on: bool = True, kinds=None) -> None:
+    """Time the launches of the given kernel kinds (names from KERNEL_KINDS; all when None)."""
+    mask = 0
+    if on:
+        mask = -1 if kinds is None else sum(1 << KERNEL_KINDS.index(k) for k in kinds)
+    _call("flce_profile_enable", lib().flce_profile_enable(mask))
 
 
 def profile_read() -> dict:

@@ -265,6 +265,7 @@ struct ProfRecord {
 struct Profiler {
   std::mutex mu;
   bool on = false;
+  int mask = 0;  // bit k: bracket launches of kind k
   std::vector<ProfRecord> records;
   std::vector<cudaEvent_t> pool;
   int64_t launches[kKinds] = {};
@@ -321,7 +322,7 @@ cudaError_t timed(int kind, double flops, cudaStream_t stream, F&& launch) {
   bool on;
   {
     std::lock_guard<std::mutex> lock(P.mu);
-    on = P.on;
+    on = P.on && ((P.mask >> kind) & 1);
   }
   if (!on) return launch();
   cudaEvent_t a, b;
@@ -548,9 +549,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.tgt = c.tgt();
     tp.mtile = c.mtile();
     tp.mref = ref_rows ? c.mref() : nullptr;
-    // tile counter of the backward launch and the fixup list count start at zero
-    st = cuda_status(cudaMemsetAsync(c.counter(), 0, 2 * sizeof(int), c.stream));
-    if (st != FLCE_OK) return st;
+    tp.zero_words = c.counter();  // the backward launch's tile counter and the fixup list count start at zero
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
@@ -820,11 +819,12 @@ flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* 
   return run_fused(c, X, W, lv, loss, lse, dX, dW);
 }
 
-flce_status_t flce_profile_enable(int on) {
+flce_status_t flce_profile_enable(int mask) {
   Profiler& P = profiler();
   std::lock_guard<std::mutex> lock(P.mu);
   P.clear();
-  P.on = on != 0;
+  P.on = mask != 0;
+  P.mask = mask;
   // Create the events up front so that recording them costs no driver
   // allocation inside the region being timed.
   while (P.on && P.pool.size() < 4096) {

@@ -29,6 +29,17 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
+// Programmatic dependent launch: wait until the kernels this one depends on
+// have finished and their writes are visible, then let the next kernel in the
+// stream start its launch and prologue while this one runs.  Every kernel of
+// the library starts with it (before touching global memory), so completion
+// stays transitive along the stream.  Both are no-ops without the launch
+// attribute.
+__device__ __forceinline__ void griddep_begin() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ uint64_t global_timer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

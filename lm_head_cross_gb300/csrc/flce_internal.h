@@ -82,6 +82,7 @@ struct TcParams {
   const float* mref;    // forward-store: per row of X its target logit, log2 units (null: tile maxima only)
   const float* rowscale;  // bwd: per chunk row factor f_i of the stored G / (s f_i) (null: the buffer holds G)
   int b2_r0;            // bwd: first row of the dW B operand's tensor map
+  int* zero_words;      // if set: two ints the launch sets to 0 once its predecessors are done
   // top-k pass: per (split, row) the best topk_k (logit, id) pairs, [vsplit][n][kTopkMax]
   float* topk_val;
   int32_t* topk_idx;

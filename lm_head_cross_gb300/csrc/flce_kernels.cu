@@ -28,6 +28,7 @@
 // columns) with tcgen05.ld, one row per thread, so row reductions need no
 // shuffles.  Every wait is bounded (see mbar_wait).
 #include <algorithm>
+#include <utility>
 
 #include "flce_device.cuh"
 #include "flce_internal.h"
@@ -766,6 +767,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
+  griddep_begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
@@ -824,6 +826,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA arrival
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  griddep_begin();  // the prologue above overlaps the previous kernel's tail
+  if (p.zero_words && blockIdx.x == 0 && threadIdx.x == 0) {
+    p.zero_words[0] = 0;
+    p.zero_words[1] = 0;
+  }
 
   if (warp == 0) {
     if (lane == 0) run_producer<MODE>(maps, p, pr, smem, full, empty, ring, abort_flag);
@@ -860,6 +867,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     const float* __restrict__ part_l, const float* __restrict__ tgt, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
     int* __restrict__ status, RefRows rr) {
+  griddep_begin();
   const int ignore_index = lv.ignore_index;
   __shared__ double s_loss[kFinalizeThreads];
   __shared__ int s_valid[kFinalizeThreads];
@@ -993,6 +1001,7 @@ __device__ __forceinline__ void fixup_row(uint4* __restrict__ prow, const float*
 __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, LabelView lv,
                                                     const float* __restrict__ lse, const float* __restrict__ scale,
                                                     const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
+  griddep_begin();
   __shared__ int s_idx[kTopkMax];
   __shared__ float s_q[kTopkMax];
   __shared__ float s_mass;
@@ -1030,6 +1039,7 @@ __global__ void __launch_bounds__(256) fixup_list_kernel(const int* __restrict__
                                                          int vtiles, LabelView lv, const float* __restrict__ lse,
                                                          const float* __restrict__ mtile,
                                                          __nv_bfloat16* __restrict__ P) {
+  griddep_begin();
   const int count = *fix_count;
   for (int e = blockIdx.x; e < count; e += gridDim.x) {
     const int lrow = fix_list[e];
@@ -1045,6 +1055,7 @@ __global__ void __launch_bounds__(256) fixup_list_kernel(const int* __restrict__
 __global__ void __launch_bounds__(256) ref_gather_kernel(int n, int h, int v, LabelView lv,
                                                          const __nv_bfloat16* __restrict__ X,
                                                          const __nv_bfloat16* __restrict__ W, float* __restrict__ mref) {
+  griddep_begin();
   const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (row >= n) return;
@@ -1071,6 +1082,7 @@ __global__ void __launch_bounds__(256) ref_gather_kernel(int n, int h, int v, La
 // xs = f_i x_i row by row (8 bf16 per thread and step).
 __global__ void __launch_bounds__(256) row_scale_kernel(int64_t count8, int h8, const float* __restrict__ f,
                                                         const uint4* __restrict__ x, uint4* __restrict__ xs) {
+  griddep_begin();
   for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < count8;
        q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float c = f[q / h8];
@@ -1089,6 +1101,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int
                                                                        double* __restrict__ blk_loss,
                                                                        int* __restrict__ blk_valid,
                                                                        int* __restrict__ status) {
+  griddep_begin();
   __shared__ int s_valid[kFinalizeThreads];
   const int ignore_index = lv.ignore_index;
   const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
@@ -1134,6 +1147,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
                                                                          int reduction, const float* grad_loss,
                                                                          float* loss_out, int* n_valid_out,
                                                                          float* scale_out) {
+  griddep_begin();
   __shared__ double s_loss[kFinalizeThreads];
   __shared__ long long s_valid[kFinalizeThreads];
   double l = 0.0;
@@ -1176,6 +1190,7 @@ __global__ void __launch_bounds__(256) soft_gather_kernel(int n, int h, int v, i
                                                           const __nv_bfloat16* __restrict__ W,
                                                           const int32_t* __restrict__ idx,
                                                           const float* __restrict__ prob, float* __restrict__ tgt) {
+  griddep_begin();
   const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const int lane = threadIdx.x & 31;
   if (warp >= n) return;
@@ -1211,6 +1226,7 @@ __global__ void __launch_bounds__(128) topk_finalize_kernel(int n, int vsplit, i
                                                             const int32_t* __restrict__ cand_idx,
                                                             float* __restrict__ lse_out, float* __restrict__ out_val,
                                                             int32_t* __restrict__ out_idx) {
+  griddep_begin();
   const int row = blockIdx.x * blockDim.x + threadIdx.x;
   if (row >= n) return;
   float m = -INFINITY;
@@ -1255,6 +1271,7 @@ __global__ void __launch_bounds__(128) topk_finalize_kernel(int n, int vsplit, i
 }
 
 __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t count8) {
+  griddep_begin();
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
@@ -1270,6 +1287,7 @@ __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16
 
 // x *= g for bf16 data (8 elements per thread-iteration), g a device scalar.
 __global__ void scale_bf16_kernel(__nv_bfloat16* __restrict__ x, int64_t count8, const float* __restrict__ g) {
+  griddep_begin();
   const float s = *g;
   for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < count8;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
@@ -1285,6 +1303,7 @@ __global__ void scale_bf16_kernel(__nv_bfloat16* __restrict__ x, int64_t count8,
 // Waits on a barrier that nothing completes; the bounded wait gives up and the
 // timeout lands in the status word.
 __global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
+  griddep_begin();
   __shared__ __align__(8) uint64_t bar;
   __shared__ int abort_flag;
   if (threadIdx.x == 0) {
@@ -1302,6 +1321,24 @@ __global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
 
 int tc_smem_bytes() { return kSmemBytes; }
 
+// Every launch carries the programmatic-stream-serialization attribute (see
+// griddep_begin): a kernel may be scheduled while its predecessor drains.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                     Args&&... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
+
 template <int MODE>
 static cudaError_t launch_mode(const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
   static int configured_device = -1;
@@ -1313,8 +1350,7 @@ static cudaError_t launch_mode(const TcMaps& maps, const TcParams& p, int grid, 
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  tc_kernel<MODE><<<grid, kThreads, kSmemBytes, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_k(tc_kernel<MODE>, dim3(grid), dim3(kThreads), kSmemBytes, stream, maps, p);
 }
 
 cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
@@ -1332,43 +1368,39 @@ cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit,
                                      const float* part_l, const float* tgt, float* lse, float* loss_rows,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
   const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
-  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse,
-                                                               loss_rows, blk_loss, blk_valid, status, RefRows{});
-  return cudaGetLastError();
+  return launch_k(fwd_finalize_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
+                  r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse, loss_rows, blk_loss, blk_valid, status, RefRows{});
 }
 
 cudaError_t launch_fwd_finalize_ref(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
                                     const float* part_l, const float* tgt, float* lse, float* loss_rows,
                                     double* blk_loss, int* blk_valid, int* status, RefRows rr, cudaStream_t stream) {
   const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
-  fwd_finalize_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse,
-                                                               loss_rows, blk_loss, blk_valid, status, rr);
-  return cudaGetLastError();
+  return launch_k(fwd_finalize_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
+                  r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse, loss_rows, blk_loss, blk_valid, status, rr);
 }
 
 cudaError_t launch_ref_gather(int n, int h, int v, LabelView lv, const void* X, const void* W, float* mref,
                               cudaStream_t stream) {
   const int blocks = (n + 7) / 8;  // 8 rows (warps) per block
-  ref_gather_kernel<<<blocks, 256, 0, stream>>>(n, h, v, lv, static_cast<const __nv_bfloat16*>(X),
-                                                static_cast<const __nv_bfloat16*>(W), mref);
-  return cudaGetLastError();
+  return launch_k(ref_gather_kernel, dim3(blocks), dim3(256), 0, stream,
+                  n, h, v, lv, static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), mref);
 }
 
 cudaError_t launch_fixup_list(int max_rows, const int* fix_list, const int* fix_count, int r0, int v, int vp,
                               int vtiles, LabelView lv, const float* lse, const float* mtile, void* P, int grid,
                               cudaStream_t stream) {
   grid = std::max(1, std::min(grid, max_rows));
-  fixup_list_kernel<<<grid, 256, 0, stream>>>(fix_list, fix_count, r0, v, vp, vtiles, lv, lse, mtile,
-                                              static_cast<__nv_bfloat16*>(P));
-  return cudaGetLastError();
+  return launch_k(fixup_list_kernel, dim3(grid), dim3(256), 0, stream,
+                  fix_list, fix_count, r0, v, vp, vtiles, lv, lse, mtile, static_cast<__nv_bfloat16*>(P));
 }
 
 cudaError_t launch_row_scale(int rows, int h, const float* f, const void* x, void* xs, cudaStream_t stream) {
   const int64_t count8 = static_cast<int64_t>(rows) * (h / 8);
   const int64_t want = (count8 + 255) / 256;
   const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 4096)));
-  row_scale_kernel<<<blocks, 256, 0, stream>>>(count8, h / 8, f, static_cast<const uint4*>(x), static_cast<uint4*>(xs));
-  return cudaGetLastError();
+  return launch_k(row_scale_kernel, dim3(blocks), dim3(256), 0, stream,
+                  count8, h / 8, f, static_cast<const uint4*>(x), static_cast<uint4*>(xs));
 }
 
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
@@ -1381,15 +1413,15 @@ cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, cons
 
 cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
                          const float* scale, const float* mtile, void* P, cudaStream_t stream) {
-  fixup_kernel<<<rows, 256, 0, stream>>>(r0, v, vp, vtiles, lv, lse, scale, mtile, static_cast<__nv_bfloat16*>(P));
-  return cudaGetLastError();
+  return launch_k(fixup_kernel, dim3(rows), dim3(256), 0, stream,
+                  r0, v, vp, vtiles, lv, lse, scale, mtile, static_cast<__nv_bfloat16*>(P));
 }
 
 cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
                                    cudaStream_t stream) {
   const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
-  label_scan_kernel<<<blocks, kFinalizeThreads, 0, stream>>>(n, v, lv, blk_loss, blk_valid, status);
-  return cudaGetLastError();
+  return launch_k(label_scan_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
+                  n, v, lv, blk_loss, blk_valid, status);
 }
 
 cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss, int* blk_valid,
@@ -1400,9 +1432,8 @@ cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* lab
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,
                                 const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
                                 cudaStream_t stream) {
-  reduce_final_kernel<<<1, kFinalizeThreads, 0, stream>>>(nblk, blk_loss, blk_valid, reduction, grad_loss, loss_out,
-                                                          n_valid_out, scale_out);
-  return cudaGetLastError();
+  return launch_k(reduce_final_kernel, dim3(1), dim3(kFinalizeThreads), 0, stream,
+                  nblk, blk_loss, blk_valid, reduction, grad_loss, loss_out, n_valid_out, scale_out);
 }
 
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream) {
@@ -1413,24 +1444,22 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
   int64_t blocks = (count8 + 255) / 256;
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
-  convert_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(src, static_cast<__nv_bfloat16*>(dst), count8);
-  return cudaGetLastError();
+  return launch_k(convert_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream, src,
+                  static_cast<__nv_bfloat16*>(dst), count8);
 }
 
 cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,
                                const float* prob, float* tgt, cudaStream_t stream) {
   const int blocks = (n + 7) / 8;  // 8 warps per block, one row each
-  soft_gather_kernel<<<blocks, 256, 0, stream>>>(n, h, v, k, static_cast<const __nv_bfloat16*>(X),
-                                                 static_cast<const __nv_bfloat16*>(W), idx, prob, tgt);
-  return cudaGetLastError();
+  return launch_k(soft_gather_kernel, dim3(blocks), dim3(256), 0, stream,
+                  n, h, v, k, static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), idx, prob, tgt);
 }
 
 cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
                                  const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
                                  int32_t* out_idx, cudaStream_t stream) {
-  topk_finalize_kernel<<<(n + 127) / 128, 128, 0, stream>>>(n, vsplit, k, part_m, part_l, cand_val, cand_idx, lse,
-                                                             out_val, out_idx);
-  return cudaGetLastError();
+  return launch_k(topk_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, stream,
+                  n, vsplit, k, part_m, part_l, cand_val, cand_idx, lse, out_val, out_idx);
 }
 
 cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream) {
@@ -1441,13 +1470,13 @@ cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream
   int64_t blocks = (count8 + 255) / 256;
   if (blocks > 8LL * sms) blocks = 8LL * sms;
   if (blocks < 1) blocks = 1;
-  scale_bf16_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<__nv_bfloat16*>(x), count8, g);
-  return cudaGetLastError();
+  return launch_k(scale_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream,
+                  static_cast<__nv_bfloat16*>(x), count8, g);
 }
 
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {
-  timeout_selftest_kernel<<<1, 32, 0, stream>>>(status, limit_ns);
-  return cudaGetLastError();
+  return launch_k(timeout_selftest_kernel, dim3(1), dim3(32), 0, stream,
+                  status, limit_ns);
 }
 
 }  // namespace flce
