@@ -25,14 +25,15 @@ size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct Layout {
   size_t status, n_valid, scale;  // header words
   size_t counter;                 // tile counter of the dynamically scheduled launches
-  size_t fix_count;               // fused path: rows listed for a full fixup in the current chunk
+  size_t fix_count;               // fused path: rows listed for the full fix-up in the current chunk
+  size_t ticket;                  // fused path: blocks of the label pass done (its last block resets it)
   size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
   size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
   size_t g;                       // one chunk buffer: recompute path G [N, chunk]; fused path p~/G [rows, Vp]
   size_t dx_acc;                  // fp32 accumulator: recompute path dX [N, H]; fused path dW [V, H]
   size_t mtile;                   // fused path: per (chunk row, vocabulary tile) reference exponent
   size_t mref;                    // fused path: per row of X its target logit, log2 units
-  size_t rowscale, fix_list;      // fused path: per chunk row factor f_i; rows listed for a full fixup
+  size_t rowscale, fix_list;      // fused path: per chunk row factor f_i; rows listed for the full fix-up
   size_t xs;                      // fused path: f_i x_i for the chunk's rows, bf16 [rows, H]
   size_t total;
   int nblk, chunk;
@@ -67,11 +68,13 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   L.scale = off + 8;
   L.counter = off + 16;
   L.fix_count = off + 20;
+  L.ticket = off + 24;
   off += kAlign;
+  const size_t nblk_alloc = std::max<size_t>(L.nblk, (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock);
   L.blk_loss = off;
-  off = align_up(off + sizeof(double) * L.nblk);
+  off = align_up(off + sizeof(double) * nblk_alloc);
   L.blk_valid = off;
-  off = align_up(off + sizeof(int) * L.nblk);
+  off = align_up(off + sizeof(int) * nblk_alloc);
   L.part_m = off;
   off = align_up(off + sizeof(float) * kMaxSplit * n);
   L.part_l = off;
@@ -239,10 +242,11 @@ struct Ctx {
   void* g() const { return ws + L.g; }
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
   float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
+  int* ticket() const { return reinterpret_cast<int*>(ws + L.ticket); }
   int* fix_count() const { return reinterpret_cast<int*>(ws + L.fix_count); }
+  int* fix_list() const { return reinterpret_cast<int*>(ws + L.fix_list); }
   float* mref() const { return reinterpret_cast<float*>(ws + L.mref); }
   float* rowscale() const { return reinterpret_cast<float*>(ws + L.rowscale); }
-  int* fix_list() const { return reinterpret_cast<int*>(ws + L.fix_list); }
   void* xs() const { return ws + L.xs; }
   LabelView labels_of(const int32_t* labels) const {
     return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1, nullptr, nullptr, 0};
@@ -355,8 +359,8 @@ flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes
   st = device_info(&c->dev);
   if (st != FLCE_OK) return st;
   if (!encode_fn()) return FLCE_ERR_CUDA;
-  // the status word starts every call cleared
-  return cuda_status(cudaMemsetAsync(c->status(), 0, sizeof(int), c->stream));
+  // the header (status word, counters) starts every call cleared
+  return cuda_status(cudaMemsetAsync(c->ws + c->L.status, 0, kAlign, c->stream));
 }
 
 flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
@@ -486,28 +490,34 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   const int32_t* labels = lv.labels;
   const int vtiles = (v + kBN - 1) / kBN;
   const int h_tiles = (h + kBN - 1) / kBN;
-  flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_label_scan_view(n, v, lv, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
-  }));
-  if (st != FLCE_OK) return st;
-  // Hard labels: the forward-store references each row to its target logit,
-  // and only the rows where that fails get the full fixup pass.
+  // Hard labels: the forward-store references each row to its target logit
+  // (the row factor f_i then finishes G in the dX/dW epilogues); soft targets
+  // keep the tile-max reference and the full fix-up pass.
   const bool ref_rows = lv.soft_k == 0;
+  const int nblk = ref_rows ? (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock : c.L.nblk;
+  flce_status_t st;
   if (ref_rows) {
-    st = cuda_status(timed(3, 0.0, c.stream, [&] { return launch_ref_gather(n, h, v, lv, X, W, c.mref(), c.stream); }));
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_label_prep(n, h, v, p.reduction, lv, X, W, c.mref(), reinterpret_cast<int*>(c.part_l()),
+                               c.ticket(), c.n_valid(), c.scale(), c.status(), c.stream);
+    }));
     if (st != FLCE_OK) return st;
-  }
-  if (lv.soft_k > 0) {  // soft targets: sum_k q_k z_{i, id_k} per row, before any finalize reads it
+  } else {
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_label_scan_view(n, v, lv, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
+    // soft targets: sum_k q_k z_{i, id_k} per row, before any finalize reads it
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
       return launch_soft_gather(n, h, v, lv.soft_k, X, W, lv.soft_idx, lv.soft_prob, c.tgt(), c.stream);
     }));
     if (st != FLCE_OK) return st;
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, nullptr, c.n_valid(),
+                                 c.scale(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
   }
-  st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, nullptr, c.n_valid(),
-                               c.scale(), c.stream);
-  }));
-  if (st != FLCE_OK) return st;
 
   TcMaps fm;  // forward-store: X, W K-major; p~ store
   if (!make_map(&fm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
@@ -549,27 +559,22 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.tgt = c.tgt();
     tp.mtile = c.mtile();
     tp.mref = ref_rows ? c.mref() : nullptr;
-    tp.zero_words = c.counter();  // the backward launch's tile counter and the fixup list count start at zero
+    tp.zero_words = c.counter();  // the backward launch's tile counter and the fix-up list count start at zero
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
     if (ref_rows) {
-      const RefRows rr{c.mref(), c.rowscale(), c.fix_list(), c.fix_count(), c.g(), c.L.vp};
       st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_fwd_finalize_ref(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(), lse,
-                                       c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(), rr,
-                                       c.stream);
+        return launch_finalize_ref(r0, cr, n, h, v, static_cast<int>(c.L.vp), tp.vsplit, vtiles, lv, c.part_m(),
+                                   c.part_l(), c.tgt(), c.mref(), c.mtile(), lse, c.per_row() ? loss : nullptr,
+                                   c.blk_loss(), c.blk_valid(), c.rowscale(), X, c.xs(), c.g(), c.fix_list(),
+                                   c.fix_count(), c.status(), c.stream);
       }));
       if (st != FLCE_OK) return st;
       st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_fixup_list(cr, c.fix_list(), c.fix_count(), r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse,
-                                 c.mtile(), c.g(), c.dev.sms, c.stream);
-      }));
-      if (st != FLCE_OK) return st;
-      st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_row_scale(cr, h, c.rowscale(), static_cast<const uint16_t*>(X) + static_cast<int64_t>(r0) * h,
-                                c.xs(), c.stream);
+        return launch_fixup_list(c.fix_list(), c.fix_count(), r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse,
+                                 c.mtile(), c.g(), 2 * c.dev.sms, c.stream);
       }));
       if (st != FLCE_OK) return st;
     } else {
@@ -630,7 +635,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     if (st != FLCE_OK) return st;
   }
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr,
+    return launch_reduce_final(nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr,
                                c.per_row() ? nullptr : loss, c.n_valid(), c.scale(), c.stream);
   }));
   return st;

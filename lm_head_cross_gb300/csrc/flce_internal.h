@@ -119,31 +119,25 @@ struct LabelView {
 cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
                                      const float* part_l, const float* tgt, float* lse, float* loss_rows,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
-// The rows' side of the target-logit-referenced chunk buffer, once lse is known
-// (rows [r0, r0 + rows)): per row the factor f_i = 2^(ref_i - lse_i log2 e)
-// (0 for rows without a gradient, 1 for rows listed for a full fixup), the
-// target entry G_iy / (s f_i), and the list of rows that a tile stored with
-// its own max.
-struct RefRows {
-  const float* mref;
-  float* rowscale;
-  int* fix_list;
-  int* fix_count;
-  void* P;
-  int64_t vp;
-};
-cudaError_t launch_fwd_finalize_ref(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
-                                    const float* part_l, const float* tgt, float* lse, float* loss_rows,
-                                    double* blk_loss, int* blk_valid, int* status, RefRows rr, cudaStream_t stream);
-// mref_i = x_i . w_{y_i} log2 e for every row with a label in range (0 otherwise).
-cudaError_t launch_ref_gather(int n, int h, int v, LabelView lv, const void* X, const void* W, float* mref,
+// Fused path with hard labels.  label_prep: label check, the rows' references
+// (target logits, log2 units) and, through the last block, n_valid and s.
+cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, const void* X, const void* W,
+                              float* mref, int* blk_cnt, int* ticket, int* n_valid, float* scale, int* status,
                               cudaStream_t stream);
-// Listed rows of a chunk buffer: G / s = p~ 2^(ref - lse log2 e) - [j = y].
-cudaError_t launch_fixup_list(int max_rows, const int* fix_list, const int* fix_count, int r0, int v, int vp,
-                              int vtiles, LabelView lv, const float* lse, const float* mtile, void* P, int grid,
+// finalize_ref, rows [r0, r0 + rows) of one chunk: lse, losses and the loss
+// partials (one per kRefRowsPerBlock rows, index r0 / kRefRowsPerBlock + b),
+// the row factors f_i, the chunk buffer's target entries, xs = f x, and the
+// list of rows a tile stored relative to its own max (fix_list / fix_count).
+constexpr int kRefRowsPerBlock = 8;
+cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+                                const float* part_m, const float* part_l, const float* tgt, const float* mref,
+                                const float* mtile, float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
+                                float* rowscale, const void* X, void* xs, void* P, int* fix_list, int* fix_count,
+                                int* status, cudaStream_t stream);
+// The listed rows' full fix-up (G / s in place), `grid` blocks.
+cudaError_t launch_fixup_list(const int* fix_list, const int* fix_count, int r0, int v, int vp, int vtiles,
+                              LabelView lv, const float* lse, const float* mtile, void* P, int grid,
                               cudaStream_t stream);
-// xs[i, :] = f_i x[i, :] (bf16) for the rows of one chunk.
-cudaError_t launch_row_scale(int rows, int h, const float* f, const void* x, void* xs, cudaStream_t stream);
 cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
                          const float* scale, const float* mtile, void* P, cudaStream_t stream);
 cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,

@@ -858,6 +858,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 
 // ----------------------------------------------------------------------------- small kernels
 
+// Merge a row's per-range (reference, sum) pairs: returns lse in log2 units
+// and the largest reference in *m_out.  All loads are issued before the first
+// use, so a row costs one memory latency rather than one per range.
+__device__ __forceinline__ float merge_ranges(const float* __restrict__ part_m, const float* __restrict__ part_l,
+                                              int vsplit, int n, int row, float* m_out) {
+  float pm[kMaxSplit], pl[kMaxSplit];
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) {
+    pm[s] = s < vsplit ? part_m[static_cast<int64_t>(s) * n + row] : -INFINITY;
+    pl[s] = s < vsplit ? part_l[static_cast<int64_t>(s) * n + row] : 0.f;
+  }
+  float m = -INFINITY;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s) m = fmaxf(m, pm[s]);
+  float l = 0.f;
+#pragma unroll
+  for (int s = 0; s < kMaxSplit; ++s)
+    if (s < vsplit) l += pl[s] * exp2f(pm[s] - m);
+  *m_out = m;
+  return m + log2f(l);
+}
+
 // Merge the per-split (max, sum) pairs of each row into lse, check its label,
 // and reduce the per-row losses of the block in a fixed order.
 // Rows [r0, r0 + rows) of an n-row problem; r0 is a multiple of the block size,
@@ -866,7 +888,7 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* __restrict__ part_m,
     const float* __restrict__ part_l, const float* __restrict__ tgt, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
-    int* __restrict__ status, RefRows rr) {
+    int* __restrict__ status) {
   griddep_begin();
   const int ignore_index = lv.ignore_index;
   __shared__ double s_loss[kFinalizeThreads];
@@ -875,13 +897,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
   double li = 0.0;
   int valid = 0;
   if (row < r0 + rows) {
-    float m = -INFINITY;
-    for (int s = 0; s < vsplit; ++s) m = fmaxf(m, part_m[static_cast<int64_t>(s) * n + row]);
-    float l = 0.f;
-    for (int s = 0; s < vsplit; ++s)
-      l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
-    const float lse2 = m + log2f(l);
-    const float lse = lse2 * kLn2;
+    float m;
+    const float lse = merge_ranges(part_m, part_l, vsplit, n, row, &m) * kLn2;
     lse_out[row] = lse;
     if (lv.soft_k > 0) {
       // KL(q || p) over the row's target ids: sum_k q_k log q_k + Q lse - sum_k q_k z_k
@@ -909,25 +926,6 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
           atomicCAS(status, 0, kErrLabel);
         }
       }
-      if (rr.mref) {
-        // m is the largest reference the row's tiles used: above the row's
-        // target logit only when some tile was stored relative to its own max
-        const int lrow = row - r0;
-        float f = 0.f;
-        if (valid) {
-          const float ref = rr.mref[row];
-          if (m > ref) {
-            f = 1.f;
-            rr.fix_list[atomicAdd(rr.fix_count, 1)] = lrow;
-          } else {
-            // G_iy / (s f_i) = (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
-            f = exp2f(ref - lse2);
-            const float gy = exp2f(fmaf(tgt[row], kLog2e, -ref)) - exp2f(lse2 - ref);
-            static_cast<__nv_bfloat16*>(rr.P)[static_cast<int64_t>(lrow) * rr.vp + y] = __float2bfloat16_rn(gy);
-          }
-        }
-        rr.rowscale[lrow] = f;
-      }
     }
     if (loss_rows) loss_rows[row] = static_cast<float>(li);
   }
@@ -951,10 +949,10 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
 // target ids (q = 1 at y for a hard label), as bf16, in place.
 __device__ __forceinline__ void fixup_row(uint4* __restrict__ prow, const float* __restrict__ mt, int v, float lse2,
                                           float coef, float mass, int y, int nsoft, const int* s_idx,
-                                          const float* s_q) {
+                                          const float* s_q, int q_begin = 0, int q_end = -1) {
   constexpr int kUnroll = 4;  // 16-byte loads in flight per thread
-  const int nvec = (v + 7) / 8;
-  for (int base = threadIdx.x; base < nvec; base += blockDim.x * kUnroll) {
+  const int nvec = q_end < 0 ? (v + 7) / 8 : q_end;  // 8-column groups [q_begin, nvec)
+  for (int base = q_begin + threadIdx.x; base < nvec; base += blockDim.x * kUnroll) {
     uint4 u[kUnroll];
 #pragma unroll
     for (int k = 0; k < kUnroll; ++k) {
@@ -1031,68 +1029,187 @@ __global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int v
             v, lse[row] * kLog2e, coef, mass, y, nsoft, s_idx, s_q);
 }
 
-// Rows of a chunk buffer listed by the finalize (stored at least partly
-// relative to their tiles' maxima): G / s = p~ 2^(ref - lse log2 e) - [j = y].
-// Blocks take list entries round-robin; an empty list costs one launch.
+// Hard labels, fused path, before the first row chunk.  One warp per row: the
+// label check and the row's reference, its target logit in log2 units
+// (ref_i = x_i . w_{y_i} log2 e, fp32 accumulation of the bf16 products); one
+// valid count per block of 8 rows.  The last block to finish (ticket) adds the
+// counts into n_valid and the gradient scale s, and resets the ticket.
+__global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, int reduction, LabelView lv,
+                                                         const __nv_bfloat16* __restrict__ X,
+                                                         const __nv_bfloat16* __restrict__ W, float* __restrict__ mref,
+                                                         int* __restrict__ blk_cnt, int* __restrict__ ticket,
+                                                         int* __restrict__ n_valid_out, float* __restrict__ scale_out,
+                                                         int* __restrict__ status) {
+  griddep_begin();
+  __shared__ int s_valid[8];
+  __shared__ long long s_sum[256];
+  __shared__ int s_last;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int row = blockIdx.x * 8 + warp;
+  int valid = 0;
+  if (row < n) {
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    float dot = 0.f;
+    if (y != lv.ignore_index) {
+      if (y >= 0 && y < v) {
+        valid = 1;
+        const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * h);
+        const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(y) * h);
+        for (int c = lane; c < h / 8; c += 32) {
+          const uint4 a = xr[c], b = wr[c];
+          const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
+            dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
+          }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+      } else if (lane == 0) {
+        atomicCAS(status, 0, kErrLabel);
+      }
+    }
+    if (lane == 0) mref[row] = dot * kLog2e;
+  }
+  if (lane == 0) s_valid[warp] = valid;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int c = 0;
+    for (int w = 0; w < 8; ++w) c += s_valid[w];
+    blk_cnt[blockIdx.x] = c;
+    __threadfence();
+    s_last = (atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  long long c = 0;
+#pragma unroll 8
+  for (int i = threadIdx.x; i < static_cast<int>(gridDim.x); i += blockDim.x) c += __ldcg(blk_cnt + i);
+  s_sum[threadIdx.x] = c;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_sum[threadIdx.x] += s_sum[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const long long nv = s_sum[0];
+    *n_valid_out = static_cast<int>(nv);
+    // as reduce_final_kernel with g = 1: mean 1 / n_valid (0 without valid rows), sum and none 1
+    *scale_out = reduction == 0 ? (nv > 0 ? static_cast<float>(1.0 / static_cast<double>(nv)) : 0.f) : 1.f;
+    *ticket = 0;
+  }
+}
+
+// Hard labels, fused path, one row chunk, kRefRowsPerBlock rows per block.
+//  - warp 0, one row per lane: lse from the per-range (reference, sum) pairs,
+//    the row's loss and the block's loss partial (fixed-order shuffle tree);
+//    f_i = 2^(ref_i - lse_i log2 e) and the target entry (p_iy - 1) / f_i of
+//    the chunk buffer, so that G_i = s f_i p~_i; f_i = 0 for rows without a
+//    gradient; rows where some tile used its own max (part max above ref_i)
+//    are marked for the full fix-up, with f_i = 1;
+//  - all threads: xs_i = f_i x_i (bf16), the dW contraction's B operand;
+//  - then, in place, the marked rows: p~ 2^(r_tile - lse log2 e) - [j = y].
+__global__ void __launch_bounds__(256) finalize_ref_kernel(
+    int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+    const float* __restrict__ part_m, const float* __restrict__ part_l, const float* __restrict__ tgt,
+    const float* __restrict__ mref, const float* __restrict__ mtile, float* __restrict__ lse_out,
+    float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
+    float* __restrict__ rowscale, const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ xs,
+    __nv_bfloat16* __restrict__ P, int* __restrict__ fix_list, int* __restrict__ fix_count,
+    int* __restrict__ status) {
+  griddep_begin();
+  __shared__ float s_f[kRefRowsPerBlock];
+  const int lrow0 = blockIdx.x * kRefRowsPerBlock;
+  const int nr = min(kRefRowsPerBlock, rows - lrow0);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    const int lrow = lrow0 + lane;
+    const int row = r0 + lrow;
+    double li = 0.0;
+    int valid = 0;
+    float f = 0.f;
+    if (lane < nr) {
+      float m;
+      const float lse2 = merge_ranges(part_m, part_l, vsplit, n, row, &m);
+      const float lse = lse2 * kLn2;
+      lse_out[row] = lse;
+      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+      if (y != lv.ignore_index) {
+        if (y >= 0 && y < v) {
+          valid = 1;
+          li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
+          const float ref = mref[row];
+          if (m > ref) {
+            f = 1.f;
+            fix_list[atomicAdd(fix_count, 1)] = lrow;
+          } else {
+            // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
+            f = exp2f(ref - lse2);
+            const float gy = exp2f(fmaf(tgt[row], kLog2e, -ref)) - exp2f(lse2 - ref);
+            P[static_cast<int64_t>(lrow) * vp + y] = __float2bfloat16_rn(gy);
+          }
+        } else {
+          atomicCAS(status, 0, kErrLabel);
+        }
+      }
+      rowscale[lrow] = f;
+      if (loss_rows) loss_rows[row] = static_cast<float>(li);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      li += __shfl_down_sync(0xffffffffu, li, o);
+      valid += __shfl_down_sync(0xffffffffu, valid, o);
+    }
+    if (lane == 0) {
+      blk_loss[r0 / kRefRowsPerBlock + blockIdx.x] = li;
+      blk_valid[r0 / kRefRowsPerBlock + blockIdx.x] = valid;
+    }
+    if (lane < kRefRowsPerBlock) s_f[lane] = f;
+  }
+  __syncthreads();
+  const int h8 = h / 8;
+  const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(r0 + lrow0) * h);
+  uint4* xo = reinterpret_cast<uint4*>(xs + static_cast<int64_t>(lrow0) * h);
+  const int total = nr * h8;
+#pragma unroll 4
+  for (int q = threadIdx.x; q < total; q += blockDim.x) {
+    const float c = s_f[q / h8];
+    const uint4 u = xr[q];
+    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      o[e] = pack_bf16x2(__uint_as_float(in[e] << 16) * c, __uint_as_float(in[e] & 0xFFFF0000u) * c);
+    xo[q] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+// The rows finalize_ref listed (a tile of theirs was stored relative to its
+// own max), in place: G / s = p~ 2^(r_tile - lse log2 e) - [j = y].  Work items
+// are (listed row, segment of kFixSegment columns), taken round-robin by the
+// blocks; an empty list costs one launch.
+constexpr int kFixSegment = 8192;
 __global__ void __launch_bounds__(256) fixup_list_kernel(const int* __restrict__ fix_list,
                                                          const int* __restrict__ fix_count, int r0, int v, int vp,
                                                          int vtiles, LabelView lv, const float* __restrict__ lse,
                                                          const float* __restrict__ mtile,
                                                          __nv_bfloat16* __restrict__ P) {
   griddep_begin();
-  const int count = *fix_count;
-  for (int e = blockIdx.x; e < count; e += gridDim.x) {
-    const int lrow = fix_list[e];
+  const int nseg = (v + kFixSegment - 1) / kFixSegment;
+  const int items = *fix_count * nseg;
+  for (int e = blockIdx.x; e < items; e += gridDim.x) {
+    const int lrow = fix_list[e / nseg];
+    const int seg = e % nseg;
     const int row = r0 + lrow;
     const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    const int q0 = seg * (kFixSegment / 8);
+    const int q1 = min((v + 7) / 8, q0 + kFixSegment / 8);
     fixup_row(reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp),
-              mtile + static_cast<int64_t>(lrow) * vtiles, v, lse[row] * kLog2e, 1.f, 1.f, y, 0, nullptr, nullptr);
-  }
-}
-
-// Target logits in log2 units (the forward-store's row references), one warp
-// per row, fp32 accumulation of the bf16 products.
-__global__ void __launch_bounds__(256) ref_gather_kernel(int n, int h, int v, LabelView lv,
-                                                         const __nv_bfloat16* __restrict__ X,
-                                                         const __nv_bfloat16* __restrict__ W, float* __restrict__ mref) {
-  griddep_begin();
-  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (row >= n) return;
-  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-  float dot = 0.f;
-  if (y >= 0 && y < v) {
-    const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * h);
-    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(y) * h);
-    for (int c = lane; c < h / 8; c += 32) {
-      const uint4 a = xr[c], b = wr[c];
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
-        dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-  }
-  if (lane == 0) mref[row] = dot * kLog2e;
-}
-
-// xs = f_i x_i row by row (8 bf16 per thread and step).
-__global__ void __launch_bounds__(256) row_scale_kernel(int64_t count8, int h8, const float* __restrict__ f,
-                                                        const uint4* __restrict__ x, uint4* __restrict__ xs) {
-  griddep_begin();
-  for (int64_t q = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; q < count8;
-       q += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const float c = f[q / h8];
-    const uint4 u = x[q];
-    const uint32_t in[4] = {u.x, u.y, u.z, u.w};
-    uint32_t o[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e)
-      o[e] = pack_bf16x2(__uint_as_float(in[e] << 16) * c, __uint_as_float(in[e] & 0xFFFF0000u) * c);
-    xs[q] = make_uint4(o[0], o[1], o[2], o[3]);
+              mtile + static_cast<int64_t>(lrow) * vtiles, v, lse[row] * kLog2e, 1.f, 1.f, y, 0, nullptr, nullptr,
+              q0, q1);
   }
 }
 
@@ -1152,7 +1269,8 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
   __shared__ long long s_valid[kFinalizeThreads];
   double l = 0.0;
   long long c = 0;
-  for (int i = threadIdx.x; i < nblk; i += kFinalizeThreads) {
+#pragma unroll 8
+  for (int i = threadIdx.x; i < nblk; i += kFinalizeThreads) {  // loads hoisted, sums kept in index order
     l += blk_loss[i];
     c += blk_valid[i];
   }
@@ -1369,38 +1487,35 @@ cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream) {
   const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
   return launch_k(fwd_finalize_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
-                  r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse, loss_rows, blk_loss, blk_valid, status, RefRows{});
+                  r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse, loss_rows, blk_loss, blk_valid, status);
 }
 
-cudaError_t launch_fwd_finalize_ref(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
-                                    const float* part_l, const float* tgt, float* lse, float* loss_rows,
-                                    double* blk_loss, int* blk_valid, int* status, RefRows rr, cudaStream_t stream) {
-  const int blocks = (rows + kFinalizeThreads - 1) / kFinalizeThreads;
-  return launch_k(fwd_finalize_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
-                  r0, rows, n, v, vsplit, lv, part_m, part_l, tgt, lse, loss_rows, blk_loss, blk_valid, status, rr);
-}
-
-cudaError_t launch_ref_gather(int n, int h, int v, LabelView lv, const void* X, const void* W, float* mref,
+cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, const void* X, const void* W,
+                              float* mref, int* blk_cnt, int* ticket, int* n_valid, float* scale, int* status,
                               cudaStream_t stream) {
   const int blocks = (n + 7) / 8;  // 8 rows (warps) per block
-  return launch_k(ref_gather_kernel, dim3(blocks), dim3(256), 0, stream,
-                  n, h, v, lv, static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), mref);
+  return launch_k(label_prep_kernel, dim3(blocks), dim3(256), 0, stream, n, h, v, reduction, lv,
+                  static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), mref, blk_cnt, ticket,
+                  n_valid, scale, status);
 }
 
-cudaError_t launch_fixup_list(int max_rows, const int* fix_list, const int* fix_count, int r0, int v, int vp,
-                              int vtiles, LabelView lv, const float* lse, const float* mtile, void* P, int grid,
+cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+                                const float* part_m, const float* part_l, const float* tgt, const float* mref,
+                                const float* mtile, float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
+                                float* rowscale, const void* X, void* xs, void* P, int* fix_list, int* fix_count,
+                                int* status, cudaStream_t stream) {
+  const int blocks = (rows + kRefRowsPerBlock - 1) / kRefRowsPerBlock;
+  return launch_k(finalize_ref_kernel, dim3(blocks), dim3(256), 0, stream, r0, rows, n, h, v, vp, vsplit, vtiles, lv,
+                  part_m, part_l, tgt, mref, mtile, lse, loss_rows, blk_loss, blk_valid, rowscale,
+                  static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(xs),
+                  static_cast<__nv_bfloat16*>(P), fix_list, fix_count, status);
+}
+
+cudaError_t launch_fixup_list(const int* fix_list, const int* fix_count, int r0, int v, int vp, int vtiles,
+                              LabelView lv, const float* lse, const float* mtile, void* P, int grid,
                               cudaStream_t stream) {
-  grid = std::max(1, std::min(grid, max_rows));
-  return launch_k(fixup_list_kernel, dim3(grid), dim3(256), 0, stream,
-                  fix_list, fix_count, r0, v, vp, vtiles, lv, lse, mtile, static_cast<__nv_bfloat16*>(P));
-}
-
-cudaError_t launch_row_scale(int rows, int h, const float* f, const void* x, void* xs, cudaStream_t stream) {
-  const int64_t count8 = static_cast<int64_t>(rows) * (h / 8);
-  const int64_t want = (count8 + 255) / 256;
-  const int blocks = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, 4096)));
-  return launch_k(row_scale_kernel, dim3(blocks), dim3(256), 0, stream,
-                  count8, h / 8, f, static_cast<const uint4*>(x), static_cast<uint4*>(xs));
+  return launch_k(fixup_list_kernel, dim3(std::max(1, grid)), dim3(256), 0, stream, fix_list, fix_count, r0, v, vp,
+                  vtiles, lv, lse, mtile, static_cast<__nv_bfloat16*>(P));
 }
 
 cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
