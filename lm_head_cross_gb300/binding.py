@@ -21,7 +21,7 @@ REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
             "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
-            "flce_soft_fwd_bwd", "flce_status_string")
+            "flce_soft_fwd_bwd", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
@@ -72,6 +72,10 @@ def lib():
     L.flce_topk.restype = ctypes.c_int
     L.flce_soft_fwd_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_soft_fwd_bwd.restype = ctypes.c_int
+    L.flce_host_buffer_bytes.argtypes = [P]
+    L.flce_host_buffer_bytes.restype = sz
+    L.flce_fwd_bwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_fwd_bwd_host.restype = ctypes.c_int
     L.flce_scale_grads.argtypes = [P, vp, vp, vp, vp]
     L.flce_scale_grads.restype = ctypes.c_int
     L.flce_read_device_status.argtypes = [vp, vp]
@@ -235,6 +239,33 @@ def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
     if check:
         _call("device", read_device_status(ws, stream))
     return loss, lse, dX, dW, ws
+
+
+def host_buffer_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
+    """Device buffer of fwd_bwd_host: the workspace, then device copies of inputs and results."""
+    p = _problem(n, h, v, ignore_index, reduction)
+    return int(lib().flce_host_buffer_bytes(ctypes.byref(p)))
+
+
+def fwd_bwd_host(x, w, labels, out, dev, ignore_index=-100, reduction="mean", stream=None, shift=0, seq_len=0):
+    """flce_fwd_bwd_host: x, w, labels and out = (loss, lse, dX, dW) are CPU tensors (pinned for
+    asynchronous copies), dev a CUDA uint8 tensor of host_buffer_bytes.  Enqueued on `stream`;
+    synchronise before reading `out`.  Device status: read_device_status(dev)."""
+    torch = _torch()
+    if x.is_cuda or w.is_cuda or labels.is_cuda or any(t.is_cuda for t in out):
+        raise ValueError("fwd_bwd_host takes host tensors")
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or labels.dtype != torch.int32:
+        raise TypeError("x and w must be bfloat16, labels int32")
+    if not (x.is_contiguous() and w.is_contiguous() and labels.is_contiguous()):
+        raise ValueError("inputs must be contiguous")
+    n, h = x.shape
+    v = w.shape[0]
+    p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
+    loss, lse, dX, dW = out
+    _call("flce_fwd_bwd_host", lib().flce_fwd_bwd_host(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
+                                                       loss.data_ptr(), lse.data_ptr(), dX.data_ptr(), dW.data_ptr(),
+                                                       dev.data_ptr(), dev.numel(), _stream_ptr(stream)))
+    return out
 
 
 def topk_workspace_bytes(n, h, v, k) -> int:

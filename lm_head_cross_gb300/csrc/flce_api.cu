@@ -686,6 +686,34 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   }));
 }
 
+// Device buffer of flce_fwd_bwd_host: the workspace, then the device copies.
+struct HostLayout {
+  size_t ws, x, w, labels, loss, lse, dx, dw, total;
+};
+
+HostLayout host_layout(const flce_problem_t& p) {
+  HostLayout L{};
+  const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
+  size_t off = align_up(make_layout(p, true).total);
+  L.ws = 0;
+  L.x = off;
+  off = align_up(off + 2 * n * h);
+  L.w = off;
+  off = align_up(off + 2 * v * h);
+  L.labels = off;
+  off = align_up(off + 4 * n);
+  L.loss = off;
+  off = align_up(off + 4 * (p.reduction == FLCE_REDUCTION_NONE ? n : 1));
+  L.lse = off;
+  off = align_up(off + 4 * n);
+  L.dx = off;
+  off = align_up(off + 2 * n * h);
+  L.dw = off;
+  off = align_up(off + 2 * v * h);
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 int chunk_width(int64_t n) { return n <= 16384 ? 8192 : 4096; }
@@ -755,6 +783,40 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
   if (st != FLCE_OK) return st;
   return run_backward(c, X, W, labels, lse, nullptr, dX, dW);
+}
+
+size_t flce_host_buffer_bytes(const flce_problem_t* p) {
+  if (check_problem(p) != FLCE_OK) return 0;
+  return host_layout(*p).total;
+}
+
+flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
+                                float* loss, float* lse, void* dX, void* dW, void* dev, size_t dev_bytes,
+                                flce_stream_t stream) {
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (!X || !W || !labels || !loss || !lse || !dX || !dW || !dev) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(dev, kAlign)) return FLCE_ERR_MISALIGNED;
+  const HostLayout L = host_layout(*p);
+  if (dev_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  uint8_t* d = static_cast<uint8_t*>(dev);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t n = static_cast<size_t>(p->n), h = static_cast<size_t>(p->h), v = static_cast<size_t>(p->v);
+  const size_t loss_bytes = 4 * (p->reduction == FLCE_REDUCTION_NONE ? n : 1);
+  if (cudaMemcpyAsync(d + L.x, X, 2 * n * h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.w, W, 2 * v * h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.labels, labels, 4 * n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  st = flce_fwd_bwd(p, d + L.x, d + L.w, reinterpret_cast<const int32_t*>(d + L.labels),
+                    reinterpret_cast<float*>(d + L.loss), reinterpret_cast<float*>(d + L.lse), d + L.dx, d + L.dw,
+                    d + L.ws, L.x - L.ws, stream);
+  if (st != FLCE_OK) return st;
+  if (cudaMemcpyAsync(loss, d + L.loss, loss_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(lse, d + L.lse, 4 * n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(dX, d + L.dx, 2 * n * h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaMemcpyAsync(dW, d + L.dw, 2 * v * h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
 }
 
 flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, void* dX, void* dW,

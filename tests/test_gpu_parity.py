@@ -281,3 +281,25 @@ def test_wide_logit_range_rows(red):
     # the x64 rows do have logits spread far past the reference span
     z = xf[group == 2].astype(np.float64) @ synth.bf16_bits_to_f32(p.W).astype(np.float64).T
     assert (z.max(axis=1) - z.min(axis=1)).max() > 64 / math.log2(math.e)
+
+
+def test_fwd_bwd_host_matches_device_call():
+    """The host-memory entry point runs the same pass: results equal the device
+    call's bit for bit, and its device status is read from the buffer's start."""
+    p = synth.make_problem(700, 136, 3001, seed=47, labels="zipf", ignore_frac=0.1, w_std=0.05)
+    a = run(p)
+    X, W, y = to_device(p)
+    xh, wh, yh = X.cpu().pin_memory(), W.cpu().pin_memory(), y.cpu().pin_memory()
+    out = (torch.empty(1, dtype=torch.float32).pin_memory(), torch.empty(p.n, dtype=torch.float32).pin_memory(),
+           torch.empty(xh.shape, dtype=torch.bfloat16).pin_memory(),
+           torch.empty(wh.shape, dtype=torch.bfloat16).pin_memory())
+    dev = torch.empty(flce.host_buffer_bytes(p.n, p.h, p.v), dtype=torch.uint8, device="cuda")
+    flce.fwd_bwd_host(xh, wh, yh, out, dev, p.ignore_index, p.reduction)
+    assert flce.read_device_status(dev) == 0
+    torch.cuda.synchronize()
+    assert float(out[0].item()) == a["loss"]
+    assert np.array_equal(out[1].numpy(), a["lse"])
+    assert np.array_equal(out[2].float().numpy(), a["dX"])
+    assert np.array_equal(out[3].float().numpy(), a["dW"])
+    with pytest.raises(flce.FlceError):
+        flce.fwd_bwd_host(xh, wh, yh, out, dev[:1024], p.ignore_index, p.reduction)
