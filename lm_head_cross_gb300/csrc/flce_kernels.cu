@@ -859,23 +859,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 // ----------------------------------------------------------------------------- small kernels
 
 // Merge a row's per-range (reference, sum) pairs: returns lse in log2 units
-// and the largest reference in *m_out.  All loads are issued before the first
-// use, so a row costs one memory latency rather than one per range.
+// and the largest reference in *m_out.  Loads are issued 16 ranges at a time
+// before their first use, so a row costs one or two memory latencies rather
+// than one per range.
 __device__ __forceinline__ float merge_ranges(const float* __restrict__ part_m, const float* __restrict__ part_l,
                                               int vsplit, int n, int row, float* m_out) {
-  float pm[kMaxSplit], pl[kMaxSplit];
+  constexpr int kBatch = 16;
+  float m = -INFINITY, l = 0.f;
+  for (int b = 0; b < vsplit; b += kBatch) {
+    float pm[kBatch], pl[kBatch];
 #pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) {
-    pm[s] = s < vsplit ? part_m[static_cast<int64_t>(s) * n + row] : -INFINITY;
-    pl[s] = s < vsplit ? part_l[static_cast<int64_t>(s) * n + row] : 0.f;
+    for (int k = 0; k < kBatch; ++k) {
+      const int s = b + k;
+      pm[k] = s < vsplit ? part_m[static_cast<int64_t>(s) * n + row] : -INFINITY;
+      pl[k] = s < vsplit ? part_l[static_cast<int64_t>(s) * n + row] : 0.f;
+    }
+    float bm = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k) bm = fmaxf(bm, pm[k]);
+    const float nm = fmaxf(m, bm);
+    float bl = 0.f;
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (b + k < vsplit) bl += pl[k] * exp2f(pm[k] - nm);
+    l = l * exp2f(m - nm) + bl;
+    m = nm;
   }
-  float m = -INFINITY;
-#pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s) m = fmaxf(m, pm[s]);
-  float l = 0.f;
-#pragma unroll
-  for (int s = 0; s < kMaxSplit; ++s)
-    if (s < vsplit) l += pl[s] * exp2f(pm[s] - m);
   *m_out = m;
   return m + log2f(l);
 }
@@ -1103,16 +1112,20 @@ __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, in
   }
 }
 
-// Hard labels, fused path, one row chunk, kRefRowsPerBlock rows per block.
-//  - warp 0, one row per lane: lse from the per-range (reference, sum) pairs,
-//    the row's loss and the block's loss partial (fixed-order shuffle tree);
-//    f_i = 2^(ref_i - lse_i log2 e) and the target entry (p_iy - 1) / f_i of
-//    the chunk buffer, so that G_i = s f_i p~_i; f_i = 0 for rows without a
-//    gradient; rows where some tile used its own max (part max above ref_i)
-//    are marked for the full fix-up, with f_i = 1;
-//  - all threads: xs_i = f_i x_i (bf16), the dW contraction's B operand;
-//  - then, in place, the marked rows: p~ 2^(r_tile - lse log2 e) - [j = y].
-__global__ void __launch_bounds__(256) finalize_ref_kernel(
+static_assert(kMaxSplit <= 32, "finalize_ref_kernel merges one vocabulary range per lane");
+
+// Hard labels, fused path, one row chunk, kRefRowsPerBlock rows per block (one
+// warp per row, one lane per vocabulary range).
+//  - every thread first starts loading its share of the block's X rows;
+//  - warp w, row w: lse from the per-range (reference, sum) pairs (butterfly
+//    max and sum over the lanes), the row's loss; f_i = 2^(ref_i - lse_i log2 e)
+//    and the target entry (p_iy - 1) / f_i of the chunk buffer, so that
+//    G_i = s f_i p~_i; f_i = 0 for rows without a gradient; rows where some
+//    tile used its own max (largest reference above ref_i) get f_i = 1 and go
+//    on the list for the full fix-up;
+//  - the block's loss partial, summed over its rows in order;
+//  - all threads: xs_i = f_i x_i (bf16), the dW contraction's B operand.
+__global__ void __launch_bounds__(kRefRowsPerBlock * 32) finalize_ref_kernel(
     int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
     const float* __restrict__ part_m, const float* __restrict__ part_l, const float* __restrict__ tgt,
     const float* __restrict__ mref, const float* __restrict__ mtile, float* __restrict__ lse_out,
@@ -1122,69 +1135,100 @@ __global__ void __launch_bounds__(256) finalize_ref_kernel(
     int* __restrict__ status) {
   griddep_begin();
   __shared__ float s_f[kRefRowsPerBlock];
+  __shared__ double s_li[kRefRowsPerBlock];
+  __shared__ int s_valid[kRefRowsPerBlock];
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
   const int lrow0 = blockIdx.x * kRefRowsPerBlock;
   const int nr = min(kRefRowsPerBlock, rows - lrow0);
-  if (threadIdx.x < 32) {
-    const int lane = threadIdx.x;
-    const int lrow = lrow0 + lane;
-    const int row = r0 + lrow;
-    double li = 0.0;
-    int valid = 0;
-    float f = 0.f;
-    if (lane < nr) {
-      float m;
-      const float lse2 = merge_ranges(part_m, part_l, vsplit, n, row, &m);
-      const float lse = lse2 * kLn2;
-      lse_out[row] = lse;
-      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-      if (y != lv.ignore_index) {
-        if (y >= 0 && y < v) {
-          valid = 1;
-          li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
-          const float ref = mref[row];
-          if (m > ref) {
-            f = 1.f;
-            fix_list[atomicAdd(fix_count, 1)] = lrow;
-          } else {
-            // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
-            f = exp2f(ref - lse2);
-            const float gy = exp2f(fmaf(tgt[row], kLog2e, -ref)) - exp2f(lse2 - ref);
-            P[static_cast<int64_t>(lrow) * vp + y] = __float2bfloat16_rn(gy);
-          }
-        } else {
-          atomicCAS(status, 0, kErrLabel);
-        }
-      }
-      rowscale[lrow] = f;
-      if (loss_rows) loss_rows[row] = static_cast<float>(li);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      li += __shfl_down_sync(0xffffffffu, li, o);
-      valid += __shfl_down_sync(0xffffffffu, valid, o);
-    }
-    if (lane == 0) {
-      blk_loss[r0 / kRefRowsPerBlock + blockIdx.x] = li;
-      blk_valid[r0 / kRefRowsPerBlock + blockIdx.x] = valid;
-    }
-    if (lane < kRefRowsPerBlock) s_f[lane] = f;
-  }
-  __syncthreads();
+  constexpr int kPre = 8;
   const int h8 = h / 8;
   const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(r0 + lrow0) * h);
   uint4* xo = reinterpret_cast<uint4*>(xs + static_cast<int64_t>(lrow0) * h);
   const int total = nr * h8;
-#pragma unroll 4
-  for (int q = threadIdx.x; q < total; q += blockDim.x) {
+  uint4 xv[kPre];
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    if (q < total) xv[k] = xr[q];
+  }
+  double li = 0.0;
+  int valid = 0;
+  float f = 0.f;
+  if (warp < nr) {
+    const int lrow = lrow0 + warp;
+    const int row = r0 + lrow;
+    const float pm = lane < vsplit ? part_m[static_cast<int64_t>(lane) * n + row] : -INFINITY;
+    const float pl = lane < vsplit ? part_l[static_cast<int64_t>(lane) * n + row] : 0.f;
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    const float z = tgt[row];
+    const float ref = mref[row];
+    float m = pm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    float l = lane < vsplit ? pl * exp2f(pm - m) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+    const float lse2 = m + log2f(l);
+    const float lse = lse2 * kLn2;
+    if (y != lv.ignore_index) {
+      if (y >= 0 && y < v) {
+        valid = 1;
+        li = static_cast<double>(lse) - static_cast<double>(z);
+        f = m > ref ? 1.f : exp2f(ref - lse2);
+      } else if (lane == 0) {
+        atomicCAS(status, 0, kErrLabel);
+      }
+    }
+    if (lane == 0) {
+      lse_out[row] = lse;
+      rowscale[lrow] = f;
+      if (loss_rows) loss_rows[row] = static_cast<float>(li);
+      if (valid) {
+        if (m > ref) {
+          fix_list[atomicAdd(fix_count, 1)] = lrow;
+        } else {
+          // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
+          const float gy = exp2f(fmaf(z, kLog2e, -ref)) - exp2f(lse2 - ref);
+          P[static_cast<int64_t>(lrow) * vp + y] = __float2bfloat16_rn(gy);
+        }
+      }
+      s_f[warp] = f;
+      s_li[warp] = li;
+      s_valid[warp] = valid;
+    }
+  } else if (lane == 0 && warp < kRefRowsPerBlock) {
+    s_f[warp] = 0.f;
+    s_li[warp] = 0.0;
+    s_valid[warp] = 0;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double bl = 0.0;
+    int bv = 0;
+    for (int w = 0; w < kRefRowsPerBlock; ++w) {
+      bl += s_li[w];
+      bv += s_valid[w];
+    }
+    blk_loss[r0 / kRefRowsPerBlock + blockIdx.x] = bl;
+    blk_valid[r0 / kRefRowsPerBlock + blockIdx.x] = bv;
+  }
+  auto scale_store = [&](int q, const uint4& u) {
     const float c = s_f[q / h8];
-    const uint4 u = xr[q];
     const uint32_t in[4] = {u.x, u.y, u.z, u.w};
     uint32_t o[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e)
       o[e] = pack_bf16x2(__uint_as_float(in[e] << 16) * c, __uint_as_float(in[e] & 0xFFFF0000u) * c);
     xo[q] = make_uint4(o[0], o[1], o[2], o[3]);
+  };
+#pragma unroll
+  for (int k = 0; k < kPre; ++k) {
+    const int q = threadIdx.x + k * blockDim.x;
+    if (q < total) scale_store(q, xv[k]);
   }
+#pragma unroll 4
+  for (int q = threadIdx.x + kPre * blockDim.x; q < total; q += blockDim.x) scale_store(q, xr[q]);
 }
 
 // The rows finalize_ref listed (a tile of theirs was stored relative to its
@@ -1505,7 +1549,8 @@ cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, i
                                 float* rowscale, const void* X, void* xs, void* P, int* fix_list, int* fix_count,
                                 int* status, cudaStream_t stream) {
   const int blocks = (rows + kRefRowsPerBlock - 1) / kRefRowsPerBlock;
-  return launch_k(finalize_ref_kernel, dim3(blocks), dim3(256), 0, stream, r0, rows, n, h, v, vp, vsplit, vtiles, lv,
+  return launch_k(finalize_ref_kernel, dim3(blocks), dim3(kRefRowsPerBlock * 32), 0, stream, r0, rows, n, h, v, vp,
+                  vsplit, vtiles, lv,
                   part_m, part_l, tgt, mref, mtile, lse, loss_rows, blk_loss, blk_valid, rowscale,
                   static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(xs),
                   static_cast<__nv_bfloat16*>(P), fix_list, fix_count, status);
