@@ -387,8 +387,13 @@ def run_flce(args, rank, world, local_rank):
     dom = "dxdw"
     n_l, ms_l, fl_l = prof_dom[dom]
     achieved = (fl_l / n_l) / ((ms_l / n_l) / 1e3) / 1e12
-    peak = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
+    peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # a timed region that ran at full clock with no power capping is compared with the burst
+    # peak, one that was power-capped (a long, heavy run) with the sustained peak
+    capped = "sw_power_cap" in clk.get("reasons", []) or (
+        clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"])
+    peak, peak_kind = (peak_sust, "bf16_tflops_sustained") if capped else (peak_burst, "bf16_tflops (burst)")
     gpu_launches = per_step["launches"] * args.steps
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -405,8 +410,10 @@ def run_flce(args, rank, world, local_rank):
         "wall_ms_per_step_incl_flush": 1e3 * t_wall / args.steps,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "peak_note": f"{peak_src} bf16_tflops_sustained (kernel timed inside a "
-                                                           f"long loop); of burst {peak_burst}: {achieved / peak_burst:.3f}",
+                     "frac": achieved / peak,
+                     "peak_note": f"{peak_src} {peak_kind} ({'power-capped' if capped else 'full clock'} during the "
+                                  f"timed region); of burst {peak_burst}: {achieved / peak_burst:.3f}, of sustained "
+                                  f"{peak_sust}: {achieved / peak_sust:.3f}",
                      "traffic": traffic_record(dom, args.config)},
         "kernels": kinds,
         "kernels_note": "separate untimed pass with every launch bracketed by events (which serialises the "
