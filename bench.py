@@ -47,6 +47,7 @@ def parse_args():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-naive", action="store_true", help="skip timing the unfused torch lm_head + cross_entropy")
     ap.add_argument("--op", choices=["fwd_bwd", "topk", "soft"], default="fwd_bwd",
                     help="fwd_bwd: fused loss + gradients (the benchmark); topk: per-row top-k logits; "
                          "soft: KL against sparse soft targets, forward + backward")
@@ -132,6 +133,54 @@ def cpu_cores():
         return len(os.sched_getaffinity(0))
     except AttributeError:
         return os.cpu_count() or 1
+
+
+def torch_naive(X, W, y, problem, flush, stream, torch, steps=5):
+    """The unfused computation the fused call replaces, in plain torch: logits = X W^T (bf16),
+    cross_entropy on their fp32 copy, autograd backward.  Time per step and the peak memory it
+    allocates beyond its inputs, or the allocation failure."""
+    import torch.nn.functional as F
+    yl = y.long()
+
+    def step():
+        Xr = X.detach().requires_grad_()
+        Wr = W.detach().requires_grad_()
+        loss = F.cross_entropy((Xr @ Wr.T).float(), yl, ignore_index=problem.ignore_index,
+                               reduction=problem.reduction)
+        loss.backward()
+        return loss
+
+    dev = X.device
+    need = 16 * problem.n * problem.v  # bf16 logits, their fp32 copy, fp32 log-softmax and its gradient, bf16 grad
+    total = torch.cuda.get_device_properties(dev).total_memory
+    if need > total // 2:
+        return {"unavailable": f"needs about {need / 1e9:.0f} GB of device memory for [N,V] buffers "
+                               f"(more than half of {total / 1e9:.0f} GB); not run"}
+    try:
+        torch.cuda.synchronize()
+        base = torch.cuda.memory_allocated(dev)
+        torch.cuda.reset_peak_memory_stats(dev)
+        step()
+        torch.cuda.synchronize()
+        peak = torch.cuda.max_memory_allocated(dev) - base
+        step()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * steps)]
+        ms = []
+        for i in range(steps):
+            flush.fill_(i & 0xFF)
+            ev[2 * i].record(stream)
+            step()
+            ev[2 * i + 1].record(stream)
+        torch.cuda.synchronize()
+        ms = [ev[2 * i].elapsed_time(ev[2 * i + 1]) for i in range(steps)]
+        t = statistics.median(ms)
+        return {"ms_per_step": t, "value": credited_flops(problem.n, problem.h, problem.v) / (t / 1e3) / 1e12,
+                "unit": UNIT, "peak_alloc_delta_bytes": int(peak),
+                "note": "torch: (X @ W.T).float() -> F.cross_entropy -> backward (cuBLAS + torch kernels), "
+                        "median of 5 steps, L2 flushed between steps"}
+    except torch.cuda.OutOfMemoryError as e:
+        torch.cuda.empty_cache()
+        return {"unavailable": f"out of device memory: {str(e).splitlines()[0][:160]}"}
 
 
 def cpu_baseline(problem, target_s):
@@ -376,6 +425,10 @@ def run_flce(args, rank, world, local_rank):
     h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
     d2h = sum(t.numel() * t.element_size() for t in out)
 
+    naive = None
+    if rank == 0 and world == 1 and not args.no_naive:
+        naive = torch_naive(X, W, y, problem, flush, stream, torch)
+
     if dist is not None:
         dist.barrier()
         dist.destroy_process_group()
@@ -426,6 +479,8 @@ def run_flce(args, rank, world, local_rank):
                         "dX, dW copied out every step; two device buffers on two streams overlap one step's "
                         "copies with the other's kernels"},
     }
+    if naive is not None:
+        line["torch_naive"] = naive
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(problem, args.cpu_seconds)
     print(json.dumps(line), flush=True)
