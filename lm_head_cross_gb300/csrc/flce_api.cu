@@ -490,34 +490,16 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   const int32_t* labels = lv.labels;
   const int vtiles = (v + kBN - 1) / kBN;
   const int h_tiles = (h + kBN - 1) / kBN;
-  // Hard labels: the forward-store references each row to its target logit
-  // (the row factor f_i then finishes G in the dX/dW epilogues); soft targets
-  // keep the tile-max reference and the full fix-up pass.
-  const bool ref_rows = lv.soft_k == 0;
-  const int nblk = ref_rows ? (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock : c.L.nblk;
-  flce_status_t st;
-  if (ref_rows) {
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_label_prep(n, h, v, p.reduction, lv, X, W, c.mref(), reinterpret_cast<int*>(c.part_l()),
-                               c.ticket(), c.n_valid(), c.scale(), c.status(), c.stream);
-    }));
-    if (st != FLCE_OK) return st;
-  } else {
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_label_scan_view(n, v, lv, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
-    }));
-    if (st != FLCE_OK) return st;
-    // soft targets: sum_k q_k z_{i, id_k} per row, before any finalize reads it
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_soft_gather(n, h, v, lv.soft_k, X, W, lv.soft_idx, lv.soft_prob, c.tgt(), c.stream);
-    }));
-    if (st != FLCE_OK) return st;
-    st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr, nullptr, c.n_valid(),
-                                 c.scale(), c.stream);
-    }));
-    if (st != FLCE_OK) return st;
-  }
+  // The forward-store references each row to its target logit (soft targets:
+  // their q-weighted mean logit); the row factor f_i then finishes G in the
+  // dX/dW epilogues, and only rows whose tiles outrun that reference get the
+  // full fix-up pass.
+  const int nblk = (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock;
+  flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_label_prep(n, h, v, p.reduction, lv, X, W, c.mref(), c.tgt(), reinterpret_cast<int*>(c.part_l()),
+                             c.ticket(), c.n_valid(), c.scale(), c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
 
   TcMaps fm;  // forward-store: X, W K-major; p~ store
   if (!make_map(&fm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
@@ -525,9 +507,6 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   TcMaps bm;  // bwd: G K-major (dX A), W MN-major (dX B), dX bf16 out; G MN-major (dW A), X MN-major (dW B), dW fp32
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
-  // dW B operand: X itself, or (per chunk, below) f_i x_i of the chunk's rows
-  if (!ref_rows && !make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK))
-    return FLCE_ERR_CUDA;
   CUtensorMap dw_acc_map, dw_bf16_map;
   if (!make_map(&dw_acc_map, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32))
     return FLCE_ERR_CUDA;
@@ -558,43 +537,28 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.part_l = c.part_l();
     tp.tgt = c.tgt();
     tp.mtile = c.mtile();
-    tp.mref = ref_rows ? c.mref() : nullptr;
+    tp.mref = c.mref();
     tp.zero_words = c.counter();  // the backward launch's tile counter and the fix-up list count start at zero
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
-    if (ref_rows) {
-      st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_finalize_ref(r0, cr, n, h, v, static_cast<int>(c.L.vp), tp.vsplit, vtiles, lv, c.part_m(),
-                                   c.part_l(), c.tgt(), c.mref(), c.mtile(), lse, c.per_row() ? loss : nullptr,
-                                   c.blk_loss(), c.blk_valid(), c.rowscale(), X, c.xs(), c.g(), c.fix_list(),
-                                   c.fix_count(), c.status(), c.stream);
-      }));
-      if (st != FLCE_OK) return st;
-      st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_fixup_list(c.fix_list(), c.fix_count(), r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse,
-                                 c.mtile(), c.g(), 2 * c.dev.sms, c.stream);
-      }));
-      if (st != FLCE_OK) return st;
-    } else {
-      st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_fwd_finalize_rows(r0, cr, n, v, tp.vsplit, lv, c.part_m(), c.part_l(), c.tgt(), lse,
-                                        c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(),
-                                        c.stream);
-      }));
-      if (st != FLCE_OK) return st;
-      st = cuda_status(timed(3, 0.0, c.stream, [&] {
-        return launch_fixup(cr, r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse, c.scale(), c.mtile(), c.g(),
-                            c.stream);
-      }));
-      if (st != FLCE_OK) return st;
-    }
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_finalize_ref(r0, cr, n, h, v, static_cast<int>(c.L.vp), tp.vsplit, vtiles, lv, c.part_m(),
+                                 c.part_l(), c.tgt(), c.mref(), c.mtile(), lse, c.per_row() ? loss : nullptr,
+                                 c.blk_loss(), c.blk_valid(), c.rowscale(), X, c.xs(), c.g(), c.fix_list(),
+                                 c.fix_count(), c.status(), c.stream);
+    }));
+    if (st != FLCE_OK) return st;
+    st = cuda_status(timed(3, 0.0, c.stream, [&] {
+      return launch_fixup_list(c.fix_list(), c.fix_count(), r0, v, static_cast<int>(c.L.vp), vtiles, lv, lse,
+                               c.mtile(), c.g(), 2 * c.dev.sms, c.stream);
+    }));
+    if (st != FLCE_OK) return st;
 
     if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, kBK, kBM)) return FLCE_ERR_CUDA;
     if (!make_map(&bm.a2, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, cr, pitch, 64, kBK)) return FLCE_ERR_CUDA;
-    if (ref_rows && !make_map(&bm.b2, c.xs(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, cr, p.h * 2, 64, kBK))
-      return FLCE_ERR_CUDA;
+    if (!make_map(&bm.b2, c.xs(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, cr, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
     TcParams bp{};
     bp.n = n;
     bp.h = h;
@@ -604,8 +568,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     bp.status = c.status();
     bp.r0 = r0;
     bp.row_end = r0 + cr;
-    bp.b2_r0 = ref_rows ? 0 : r0;
-    bp.rowscale = ref_rows ? c.rowscale() : nullptr;
+    bp.b2_r0 = 0;
+    bp.rowscale = c.rowscale();
     bp.scale = c.scale();
     bp.c0 = 0;
     bp.cw = v;

@@ -101,9 +101,6 @@ struct TcMaps {
 
 // Launchers (asynchronous on `stream`; return the launch error, if any).
 cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream);
-cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m,
-                                const float* part_l, const float* tgt, const int32_t* labels, float* lse,
-                                double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
 // Labels as the kernels read them: with shift, row i takes labels[i + 1] and
 // the last row of each sequence of seq_len rows is ignored.
 struct LabelView {
@@ -119,11 +116,13 @@ struct LabelView {
 cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit, LabelView lv, const float* part_m,
                                      const float* part_l, const float* tgt, float* lse, float* loss_rows,
                                      double* blk_loss, int* blk_valid, int* status, cudaStream_t stream);
-// Fused path with hard labels.  label_prep: label check, the rows' references
-// (target logits, log2 units) and, through the last block, n_valid and s.
+// Fused path.  label_prep: label check, the rows' references (log2 units: the
+// target logit, or for soft targets the q-weighted mean target logit, whose
+// q-weighted sum goes to tgt; +inf for rows without a gradient) and, through
+// the last block, n_valid and s.
 cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, const void* X, const void* W,
-                              float* mref, int* blk_cnt, int* ticket, int* n_valid, float* scale, int* status,
-                              cudaStream_t stream);
+                              float* mref, float* tgt, int* blk_cnt, int* ticket, int* n_valid, float* scale,
+                              int* status, cudaStream_t stream);
 // finalize_ref, rows [r0, r0 + rows) of one chunk: lse, losses and the loss
 // partials (one per kRefRowsPerBlock rows, index r0 / kRefRowsPerBlock + b),
 // the row factors f_i, the chunk buffer's target entries, xs = f x, and the
@@ -138,17 +137,11 @@ cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, i
 cudaError_t launch_fixup_list(const int* fix_list, const int* fix_count, int r0, int v, int vp, int vtiles,
                               LabelView lv, const float* lse, const float* mtile, void* P, int grid,
                               cudaStream_t stream);
-cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
-                         const float* scale, const float* mtile, void* P, cudaStream_t stream);
-cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,
-                               const float* prob, float* tgt, cudaStream_t stream);
 cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
                                  const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
                                  int32_t* out_idx, cudaStream_t stream);
 cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
                                    cudaStream_t stream);
-cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss,
-                              int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,
                                 const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
                                 cudaStream_t stream);

@@ -505,8 +505,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         found = false;
         y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
         if (MODE == kModeFwdStore && p.mref) {
-          zero_row = (y_fwd == p.ignore_index) || y_fwd < 0 || y_fwd >= p.v;
-          ref_row = zero_row ? -INFINITY : p.mref[row];
+          ref_row = (row < row_end) ? p.mref[row] : INFINITY;
+          zero_row = (ref_row == INFINITY);  // no gradient: p~ = 0, the tiles' own maxima for the lse
+          if (zero_row) ref_row = -INFINITY;
         }
         if (MODE == kModeTopk) {
           tk.count = 0;
@@ -909,31 +910,13 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     float m;
     const float lse = merge_ranges(part_m, part_l, vsplit, n, row, &m) * kLn2;
     lse_out[row] = lse;
-    if (lv.soft_k > 0) {
-      // KL(q || p) over the row's target ids: sum_k q_k log q_k + Q lse - sum_k q_k z_k
-      double Q = 0.0, C = 0.0;
-      for (int k = 0; k < lv.soft_k; ++k) {
-        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + k];
-        const int id = lv.soft_idx[static_cast<int64_t>(row) * lv.soft_k + k];
-        if (q > 0.f) {
-          if (id < 0 || id >= v) atomicCAS(status, 0, kErrLabel);
-          Q += q;
-          C += static_cast<double>(q) * log(static_cast<double>(q));
-        }
-      }
-      if (Q > 0.0) {
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
+    if (y != ignore_index) {
+      if (y >= 0 && y < v) {
         valid = 1;
-        li = C + Q * static_cast<double>(lse) - static_cast<double>(tgt[row]);
-      }
-    } else {
-      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
-      if (y != ignore_index) {
-        if (y >= 0 && y < v) {
-          valid = 1;
-          li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
-        } else {
-          atomicCAS(status, 0, kErrLabel);
-        }
+        li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
+      } else {
+        atomicCAS(status, 0, kErrLabel);
       }
     }
     if (loss_rows) loss_rows[row] = static_cast<float>(li);
@@ -1001,54 +984,40 @@ __device__ __forceinline__ void fixup_row(uint4* __restrict__ prow, const float*
   }
 }
 
-// In place over one row chunk of the forward-store buffer:
-//   G = s * valid * (p~ * 2^(ref_tile - lse*log2e) - [j = y])
-// turning the stored, reference-scaled probabilities into the gradient of the
-// logits once the row's log-sum-exp is known.  One block per row.
-__global__ void __launch_bounds__(256) fixup_kernel(int r0, int v, int vp, int vtiles, LabelView lv,
-                                                    const float* __restrict__ lse, const float* __restrict__ scale,
-                                                    const float* __restrict__ mtile, __nv_bfloat16* __restrict__ P) {
-  griddep_begin();
-  __shared__ int s_idx[kTopkMax];
-  __shared__ float s_q[kTopkMax];
-  __shared__ float s_mass;
-  const int lrow = blockIdx.x;
-  const int row = r0 + lrow;
-  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-  float coef = (y != lv.ignore_index) ? *scale : 0.f;
-  const int nsoft = lv.soft_k;
-  if (nsoft > 0) {
-    // soft targets: G = s (Q p - sum_k q_k [j = id_k]), Q = sum_k q_k
-    if (threadIdx.x < nsoft) {
-      const float q = lv.soft_prob[static_cast<int64_t>(row) * nsoft + threadIdx.x];
-      s_q[threadIdx.x] = q > 0.f ? q : 0.f;
-      s_idx[threadIdx.x] = lv.soft_idx[static_cast<int64_t>(row) * nsoft + threadIdx.x];
+// x . w over h bf16 pairs, one warp: fp32 accumulation of the exact
+// products, lanes over 16-byte pieces, then a butterfly sum (every lane holds it).
+__device__ __forceinline__ float warp_dot_bf16(const __nv_bfloat16* __restrict__ x, const __nv_bfloat16* __restrict__ w,
+                                               int h, int lane) {
+  const uint4* xr = reinterpret_cast<const uint4*>(x);
+  const uint4* wr = reinterpret_cast<const uint4*>(w);
+  float dot = 0.f;
+  for (int c = lane; c < h / 8; c += 32) {
+    const uint4 a = xr[c], b = wr[c];
+    const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
+      dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      float m = 0.f;
-      for (int k = 0; k < nsoft; ++k) m += s_q[k];
-      s_mass = m;
-    }
-    __syncthreads();
-    coef = s_mass > 0.f ? *scale : 0.f;
   }
-  const float mass = nsoft > 0 ? s_mass : 1.f;
-  fixup_row(reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp), mtile + static_cast<int64_t>(lrow) * vtiles,
-            v, lse[row] * kLog2e, coef, mass, y, nsoft, s_idx, s_q);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+  return dot;
 }
 
-// Hard labels, fused path, before the first row chunk.  One warp per row: the
-// label check and the row's reference, its target logit in log2 units
-// (ref_i = x_i . w_{y_i} log2 e, fp32 accumulation of the bf16 products); one
-// valid count per block of 8 rows.  The last block to finish (ticket) adds the
-// counts into n_valid and the gradient scale s, and resets the ticket.
+// Fused path, before the first row chunk.  One warp per row: the label check
+// and the row's reference in log2 units — for a hard label its target logit
+// x_i . w_{y_i}, for soft targets the q-weighted mean of the target logits
+// (whose q-weighted sum, the KL's cross term, goes to tgt) — or +inf for a row
+// without a gradient; one valid count per block of 8 rows.  The last block to
+// finish (ticket) adds the counts into n_valid and the gradient scale s, and
+// resets the ticket.
 __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, int reduction, LabelView lv,
                                                          const __nv_bfloat16* __restrict__ X,
                                                          const __nv_bfloat16* __restrict__ W, float* __restrict__ mref,
-                                                         int* __restrict__ blk_cnt, int* __restrict__ ticket,
-                                                         int* __restrict__ n_valid_out, float* __restrict__ scale_out,
-                                                         int* __restrict__ status) {
+                                                         float* __restrict__ tgt, int* __restrict__ blk_cnt,
+                                                         int* __restrict__ ticket, int* __restrict__ n_valid_out,
+                                                         float* __restrict__ scale_out, int* __restrict__ status) {
   griddep_begin();
   __shared__ int s_valid[8];
   __shared__ long long s_sum[256];
@@ -1058,29 +1027,38 @@ __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, in
   const int row = blockIdx.x * 8 + warp;
   int valid = 0;
   if (row < n) {
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
-    float dot = 0.f;
-    if (y != lv.ignore_index) {
-      if (y >= 0 && y < v) {
-        valid = 1;
-        const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(row) * h);
-        const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(y) * h);
-        for (int c = lane; c < h / 8; c += 32) {
-          const uint4 a = xr[c], b = wr[c];
-          const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
-            dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
-          }
+    const __nv_bfloat16* xrow = X + static_cast<int64_t>(row) * h;
+    float ref = INFINITY;
+    if (lv.soft_k > 0) {
+      float Q = 0.f, acc = 0.f;
+      for (int t = 0; t < lv.soft_k; ++t) {
+        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + t];
+        const int id = lv.soft_idx[static_cast<int64_t>(row) * lv.soft_k + t];
+        if (!(q > 0.f)) continue;
+        Q += q;
+        if (id < 0 || id >= v) {
+          if (lane == 0) atomicCAS(status, 0, kErrLabel);
+          continue;
         }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-      } else if (lane == 0) {
-        atomicCAS(status, 0, kErrLabel);
+        acc = fmaf(q, warp_dot_bf16(xrow, W + static_cast<int64_t>(id) * h, h, lane), acc);
+      }
+      if (lane == 0) tgt[row] = acc;
+      if (Q > 0.f) {
+        valid = 1;
+        ref = acc / Q * kLog2e;
+      }
+    } else {
+      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+      if (y != lv.ignore_index) {
+        if (y >= 0 && y < v) {
+          valid = 1;
+          ref = warp_dot_bf16(xrow, W + static_cast<int64_t>(y) * h, h, lane) * kLog2e;
+        } else if (lane == 0) {
+          atomicCAS(status, 0, kErrLabel);
+        }
       }
     }
-    if (lane == 0) mref[row] = dot * kLog2e;
+    if (lane == 0) mref[row] = ref;
   }
   if (lane == 0) s_valid[warp] = valid;
   __syncthreads();
@@ -1114,7 +1092,7 @@ __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, in
 
 static_assert(kMaxSplit <= 32, "finalize_ref_kernel merges one vocabulary range per lane");
 
-// Hard labels, fused path, one row chunk, kRefRowsPerBlock rows per block (one
+// Fused path, one row chunk, kRefRowsPerBlock rows per block (one
 // warp per row, one lane per vocabulary range).
 //  - every thread first starts loading its share of the block's X rows;
 //  - warp w, row w: lse from the per-range (reference, sum) pairs (butterfly
@@ -1158,9 +1136,11 @@ __global__ void __launch_bounds__(kRefRowsPerBlock * 32) finalize_ref_kernel(
   if (warp < nr) {
     const int lrow = lrow0 + warp;
     const int row = r0 + lrow;
+    const int k = lv.soft_k;
     const float pm = lane < vsplit ? part_m[static_cast<int64_t>(lane) * n + row] : -INFINITY;
     const float pl = lane < vsplit ? part_l[static_cast<int64_t>(lane) * n + row] : 0.f;
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    const int y = k > 0 ? lv.ignore_index : label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    const float qv = lane < k ? lv.soft_prob[static_cast<int64_t>(row) * k + lane] : 0.f;
     const float z = tgt[row];
     const float ref = mref[row];
     float m = pm;
@@ -1171,26 +1151,49 @@ __global__ void __launch_bounds__(kRefRowsPerBlock * 32) finalize_ref_kernel(
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     const float lse2 = m + log2f(l);
     const float lse = lse2 * kLn2;
-    if (y != lv.ignore_index) {
+    float Q = 0.f;
+    if (k > 0) {
+      // KL(q || p) over the row's targets: sum_t q_t log q_t + Q lse - sum_t q_t z_t, Q = sum_t q_t
+      double qd = qv > 0.f ? static_cast<double>(qv) : 0.0;
+      double cd = qv > 0.f ? qd * log(qd) : 0.0;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        qd += __shfl_xor_sync(0xffffffffu, qd, o);
+        cd += __shfl_xor_sync(0xffffffffu, cd, o);
+      }
+      Q = static_cast<float>(qd);
+      if (qd > 0.0) {
+        valid = 1;
+        li = cd + qd * static_cast<double>(lse) - static_cast<double>(z);
+      }
+    } else if (y != lv.ignore_index) {
       if (y >= 0 && y < v) {
         valid = 1;
+        Q = 1.f;
         li = static_cast<double>(lse) - static_cast<double>(z);
-        f = m > ref ? 1.f : exp2f(ref - lse2);
       } else if (lane == 0) {
         atomicCAS(status, 0, kErrLabel);
       }
     }
+    // G_ij = s (Q p_ij - q_ij) = s f_i (p~_ij - q_ij / f_i), f_i = Q 2^(ref - lse2)
+    if (valid) f = m > ref ? 1.f : Q * exp2f(ref - lse2);
     if (lane == 0) {
       lse_out[row] = lse;
       rowscale[lrow] = f;
       if (loss_rows) loss_rows[row] = static_cast<float>(li);
       if (valid) {
+        __nv_bfloat16* prow = P + static_cast<int64_t>(lrow) * vp;
         if (m > ref) {
           fix_list[atomicAdd(fix_count, 1)] = lrow;
+        } else if (k == 0) {
+          // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2), from the fp32 logit
+          prow[y] = __float2bfloat16_rn(exp2f(fmaf(z, kLog2e, -ref)) - exp2f(lse2 - ref));
         } else {
-          // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2)
-          const float gy = exp2f(fmaf(z, kLog2e, -ref)) - exp2f(lse2 - ref);
-          P[static_cast<int64_t>(lrow) * vp + y] = __float2bfloat16_rn(gy);
+          for (int t = 0; t < k; ++t) {  // one lane, in order: repeated ids accumulate
+            const float q = lv.soft_prob[static_cast<int64_t>(row) * k + t];
+            const int id = lv.soft_idx[static_cast<int64_t>(row) * k + t];
+            if (q > 0.f && id >= 0 && id < v) prow[id] = __float2bfloat16_rn(__bfloat162float(prow[id]) - q / f);
+          }
         }
       }
       s_f[warp] = f;
@@ -1242,17 +1245,35 @@ __global__ void __launch_bounds__(256) fixup_list_kernel(const int* __restrict__
                                                          const float* __restrict__ mtile,
                                                          __nv_bfloat16* __restrict__ P) {
   griddep_begin();
+  __shared__ int s_idx[kTopkMax];
+  __shared__ float s_q[kTopkMax];
   const int nseg = (v + kFixSegment - 1) / kFixSegment;
   const int items = *fix_count * nseg;
-  for (int e = blockIdx.x; e < items; e += gridDim.x) {
+  const int k = lv.soft_k;
+  for (int e = blockIdx.x; e < items; e += gridDim.x) {  // the same count for the whole block
     const int lrow = fix_list[e / nseg];
     const int seg = e % nseg;
     const int row = r0 + lrow;
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    int y = -1;
+    float mass = 1.f;
+    if (k > 0) {
+      // soft targets: G / s = Q p - sum_t q_t [j = id_t]
+      __syncthreads();  // the previous item's reads of s_q / s_idx are done
+      if (threadIdx.x < k) {
+        const float q = lv.soft_prob[static_cast<int64_t>(row) * k + threadIdx.x];
+        s_q[threadIdx.x] = q > 0.f ? q : 0.f;
+        s_idx[threadIdx.x] = lv.soft_idx[static_cast<int64_t>(row) * k + threadIdx.x];
+      }
+      __syncthreads();
+      mass = 0.f;
+      for (int t = 0; t < k; ++t) mass += s_q[t];
+    } else {
+      y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    }
     const int q0 = seg * (kFixSegment / 8);
     const int q1 = min((v + 7) / 8, q0 + kFixSegment / 8);
     fixup_row(reinterpret_cast<uint4*>(P + static_cast<int64_t>(lrow) * vp),
-              mtile + static_cast<int64_t>(lrow) * vtiles, v, lse[row] * kLog2e, 1.f, 1.f, y, 0, nullptr, nullptr,
+              mtile + static_cast<int64_t>(lrow) * vtiles, v, lse[row] * kLog2e, 1.f, mass, y, k, s_idx, s_q,
               q0, q1);
   }
 }
@@ -1268,25 +1289,12 @@ __global__ void __launch_bounds__(kFinalizeThreads) label_scan_kernel(int n, int
   const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
   int valid = 0;
   if (row < n) {
-    if (lv.soft_k > 0) {
-      float Q = 0.f;
-      for (int k = 0; k < lv.soft_k; ++k) {
-        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + k];
-        const int id = lv.soft_idx[static_cast<int64_t>(row) * lv.soft_k + k];
-        if (q > 0.f) {
-          Q += q;
-          if (id < 0 || id >= v) atomicCAS(status, 0, kErrLabel);
-        }
-      }
-      valid = Q > 0.f;
-    } else {
-      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
-      if (y != ignore_index) {
-        if (y >= 0 && y < v)
-          valid = 1;
-        else
-          atomicCAS(status, 0, kErrLabel);
-      }
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
+    if (y != ignore_index) {
+      if (y >= 0 && y < v)
+        valid = 1;
+      else
+        atomicCAS(status, 0, kErrLabel);
     }
   }
   s_valid[threadIdx.x] = valid;
@@ -1344,40 +1352,6 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
     *n_valid_out = static_cast<int>(nv);
     *scale_out = static_cast<float>(scale);
   }
-}
-
-// Soft targets: tgt_i = sum_k q_ik (x_i . w_{id_ik}), one warp per row, fp32
-// accumulation of the bf16 products (ids with q <= 0 or out of range skipped).
-__global__ void __launch_bounds__(256) soft_gather_kernel(int n, int h, int v, int k, const __nv_bfloat16* __restrict__ X,
-                                                          const __nv_bfloat16* __restrict__ W,
-                                                          const int32_t* __restrict__ idx,
-                                                          const float* __restrict__ prob, float* __restrict__ tgt) {
-  griddep_begin();
-  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int lane = threadIdx.x & 31;
-  if (warp >= n) return;
-  const uint4* xr = reinterpret_cast<const uint4*>(X + static_cast<int64_t>(warp) * h);
-  float acc = 0.f;
-  for (int t = 0; t < k; ++t) {
-    const float q = prob[static_cast<int64_t>(warp) * k + t];
-    const int id = idx[static_cast<int64_t>(warp) * k + t];
-    if (!(q > 0.f) || id < 0 || id >= v) continue;
-    const uint4* wr = reinterpret_cast<const uint4*>(W + static_cast<int64_t>(id) * h);
-    float dot = 0.f;
-    for (int c = lane; c < h / 8; c += 32) {
-      const uint4 a = xr[c], b = wr[c];
-      const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        dot = fmaf(__uint_as_float(av[e] << 16), __uint_as_float(bv[e] << 16), dot);
-        dot = fmaf(__uint_as_float(av[e] & 0xFFFF0000u), __uint_as_float(bv[e] & 0xFFFF0000u), dot);
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
-    acc = fmaf(q, dot, acc);
-  }
-  if (lane == 0) tgt[warp] = acc;
 }
 
 // Top-k pass: merge the per-split candidates of each row into its best k
@@ -1535,12 +1509,12 @@ cudaError_t launch_fwd_finalize_rows(int r0, int rows, int n, int v, int vsplit,
 }
 
 cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, const void* X, const void* W,
-                              float* mref, int* blk_cnt, int* ticket, int* n_valid, float* scale, int* status,
-                              cudaStream_t stream) {
+                              float* mref, float* tgt, int* blk_cnt, int* ticket, int* n_valid, float* scale,
+                              int* status, cudaStream_t stream) {
   const int blocks = (n + 7) / 8;  // 8 rows (warps) per block
   return launch_k(label_prep_kernel, dim3(blocks), dim3(256), 0, stream, n, h, v, reduction, lv,
-                  static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), mref, blk_cnt, ticket,
-                  n_valid, scale, status);
+                  static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), mref, tgt, blk_cnt,
+                  ticket, n_valid, scale, status);
 }
 
 cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
@@ -1563,30 +1537,11 @@ cudaError_t launch_fixup_list(const int* fix_list, const int* fix_count, int r0,
                   vtiles, lv, lse, mtile, static_cast<__nv_bfloat16*>(P));
 }
 
-cudaError_t launch_fwd_finalize(int n, int v, int vsplit, int ignore_index, const float* part_m, const float* part_l,
-                                const float* tgt, const int32_t* labels, float* lse, double* blk_loss, int* blk_valid,
-                                int* status, cudaStream_t stream) {
-  const LabelView lv{labels, ignore_index, 0, 1};
-  return launch_fwd_finalize_rows(0, n, n, v, vsplit, lv, part_m, part_l, tgt, lse, nullptr, blk_loss, blk_valid,
-                                  status, stream);
-}
-
-cudaError_t launch_fixup(int rows, int r0, int v, int vp, int vtiles, LabelView lv, const float* lse,
-                         const float* scale, const float* mtile, void* P, cudaStream_t stream) {
-  return launch_k(fixup_kernel, dim3(rows), dim3(256), 0, stream,
-                  r0, v, vp, vtiles, lv, lse, scale, mtile, static_cast<__nv_bfloat16*>(P));
-}
-
 cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
                                    cudaStream_t stream) {
   const int blocks = (n + kFinalizeThreads - 1) / kFinalizeThreads;
   return launch_k(label_scan_kernel, dim3(blocks), dim3(kFinalizeThreads), 0, stream,
                   n, v, lv, blk_loss, blk_valid, status);
-}
-
-cudaError_t launch_label_scan(int n, int v, int ignore_index, const int32_t* labels, double* blk_loss, int* blk_valid,
-                              int* status, cudaStream_t stream) {
-  return launch_label_scan_view(n, v, LabelView{labels, ignore_index, 0, 1}, blk_loss, blk_valid, status, stream);
 }
 
 cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk_valid, int reduction,
@@ -1606,13 +1561,6 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
   if (blocks < 1) blocks = 1;
   return launch_k(convert_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream, src,
                   static_cast<__nv_bfloat16*>(dst), count8);
-}
-
-cudaError_t launch_soft_gather(int n, int h, int v, int k, const void* X, const void* W, const int32_t* idx,
-                               const float* prob, float* tgt, cudaStream_t stream) {
-  const int blocks = (n + 7) / 8;  // 8 warps per block, one row each
-  return launch_k(soft_gather_kernel, dim3(blocks), dim3(256), 0, stream,
-                  n, h, v, k, static_cast<const __nv_bfloat16*>(X), static_cast<const __nv_bfloat16*>(W), idx, prob, tgt);
 }
 
 cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,

@@ -82,3 +82,26 @@ def test_soft_target_id_out_of_range_sets_status():
     q = torch.full((256, 2), 0.5, device="cuda")
     _, _, _, _, ws = flce.soft_fwd_bwd(X, W, idx, q)
     assert flce.read_device_status(ws) == 5
+
+
+def test_soft_targets_wide_logit_range_and_repeated_ids():
+    """Rows whose logits spread far past the reference span (×16 and ×64 rows: the
+    list fix-up with soft targets), and a row that names one id twice (its two
+    probabilities add), over two row chunks."""
+    n, h, v, k = 1500, 128, 4001, 8
+    idx, q = _teacher_targets(n, h, v, k, seed=85)
+    idx[11, 3] = idx[11, 0]                                         # repeated id
+    p = synth.make_problem(n, h, v, seed=86, w_std=0.05)
+    xf = synth.bf16_bits_to_f32(p.X) * np.array([1.0, 16.0, 64.0], np.float32)[np.arange(n) % 3][:, None]
+    p.X = synth.f32_to_bf16_bits(xf)
+    X, W, _ = to_device(p)
+    loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), "mean")
+    assert flce.read_device_status(ws) == 0
+    ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), "mean")
+    assert_loss(float(loss.item()), ref["loss"])
+    assert_lse(lse.cpu().numpy(), ref["lse"])
+    got_dx = dX.float().cpu().numpy()
+    for g in range(3):
+        rows = np.arange(n) % 3 == g
+        assert_grad(got_dx[rows], ref["dX"][rows], name=f"dX rows x{[1, 16, 64][g]}")
+    assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
