@@ -606,8 +606,12 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
 }
 
 // Top-k pass: the forward with a per-row best-k list, then the merge.
-size_t topk_extra_bytes(const flce_problem_t& p) {
+size_t topk_cand_bytes(const flce_problem_t& p) {
   return align_up(static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * (sizeof(float) + sizeof(int32_t)));
+}
+
+size_t topk_extra_bytes(const flce_problem_t& p) {
+  return topk_cand_bytes(p) + align_up(static_cast<size_t>(p.n) * sizeof(unsigned));  // + shared thresholds
 }
 
 flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_t* out_idx, float* out_val, float* lse) {
@@ -616,11 +620,15 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   float* cand_val = reinterpret_cast<float*>(c.ws + base.total);
   int32_t* cand_idx = reinterpret_cast<int32_t*>(
       c.ws + base.total + static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * sizeof(float));
+  unsigned* thr = reinterpret_cast<unsigned*>(c.ws + base.total + topk_cand_bytes(p));
+  if (cudaMemsetAsync(thr, 0, static_cast<size_t>(p.n) * sizeof(unsigned), c.stream) != cudaSuccess)
+    return FLCE_ERR_CUDA;
   TcMaps maps;
   if (!make_map(&maps.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
   if (!make_map(&maps.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
   maps.out = maps.a2 = maps.b2 = maps.out2 = maps.a;
   TcParams tp{};
+  tp.topk_thr = thr;
   tp.n = static_cast<int>(p.n);
   tp.h = static_cast<int>(p.h);
   tp.v = static_cast<int>(p.v);

@@ -87,6 +87,7 @@ struct TcParams {
   float* topk_val;
   int32_t* topk_idx;
   int topk_k;
+  unsigned* topk_thr;   // top-k: per row the best 16th-best value any range has reached (ordered key), zeroed
 };
 
 struct TcMaps {

@@ -406,7 +406,18 @@ struct TopkBuf {
   int* idx;      // [kTopkCand][32]
   int count;
   float thr;
+  unsigned* shared_thr;  // the row's threshold shared by all its vocabulary ranges (global memory), or null
 };
+
+// Order-preserving map of a float to an unsigned (0 stands below every float).
+__device__ __forceinline__ unsigned topk_key(float f) {
+  const unsigned b = __float_as_uint(f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float topk_unkey(unsigned u) {
+  if (u == 0u) return -INFINITY;
+  return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
 
 __device__ __forceinline__ bool topk_better(float av, int ai, float bv, int bi) {
   return av > bv || (av == bv && static_cast<unsigned>(ai) < static_cast<unsigned>(bi));
@@ -442,7 +453,11 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
     const float kth = __shfl_sync(0xffffffffu, v, kTopkMax - 1);
     if (lane == L) {
       b.count = min(cnt, kTopkMax);
-      if (cnt >= kTopkMax) b.thr = kth;
+      if (cnt >= kTopkMax) {
+        b.thr = kth;
+        // 16 values of this row are >= kth, so any value below it, in any range, is out
+        if (b.shared_thr) atomicMax(b.shared_thr, topk_key(kth));
+      }
     }
   }
 }
@@ -478,6 +493,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   tk.idx = reinterpret_cast<int*>(stg + kTopkCand * 32 * sizeof(float));
   tk.count = 0;
   tk.thr = -INFINITY;
+  tk.shared_thr = nullptr;
+  float gthr = -INFINITY;  // top-k: the row's shared threshold as last read
   static_assert(kTopkCand * 32 * 8 <= kStagingPerWarp, "top-k candidates fit the staging area");
   float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
   bool found = false;
@@ -512,8 +529,10 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         if (MODE == kModeTopk) {
           tk.count = 0;
           tk.thr = -INFINITY;
+          tk.shared_thr = (p.topk_thr && row < row_end) ? p.topk_thr + row : nullptr;
         }
       }
+      if (MODE == kModeTopk && tk.shared_thr) gthr = topk_unkey(*reinterpret_cast<volatile unsigned*>(tk.shared_thr));
       if (MODE == kModeForward || MODE == kModeTopk) {
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
@@ -550,13 +569,15 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           if (MODE == kModeTopk) {
             // groups of 8: a buffer holding at most kTopkCand - 8 never overflows, and a
             // lane is compacted only once it has gathered more than that
+            // a value must beat this range's own 16th best (ids grow along the range, so an
+            // equal later value ranks after it) and be no lower than the row's shared threshold
 #pragma unroll
             for (int hh = 0; hh < 4; ++hh) {
-              if (cmax > tk.thr) {
+              if (cmax > tk.thr && cmax >= gthr) {
 #pragma unroll
                 for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
                   const float x = __uint_as_float(v[j]);
-                  if (x > tk.thr) {
+                  if (x > tk.thr && x >= gthr) {
                     tk.val[tk.count * 32 + lane] = x;
                     tk.idx[tk.count * 32 + lane] = col0 + j;
                     ++tk.count;
