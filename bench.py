@@ -54,6 +54,8 @@ def parse_args():
     ap.add_argument("--k", type=int, default=8, help="k of --op topk / soft")
     ap.add_argument("--reduction", choices=["mean", "sum", "none"], default=None, help="override the workload's")
     ap.add_argument("--shift", type=int, default=0, help="1: causal next-token shift inside the kernels")
+    ap.add_argument("--workspace", choices=["full", "min"], default="full",
+                    help="min: flce_workspace_bytes_min, the recompute path (8NHV executed)")
     return ap.parse_args()
 
 
@@ -306,7 +308,8 @@ def run_flce(args, rank, world, local_rank):
     X = torch.from_numpy(problem.X.view(np.int16)).view(torch.bfloat16).to(dev)
     W = torch.from_numpy(problem.W.view(np.int16)).view(torch.bfloat16).to(dev)
     y = torch.from_numpy(problem.labels).to(dev)
-    ws_bytes = flce.workspace_bytes(n, h, v, problem.ignore_index, problem.reduction)
+    ws_bytes = (flce.workspace_bytes_min if args.workspace == "min" else flce.workspace_bytes)(
+        n, h, v, problem.ignore_index, problem.reduction)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = (torch.empty(1, dtype=torch.float32, device=dev), torch.empty(n, dtype=torch.float32, device=dev),
            torch.empty_like(X), torch.empty_like(W))

@@ -303,3 +303,22 @@ def test_fwd_bwd_host_matches_device_call():
     assert np.array_equal(out[3].float().numpy(), a["dW"])
     with pytest.raises(flce.FlceError):
         flce.fwd_bwd_host(xh, wh, yh, out, dev[:1024], p.ignore_index, p.reduction)
+
+
+def test_profile_mask_times_only_the_selected_kinds():
+    """flce_profile_enable(mask): only launches of the selected kinds are bracketed."""
+    p = synth.make_problem(600, 128, 3000, seed=48, labels="zipf", ignore_frac=0.05)
+    X, W, y = to_device(p)
+    flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction)
+    torch.cuda.synchronize()
+    flce.profile_enable(True, kinds=["dxdw"])
+    flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction)
+    only = flce.profile_read()
+    flce.profile_enable(True)
+    flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction)
+    every = flce.profile_read()
+    flce.profile_enable(False)
+    assert only["dxdw"][0] == every["dxdw"][0] > 0
+    assert only["forward"][0] == only["small"][0] == 0
+    assert every["forward"][0] > 0 and every["small"][0] > 0
+    assert every["dxdw"][2] == pytest.approx(4.0 * p.n * p.h * p.v)   # the credited flops of the contraction
