@@ -395,7 +395,7 @@ __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int la
 // ----------------------------------------------------------------------------- top-k candidates
 // Each epilogue thread (one row) appends (logit, id) candidates that beat its
 // row's threshold to a buffer in the warp's shared-memory staging area (entry e
-// of lane l at [e][l]: no bank conflicts).  Whenever a lane holds more than
+// of lane l at topk_slot(e, l)).  Whenever a lane holds more than
 // kTopkMax, the whole warp compacts that lane's buffer with one 32-wide bitonic
 // sort, keeping the best kTopkMax; the threshold becomes the smallest kept.
 
@@ -408,6 +408,11 @@ struct TopkBuf {
   float thr;
   unsigned* shared_thr;  // the row's threshold shared by all its vocabulary ranges (global memory), or null
 };
+
+// Word of entry e of lane l's buffer.  Rows of 32 words, the lane index XORed
+// with the entry: a warp appending at equal counts, and a warp reading one
+// lane's whole buffer (entry e by lane e), both touch 32 different banks.
+__device__ __forceinline__ int topk_slot(int e, int l) { return e * 32 + (l ^ e); }
 
 // Order-preserving map of a float to an unsigned (0 stands below every float).
 __device__ __forceinline__ unsigned topk_key(float f) {
@@ -429,8 +434,8 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
     const int L = __ffs(mask) - 1;
     mask &= mask - 1;
     const int cnt = __shfl_sync(0xffffffffu, b.count, L);
-    float v = lane < cnt ? b.val[lane * 32 + L] : -INFINITY;
-    int i = lane < cnt ? b.idx[lane * 32 + L] : -1;
+    float v = lane < cnt ? b.val[topk_slot(lane, L)] : -INFINITY;
+    int i = lane < cnt ? b.idx[topk_slot(lane, L)] : -1;
 #pragma unroll
     for (int kk = 2; kk <= 32; kk <<= 1) {
 #pragma unroll
@@ -447,8 +452,8 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
     }
     // lanes now hold the candidates high to low; keep the best kTopkMax
     if (lane < kTopkMax) {
-      b.val[lane * 32 + L] = v;
-      b.idx[lane * 32 + L] = i;
+      b.val[topk_slot(lane, L)] = v;
+      b.idx[topk_slot(lane, L)] = i;
     }
     const float kth = __shfl_sync(0xffffffffu, v, kTopkMax - 1);
     if (lane == L) {
@@ -578,8 +583,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
                 for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
                   const float x = __uint_as_float(v[j]);
                   if (x > tk.thr && x >= gthr) {
-                    tk.val[tk.count * 32 + lane] = x;
-                    tk.idx[tk.count * 32 + lane] = col0 + j;
+                    tk.val[topk_slot(tk.count, lane)] = x;
+                    tk.idx[topk_slot(tk.count, lane)] = col0 + j;
                     ++tk.count;
                   }
                 }
@@ -651,8 +656,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           const int kept = tk.count;  // at most kTopkMax (the merge does not need them sorted)
           const int64_t base = (static_cast<int64_t>(t.split) * p.n + row) * kTopkMax;
           for (int i = 0; i < kTopkMax; ++i) {
-            p.topk_val[base + i] = i < kept ? tk.val[i * 32 + lane] : -INFINITY;
-            p.topk_idx[base + i] = i < kept ? tk.idx[i * 32 + lane] : -1;
+            p.topk_val[base + i] = i < kept ? tk.val[topk_slot(i, lane)] : -INFINITY;
+            p.topk_idx[base + i] = i < kept ? tk.idx[topk_slot(i, lane)] : -1;
           }
         }
       }
