@@ -89,7 +89,8 @@ typedef struct {
  * (0 if p is invalid): the minimum size plus room for flce_fwd_bwd's fused path,
  * i.e. a chunk of R rows of the bf16 vocabulary gradient (R x V, at most 1 GiB,
  * at least two chunks once N > 256), one fp32 per (chunk row, 256-wide
- * vocabulary tile) and an fp32 dW accumulator (V x H). */
+ * vocabulary tile), an fp32 dW accumulator (V x H), the chunk's rows of X
+ * scaled by their per-row factor (R x H bf16) and O(N) per-row words. */
 size_t flce_workspace_bytes(const flce_problem_t* p);
 
 /* Smallest workspace every call below accepts (0 if p is invalid): the device

@@ -544,8 +544,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
     if (st != FLCE_OK) return st;
     st = cuda_status(timed(3, 0.0, c.stream, [&] {
-      return launch_finalize_ref(r0, cr, n, h, v, static_cast<int>(c.L.vp), tp.vsplit, vtiles, lv, c.part_m(),
-                                 c.part_l(), c.tgt(), c.mref(), c.mtile(), lse, c.per_row() ? loss : nullptr,
+      return launch_finalize_ref(r0, cr, n, h, v, static_cast<int>(c.L.vp), tp.vsplit, lv, c.part_m(), c.part_l(),
+                                 c.tgt(), c.mref(), lse, c.per_row() ? loss : nullptr,
                                  c.blk_loss(), c.blk_valid(), c.rowscale(), X, c.xs(), c.g(), c.fix_list(),
                                  c.fix_count(), c.status(), c.stream);
     }));

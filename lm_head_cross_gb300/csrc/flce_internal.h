@@ -129,9 +129,9 @@ cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, 
 // the row factors f_i, the chunk buffer's target entries, xs = f x, and the
 // list of rows a tile stored relative to its own max (fix_list / fix_count).
 constexpr int kRefRowsPerBlock = 8;
-cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, LabelView lv,
                                 const float* part_m, const float* part_l, const float* tgt, const float* mref,
-                                const float* mtile, float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
+                                float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
                                 float* rowscale, const void* X, void* xs, void* P, int* fix_list, int* fix_count,
                                 int* status, cudaStream_t stream);
 // The listed rows' full fix-up (G / s in place), `grid` blocks.

@@ -8,12 +8,16 @@
 //   kModeForward   S = X W^T tile by tile (K = H) into TMEM; the epilogue keeps
 //                  a running (max, sum-of-exp) per row over the vocabulary tiles
 //                  of its split and picks out the target logit.
-//   kModeFwdStore  the same, and it also writes p~ = 2^(S - tile max) as bf16
-//                  for one row chunk (fused forward + backward).
+//   kModeFwdStore  the same, and it also writes p~ = 2^(S log2 e - r) as bf16
+//                  for one row chunk (fused forward + backward), r the row's
+//                  reference (its target logit) or, past a span, the tile max.
+//   kModeTopk      the forward's log-sum-exp plus each row's best 16 logits
+//                  and their ids per vocabulary range.
 //   kModeGrad      recomputes S for one vocabulary chunk and writes
 //                  G = s (exp(S - lse) - onehot) valid as bf16.
-//   kModeBwd       dX and dW tiles of one chunk of G in one launch, handed out
-//                  longest-first by a global counter.
+//   kModeBwd       dX and dW tiles of one chunk of G (or of p~ with per-row
+//                  factors) in one launch, handed out longest-first by a
+//                  global counter.
 //
 // CTA pairs: every launch is a grid of 2-CTA clusters.  A pair owns a 256 x 256
 // output tile; each CTA stages its own 128 rows of A and its own half (128 rows)
@@ -1130,9 +1134,9 @@ static_assert(kMaxSplit <= 32, "finalize_ref_kernel merges one vocabulary range 
 //  - the block's loss partial, summed over its rows in order;
 //  - all threads: xs_i = f_i x_i (bf16), the dW contraction's B operand.
 __global__ void __launch_bounds__(kRefRowsPerBlock * 32) finalize_ref_kernel(
-    int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+    int r0, int rows, int n, int h, int v, int vp, int vsplit, LabelView lv,
     const float* __restrict__ part_m, const float* __restrict__ part_l, const float* __restrict__ tgt,
-    const float* __restrict__ mref, const float* __restrict__ mtile, float* __restrict__ lse_out,
+    const float* __restrict__ mref, float* __restrict__ lse_out,
     float* __restrict__ loss_rows, double* __restrict__ blk_loss, int* __restrict__ blk_valid,
     float* __restrict__ rowscale, const __nv_bfloat16* __restrict__ X, __nv_bfloat16* __restrict__ xs,
     __nv_bfloat16* __restrict__ P, int* __restrict__ fix_list, int* __restrict__ fix_count,
@@ -1543,15 +1547,15 @@ cudaError_t launch_label_prep(int n, int h, int v, int reduction, LabelView lv, 
                   ticket, n_valid, scale, status);
 }
 
-cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, int vtiles, LabelView lv,
+cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, int vsplit, LabelView lv,
                                 const float* part_m, const float* part_l, const float* tgt, const float* mref,
-                                const float* mtile, float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
+                                float* lse, float* loss_rows, double* blk_loss, int* blk_valid,
                                 float* rowscale, const void* X, void* xs, void* P, int* fix_list, int* fix_count,
                                 int* status, cudaStream_t stream) {
   const int blocks = (rows + kRefRowsPerBlock - 1) / kRefRowsPerBlock;
   return launch_k(finalize_ref_kernel, dim3(blocks), dim3(kRefRowsPerBlock * 32), 0, stream, r0, rows, n, h, v, vp,
-                  vsplit, vtiles, lv,
-                  part_m, part_l, tgt, mref, mtile, lse, loss_rows, blk_loss, blk_valid, rowscale,
+                  vsplit, lv,
+                  part_m, part_l, tgt, mref, lse, loss_rows, blk_loss, blk_valid, rowscale,
                   static_cast<const __nv_bfloat16*>(X), static_cast<__nv_bfloat16*>(xs),
                   static_cast<__nv_bfloat16*>(P), fix_list, fix_count, status);
 }
