@@ -580,20 +580,22 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             // lane is compacted only once it has gathered more than that
             // a value must beat this range's own 16th best (ids grow along the range, so an
             // equal later value ranks after it) and be no lower than the row's shared threshold
+            // (a warp vote per value: a value that no lane keeps costs three instructions)
+            if (__any_sync(0xffffffffu, cmax > tk.thr && cmax >= gthr)) {
 #pragma unroll
-            for (int hh = 0; hh < 4; ++hh) {
-              if (cmax > tk.thr && cmax >= gthr) {
+              for (int hh = 0; hh < 4; ++hh) {
 #pragma unroll
                 for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
                   const float x = __uint_as_float(v[j]);
-                  if (x > tk.thr && x >= gthr) {
+                  const bool keep = x > tk.thr && x >= gthr;
+                  if (__any_sync(0xffffffffu, keep) && keep) {
                     tk.val[topk_slot(tk.count, lane)] = x;
                     tk.idx[topk_slot(tk.count, lane)] = col0 + j;
                     ++tk.count;
                   }
                 }
+                topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8));
               }
-              topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8));
             }
           }
         }
