@@ -621,10 +621,17 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
               if (j == yi) z_tgt = __uint_as_float(v[j]);
             found = true;
           }
-          const int nv = min(32, p.v - col0);
+          const int nv = p.v - col0;
+          if (nv >= 32) {  // full chunk: four independent max chains, no column test
+            float m4[4] = {tmax, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int j = 0; j < 32; ++j)
-            if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
+            for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(v[j]));
+            tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
+          }
         }
         const float tmax2 = tmax * kLog2e;
         const float ref = (tmax2 - ref_row > kRefSpan) ? tmax2 : ref_row;
@@ -638,12 +645,28 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           tmem_ld_32x64(tbase + g * 64, v);
           const int nv = p.v - col0;
           uint32_t w[32];
+          if (nv >= 64) {  // full group: no column test, four independent sums
+            float s4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref)) : 0.f;
-            const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref)) : 0.f;
-            sum += a + b;
-            w[j] = zero_row ? 0u : pack_bf16x2(a, b);
+            for (int j = 0; j < 32; ++j) {
+              const float a = fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref));
+              const float b = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref));
+              s4[j & 3] += a + b;
+              w[j] = pack_bf16x2(a, b);
+            }
+            sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+              const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref)) : 0.f;
+              const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref)) : 0.f;
+              sum += a + b;
+              w[j] = pack_bf16x2(a, b);
+            }
+          }
+          if (zero_row) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) w[j] = 0u;
           }
           stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
         }
