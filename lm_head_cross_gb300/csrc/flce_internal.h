@@ -34,8 +34,9 @@ int chunk_width(int64_t n);
 
 enum Mode : int { kModeForward = 0, kModeGrad = 1, kModeBwd = 2, kModeFwdStore = 3, kModeTopk = 4 };
 
-// Forward-store: a row's p~ is stored relative to its target logit (log2
-// units) unless a tile's max lies more than this above it.
+// Forward-store: a row's p~ is stored relative to its reference logit (log2
+// units) unless a tile's p~ sum exceeds 2^kRefSpan; then relative to the
+// tile's max.
 constexpr float kRefSpan = 64.f;
 
 constexpr int kTopkMax = 16;     // largest k of flce_topk / of soft targets per row
@@ -79,7 +80,7 @@ struct TcParams {
   // row chunk of the forward-store pass: rows [r0, row_end) (row_end 0 means n)
   int r0, row_end;
   float* mtile;         // forward-store: per (chunk row, vocabulary tile) reference exponent, log2 units
-  const float* mref;    // forward-store: per row of X its target logit, log2 units (null: tile maxima only)
+  const float* mref;    // forward-store: per row of X its reference logit, log2 units
   const float* rowscale;  // bwd: per chunk row factor f_i of the stored G / (s f_i) (null: the buffer holds G)
   int b2_r0;            // bwd: first row of the dW B operand's tensor map
   int* zero_words;      // if set: two ints the launch sets to 0 once its predecessors are done

@@ -473,6 +473,35 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
 
 // ----------------------------------------------------------------------------- epilogue
 
+// Forward-store: a row's tile sum above this means some p~ may exceed 2^kRefSpan.
+constexpr float kRefSumMax = 18446744073709551616.0f;  // 2^64
+static_assert(kRefSpan == 64.f, "kRefSumMax is 2^kRefSpan");
+
+// One 64-column group of a row: p~ = 2^(t log2 e - ref) packed as bf16 pairs
+// into w, and their fp32 sum (columns at or past nv count as 0).
+__device__ __forceinline__ float exp_pack_group(const uint32_t (&v)[64], uint32_t (&w)[32], int nv, float ref) {
+  if (nv >= 64) {  // full group: no column test, four independent sums
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      const float a = fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref));
+      const float b = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref));
+      s4[j & 3] += a + b;
+      w[j] = pack_bf16x2(a, b);
+    }
+    return (s4[0] + s4[1]) + (s4[2] + s4[3]);
+  }
+  float sum = 0.f;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref)) : 0.f;
+    const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref)) : 0.f;
+    sum += a + b;
+    w[j] = pack_bf16x2(a, b);
+  }
+  return sum;
+}
+
 template <int MODE>
 __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& pr, uint8_t* staging, uint64_t* tfull,
                              uint64_t* tempty, uint32_t tmem_base, TileRing ring, uint64_t* ebar,
@@ -508,8 +537,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   float run_m = -INFINITY, run_l = 0.f, z_tgt = 0.f;
   bool found = false;
   int y_fwd = p.ignore_index;
-  float ref_row = -INFINITY;  // forward-store: the row's reference exponent (-inf: every tile uses its own max)
-  bool zero_row = false;      // forward-store: the row has no gradient, p~ is written as 0
+  float ref_row = 0.f;  // forward-store: the row's reference exponent, log2 units
   const float scale = (MODE == kModeGrad) ? *p.scale : 0.f;
   const int row_end = p.row_end > 0 ? p.row_end : p.n;
 
@@ -530,11 +558,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_l = 0.f;
         found = false;
         y_fwd = (row < row_end) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
-        if (MODE == kModeFwdStore && p.mref) {
-          ref_row = (row < row_end) ? p.mref[row] : INFINITY;
-          zero_row = (ref_row == INFINITY);  // no gradient: p~ = 0, the tiles' own maxima for the lse
-          if (zero_row) ref_row = -INFINITY;
-        }
+        if (MODE == kModeFwdStore) ref_row = (row < p.n) ? p.mref[row] : 0.f;
         if (MODE == kModeTopk) {
           tk.count = 0;
           tk.thr = -INFINITY;
@@ -601,74 +625,67 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         }
         release_accumulator(&tempty[acc], lane);
       } else {
-        // forward-store: the tile's row max first, then p~ = 2^(t - ref) as
-        // bf16 into the chunk buffer (relative error 2^-9), its fp32 sum into
-        // the running log-sum-exp.  ref is the row's reference exponent (its
-        // target logit) unless the tile's max lies more than kRefSpan above
-        // it, or the row has none; then it is the tile's max.
-        float tmax = -INFINITY;
-#pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
-          const int col0 = t.n0 + c * 32;
-          if (col0 >= p.v) break;
-          __syncwarp();
-          uint32_t v[32];
-          tmem_ld_32x32(tbase + c * 32, v);
-          const int yi = y_fwd - col0;
-          if (static_cast<unsigned>(yi) < 32u) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j == yi) z_tgt = __uint_as_float(v[j]);
-            found = true;
-          }
-          const int nv = p.v - col0;
-          if (nv >= 32) {  // full chunk: four independent max chains, no column test
-            float m4[4] = {tmax, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int j = 0; j < 32; ++j) m4[j & 3] = fmaxf(m4[j & 3], __uint_as_float(v[j]));
-            tmax = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j)
-              if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
-          }
-        }
-        const float tmax2 = tmax * kLog2e;
-        const float ref = (tmax2 - ref_row > kRefSpan) ? tmax2 : ref_row;
+        // forward-store, one pass: p~ = 2^(t log2 e - r) as bf16 into the chunk
+        // buffer (relative error 2^-9), its fp32 sum into the running log-sum-exp,
+        // r the row's reference (its target logit; another of its logits for a
+        // row without a gradient).  A tile whose sum exceeds 2^kRefSpan — so a
+        // value may — is written again relative to its own max.
+        float ref = ref_row;
         float sum = 0.f;
 #pragma unroll 1
         for (int g = 0; g < kBN / 64; ++g) {
           const int col0 = t.n0 + g * 64;
-          if (col0 >= p.v) break;
+          if (col0 >= p.v) break;  // same for the whole warp
           __syncwarp();
           uint32_t v[64];
           tmem_ld_32x64(tbase + g * 64, v);
+          const int yi = y_fwd - col0;
+          if (static_cast<unsigned>(yi) < 64u) {
+#pragma unroll
+            for (int j = 0; j < 64; ++j)
+              if (j == yi) z_tgt = __uint_as_float(v[j]);
+            found = true;
+          }
           const int nv = p.v - col0;
           uint32_t w[32];
-          if (nv >= 64) {  // full group: no column test, four independent sums
-            float s4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float a = fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref));
-              const float b = fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref));
-              s4[j & 3] += a + b;
-              w[j] = pack_bf16x2(a, b);
-            }
-            sum += (s4[0] + s4[1]) + (s4[2] + s4[3]);
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-              const float a = (2 * j < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j]), kLog2e, -ref)) : 0.f;
-              const float b = (2 * j + 1 < nv) ? fast_exp2(fmaf(__uint_as_float(v[2 * j + 1]), kLog2e, -ref)) : 0.f;
-              sum += a + b;
-              w[j] = pack_bf16x2(a, b);
-            }
-          }
-          if (zero_row) {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) w[j] = 0u;
-          }
+          sum += exp_pack_group(v, w, nv, ref);
           stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
+        }
+        const bool over = !(sum <= kRefSumMax);  // also true for a non-finite sum
+        if (__any_sync(0xffffffffu, over)) {
+          // again relative to the tile's max, for the rows that need it (the others
+          // rewrite the same bytes); the first pass's stores land first
+          if (lane == 0) bulk_wait_group_all();
+          __syncwarp();
+          float tmax = -INFINITY;
+#pragma unroll 1
+          for (int c = 0; c < kBN / 32; ++c) {
+            const int col0 = t.n0 + c * 32;
+            if (col0 >= p.v) break;
+            __syncwarp();
+            uint32_t v[32];
+            tmem_ld_32x32(tbase + c * 32, v);
+            const int nv = p.v - col0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+              if (j < nv) tmax = fmaxf(tmax, __uint_as_float(v[j]));
+          }
+          if (over) {
+            ref = tmax * kLog2e;
+            sum = 0.f;
+          }
+#pragma unroll 1
+          for (int g = 0; g < kBN / 64; ++g) {
+            const int col0 = t.n0 + g * 64;
+            if (col0 >= p.v) break;
+            __syncwarp();
+            uint32_t v[64];
+            tmem_ld_32x64(tbase + g * 64, v);
+            uint32_t w[32];
+            const float gs = exp_pack_group(v, w, p.v - col0, ref);
+            if (over) sum += gs;
+            stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
+          }
         }
         release_accumulator(&tempty[acc], lane);
         if (row < row_end) p.mtile[static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN] = ref;
@@ -1063,8 +1080,8 @@ __device__ __forceinline__ float warp_dot_bf16(const __nv_bfloat16* __restrict__
 // Fused path, before the first row chunk.  One warp per row: the label check
 // and the row's reference in log2 units — for a hard label its target logit
 // x_i . w_{y_i}, for soft targets the q-weighted mean of the target logits
-// (whose q-weighted sum, the KL's cross term, goes to tgt) — or +inf for a row
-// without a gradient; one valid count per block of 8 rows.  The last block to
+// (whose q-weighted sum, the KL's cross term, goes to tgt), for a row without
+// a gradient its logit of vocabulary id 0; one valid count per block of 8 rows.  The last block to
 // finish (ticket) adds the counts into n_valid and the gradient scale s, and
 // resets the ticket.
 __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, int reduction, LabelView lv,
@@ -1113,6 +1130,7 @@ __global__ void __launch_bounds__(256) label_prep_kernel(int n, int h, int v, in
         }
       }
     }
+    if (!valid) ref = warp_dot_bf16(xrow, W, h, lane) * kLog2e;
     if (lane == 0) mref[row] = ref;
   }
   if (lane == 0) s_valid[warp] = valid;
