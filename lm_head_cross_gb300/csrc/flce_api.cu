@@ -180,9 +180,11 @@ flce_status_t device_info(Device* d) {
 
 // Forward split count: the number of vocabulary ranges each row tile is cut
 // into.  Picks the count (4..32, at most the number of vocabulary tiles) whose
-// round-robin assignment of (row tile, range) units to `grid` CTAs gives the
-// smallest largest per-CTA tile count; a wave then holds about grid/vsplit row
-// tiles, which keeps the X panels it reads resident in L2.
+// round-robin assignment of (row tile, range) units to `grid` pairs gives the
+// smallest largest per-pair tile count.  Units are numbered row tile fastest,
+// so the pairs of a wave work on few vocabulary ranges across all row tiles:
+// each W tile is read by many pairs at about the same time (from L2), and the
+// rows' X panels stay resident.
 int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
   const int hi = std::min(cap, vocab_tiles);
   const int lo = std::min(4, hi);
@@ -196,7 +198,7 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
     for (int b = 0; b < g; ++b) {
       long long tiles = 0;
       for (long long u = b; u < units; u += g) {
-        const int sp = static_cast<int>(u % vs);
+        const int sp = static_cast<int>(u / row_tiles);
         tiles += (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
       }
       worst = std::max(worst, tiles);

@@ -107,8 +107,8 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
     s.done = true;
     return;
   }
-  s.rt = s.unit / p.vsplit;
-  s.sp = s.unit % p.vsplit;
+  s.rt = s.unit % p.row_tiles;  // consecutive units: the same vocabulary range for every row tile
+  s.sp = s.unit / p.row_tiles;
   s.vt = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
   s.ve = static_cast<int>(static_cast<int64_t>(s.sp + 1) * p.vocab_tiles / p.vsplit);
 }
