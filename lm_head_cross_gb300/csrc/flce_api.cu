@@ -178,6 +178,14 @@ flce_status_t device_info(Device* d) {
   return FLCE_OK;
 }
 
+// Order of a forward launch's (row tile, vocabulary range) units.  Row tile
+// fastest, the pairs of a wave share W tiles in L2 across all row tiles, which
+// pays while the X panels of all row tiles stay resident too (up to 48 MB);
+// past that, ranges fastest keeps a wave on a few row tiles' X panels.
+int units_split_fast(int row_tiles, int64_t h) {
+  return static_cast<int64_t>(row_tiles) * kPairRows * h * 2 > (int64_t{48} << 20) ? 1 : 0;
+}
+
 // Forward split count: the number of vocabulary ranges each row tile is cut
 // into.  Picks the count (4..32, at most the number of vocabulary tiles) whose
 // round-robin assignment of (row tile, range) units to `grid` pairs gives the
@@ -185,7 +193,7 @@ flce_status_t device_info(Device* d) {
 // so the pairs of a wave work on few vocabulary ranges across all row tiles:
 // each W tile is read by many pairs at about the same time (from L2), and the
 // rows' X panels stay resident.
-int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
+int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, bool split_fast) {
   const int hi = std::min(cap, vocab_tiles);
   const int lo = std::min(4, hi);
   int best = lo;
@@ -193,12 +201,12 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
   for (int vs = lo; vs <= hi; ++vs) {
     const long long units = static_cast<long long>(row_tiles) * vs;
     const int g = static_cast<int>(std::min<long long>(grid, units));
-    // per CTA b: units b, b+g, ...; unit u has split u % vs
+    // per pair b: units b, b+g, ...; unit u has split u / row_tiles (u % vs when ranges run fastest)
     long long worst = 0;
     for (int b = 0; b < g; ++b) {
       long long tiles = 0;
       for (long long u = b; u < units; u += g) {
-        const int sp = static_cast<int>(u / row_tiles);
+        const int sp = static_cast<int>(split_fast ? u % vs : u / row_tiles);
         tiles += (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
       }
       worst = std::max(worst, tiles);
@@ -211,17 +219,18 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap) {
   return best;
 }
 
-int choose_vsplit(int row_tiles, int vocab_tiles, int grid, int cap = kMaxSplit) {
+int choose_vsplit(int row_tiles, int vocab_tiles, int grid, int cap = kMaxSplit, bool split_fast = false) {
   static std::mutex mu;
-  static int key[4] = {-1, -1, -1, -1};
+  static int key[5] = {-1, -1, -1, -1, -1};
   static int val = 1;
   std::lock_guard<std::mutex> lock(mu);
-  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid || key[3] != cap) {
-    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid, cap);
+  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid || key[3] != cap || key[4] != split_fast) {
+    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid, cap, split_fast);
     key[0] = row_tiles;
     key[1] = vocab_tiles;
     key[2] = grid;
     key[3] = cap;
+    key[4] = split_fast;
   }
   return val;
 }
@@ -382,7 +391,8 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.status = c.status();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2);
+  tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kMaxSplit, tp.units_split_fast);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
@@ -534,7 +544,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.row_end = r0 + cr;
     tp.row_tiles = (cr + kPairRows - 1) / kPairRows;
     tp.vocab_tiles = vtiles;
-    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms / 2);
+    tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
+    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms / 2, kMaxSplit, tp.units_split_fast);
     tp.part_m = c.part_m();
     tp.part_l = c.part_l();
     tp.tgt = c.tgt();
@@ -608,8 +619,14 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
 }
 
 // Top-k pass: the forward with a per-row best-k list, then the merge.
+// Top-k candidates: per (vocabulary sub-range, row) the best kTopkMax; the
+// top-k launch reports two sub-ranges per range (two epilogue warps per row).
+constexpr int kTopkSubranges = 2 * kTopkSplit;
+static_assert(kTopkSubranges <= kMaxSplit, "the sub-ranges' (max, sum) pairs fit the split partials");
+
 size_t topk_cand_bytes(const flce_problem_t& p) {
-  return align_up(static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * (sizeof(float) + sizeof(int32_t)));
+  return align_up(static_cast<size_t>(kTopkSubranges) * static_cast<size_t>(p.n) * kTopkMax *
+                  (sizeof(float) + sizeof(int32_t)));
 }
 
 size_t topk_extra_bytes(const flce_problem_t& p) {
@@ -621,7 +638,7 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   const Layout base = make_layout(p, false);
   float* cand_val = reinterpret_cast<float*>(c.ws + base.total);
   int32_t* cand_idx = reinterpret_cast<int32_t*>(
-      c.ws + base.total + static_cast<size_t>(kTopkSplit) * static_cast<size_t>(p.n) * kTopkMax * sizeof(float));
+      c.ws + base.total + static_cast<size_t>(kTopkSubranges) * static_cast<size_t>(p.n) * kTopkMax * sizeof(float));
   unsigned* thr = reinterpret_cast<unsigned*>(c.ws + base.total + topk_cand_bytes(p));
   if (cudaMemsetAsync(thr, 0, static_cast<size_t>(p.n) * sizeof(unsigned), c.stream) != cudaSuccess)
     return FLCE_ERR_CUDA;
@@ -639,7 +656,8 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   tp.status = c.status();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kTopkSplit);
+  tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kTopkSplit, tp.units_split_fast);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
@@ -655,8 +673,8 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
       cuda_status(timed(0, flops, c.stream, [&] { return launch_tc(kModeTopk, maps, tp, grid, c.stream); }));
   if (st != FLCE_OK) return st;
   return cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_topk_finalize(tp.n, tp.vsplit, k, c.part_m(), c.part_l(), cand_val, cand_idx, lse, out_val, out_idx,
-                                c.stream);
+    return launch_topk_finalize(tp.n, tc_topk_subranges() * tp.vsplit, k, c.part_m(), c.part_l(), cand_val, cand_idx,
+                                lse, out_val, out_idx, c.stream);
   }));
 }
 

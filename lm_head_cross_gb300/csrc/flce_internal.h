@@ -89,6 +89,7 @@ struct TcParams {
   int32_t* topk_idx;
   int topk_k;
   unsigned* topk_thr;   // top-k: per row the best 16th-best value any range has reached (ordered key), zeroed
+  int units_split_fast; // forward modes: 1 numbers units range fastest, 0 row tile fastest
 };
 
 struct TcMaps {
@@ -139,7 +140,8 @@ cudaError_t launch_finalize_ref(int r0, int rows, int n, int h, int v, int vp, i
 cudaError_t launch_fixup_list(const int* fix_list, const int* fix_count, int r0, int v, int vp, int vtiles,
                               LabelView lv, const float* lse, const float* mtile, void* P, int grid,
                               cudaStream_t stream);
-cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
+// nsub: the (max, sum) pairs and candidate lists per row, vocabulary sub-ranges.
+cudaError_t launch_topk_finalize(int n, int nsub, int k, const float* part_m, const float* part_l,
                                  const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
                                  int32_t* out_idx, cudaStream_t stream);
 cudaError_t launch_label_scan_view(int n, int v, LabelView lv, double* blk_loss, int* blk_valid, int* status,
@@ -152,6 +154,7 @@ cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
 
 int tc_smem_bytes();
+int tc_topk_subranges();  // vocabulary sub-ranges the top-k launch reports per range
 constexpr int kFinalizeThreads = 256;
 
 }  // namespace flce

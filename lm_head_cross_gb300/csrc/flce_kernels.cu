@@ -52,14 +52,25 @@ constexpr int kStageBytes = kAStage + kBStage;     // 32 KiB
 constexpr int kMnBlock = 64 * kBK * 2;             // one 64-wide MN block of 64 K rows: 8 KiB
 constexpr int kStagingBuf = 32 * 128;              // 32 rows x 128 B
 constexpr int kStagingPerWarp = 2 * kStagingBuf;
-constexpr int kSmemStages = kStages * kStageBytes;
-constexpr int kSmemStagingOff = kSmemStages;
-constexpr int kSmemBarOff = kSmemStagingOff + 4 * kStagingPerWarp;
-constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;  // barriers, ring, slot, flag; 1 KiB alignment slack
 constexpr uint32_t kTmemCols = 2 * kBN;
 constexpr uint16_t kPairMask = 0x3;
 
-static_assert(kSmemBytes <= 232448, "shared memory budget");
+// Per-mode shape of a CTA: epilogue warps (4, or 8 as two per TMEM lane
+// quarter, each on half of a tile's columns, reported as two vocabulary
+// sub-ranges) and ring stages.  Every mode runs 4 and the full ring: eight
+// top-k epilogue warps with five stages were 5% faster at H = 2048 and 5%
+// slower at H = 4096.
+template <int MODE>
+struct Cfg {
+  static constexpr int kEpiWarps = 4;
+  static constexpr int kThreads = 64 + 32 * kEpiWarps;
+  static constexpr int kStages = flce::kStages;
+  static constexpr int kSmemStagingOff = kStages * kStageBytes;
+  static constexpr int kSmemBarOff = kSmemStagingOff + kEpiWarps * kStagingPerWarp;
+  static constexpr int kSmemBytes = kSmemBarOff + 512 + 1024;  // barriers, ring, slot, flag; 1 KiB alignment slack
+  static_assert(kSmemBytes <= 232448, "shared memory budget");
+  static_assert(2 * kStages + 6 + 2 * 8 + 4 + kEpiWarps <= 512 / 8, "barrier area");
+};
 
 struct Tile {
   int m0, n0;   // m0: this CTA's first row (pair base + 128 * rank); n0: first column of the 256-wide tile
@@ -107,8 +118,13 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
     s.done = true;
     return;
   }
-  s.rt = s.unit % p.row_tiles;  // consecutive units: the same vocabulary range for every row tile
-  s.sp = s.unit / p.row_tiles;
+  if (p.units_split_fast) {  // consecutive units: the vocabulary ranges of one row tile
+    s.rt = s.unit / p.vsplit;
+    s.sp = s.unit % p.vsplit;
+  } else {  // consecutive units: one vocabulary range of every row tile
+    s.rt = s.unit % p.row_tiles;
+    s.sp = s.unit / p.row_tiles;
+  }
   s.vt = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
   s.ve = static_cast<int>(static_cast<int64_t>(s.sp + 1) * p.vocab_tiles / p.vsplit);
 }
@@ -274,7 +290,7 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& 
         for (int j = 0; j < kHalfN / 64; ++j)
           tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.b2_r0 + k0);
       }
-      if (++stage == kStages) {
+      if (++stage == Cfg<MODE>::kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -339,7 +355,7 @@ __device__ void run_mma(const TcParams& p, const Pair& pr, uint8_t* smem, uint64
         umma_bf16_pair(d_tmem, ad, bd, idesc, (kb | k) != 0 ? 1u : 0u);
       }
       umma_commit_pair(&empty[stage], kPairMask);  // frees this stage in both CTAs once read
-      if (++stage == kStages) {
+      if (++stage == Cfg<MODE>::kStages) {
         stage = 0;
         phase ^= 1u;
       }
@@ -510,6 +526,10 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   const int lane = threadIdx.x & 31;
   const int quarter = warp & 3;  // a warp may only touch TMEM lanes [32*(warp%4), +32)
   const int r = quarter * 32 + lane;
+  // top-k: the second set of four warps takes the upper half of each tile's
+  // columns and reports it as its own vocabulary sub-range (split 2s + 1)
+  const int ehalf = (warp - 2) >> 2;
+  constexpr int kChunkCols = kBN / 32 / (Cfg<MODE>::kEpiWarps / 4);  // 32-column chunks per warp and tile
   uint8_t* stg = staging + (warp - 2) * kStagingPerWarp;
   int sbuf = 0;
   uint64_t* my_ebar = &ebar[warp - 2];  // TMA loads into this warp's staging buffers
@@ -568,7 +588,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       if (MODE == kModeTopk && tk.shared_thr) gthr = topk_unkey(*reinterpret_cast<volatile unsigned*>(tk.shared_thr));
       if (MODE == kModeForward || MODE == kModeTopk) {
 #pragma unroll 1
-        for (int c = 0; c < kBN / 32; ++c) {
+        for (int c = ehalf * kChunkCols; c < (ehalf + 1) * kChunkCols; ++c) {
           const int col0 = t.n0 + c * 32;
           if (col0 >= p.v) break;  // same for the whole warp
           __syncwarp();
@@ -695,12 +715,13 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       }
       if (MODE == kModeTopk && t.last) topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkMax));
       if (t.last && row < row_end) {
-        p.part_m[static_cast<int64_t>(t.split) * p.n + row] = run_m;
-        p.part_l[static_cast<int64_t>(t.split) * p.n + row] = run_l;
+        const int osplit = (Cfg<MODE>::kEpiWarps == 8) ? 2 * t.split + ehalf : t.split;
+        p.part_m[static_cast<int64_t>(osplit) * p.n + row] = run_m;
+        p.part_l[static_cast<int64_t>(osplit) * p.n + row] = run_l;
         if (found) p.tgt[row] = z_tgt;
         if (MODE == kModeTopk) {
           const int kept = tk.count;  // at most kTopkMax (the merge does not need them sorted)
-          const int64_t base = (static_cast<int64_t>(t.split) * p.n + row) * kTopkMax;
+          const int64_t base = (static_cast<int64_t>(osplit) * p.n + row) * kTopkMax;
           for (int i = 0; i < kTopkMax; ++i) {
             p.topk_val[base + i] = i < kept ? tk.val[topk_slot(i, lane)] : -INFINITY;
             p.topk_idx[base + i] = i < kept ? tk.idx[topk_slot(i, lane)] : -1;
@@ -838,20 +859,21 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
 // ----------------------------------------------------------------------------- the kernel
 
 template <int MODE>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
   griddep_begin();
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kSmemBarOff);
+  constexpr int kSt = Cfg<MODE>::kStages;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg<MODE>::kSmemBarOff);
   uint64_t* full = bars;
-  uint64_t* empty = bars + kStages;
-  uint64_t* tfull = bars + 2 * kStages;
-  uint64_t* tempty = bars + 2 * kStages + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 4);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kStages + 5);
+  uint64_t* empty = bars + kSt;
+  uint64_t* tfull = bars + 2 * kSt;
+  uint64_t* tempty = bars + 2 * kSt + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kSt + 4);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * kSt + 5);
   TileRing ring;
-  ring.full = bars + 2 * kStages + 6;
+  ring.full = bars + 2 * kSt + 6;
   ring.empty = ring.full + kRing;
   ring.slot = reinterpret_cast<volatile int*>(ring.empty + kRing);
   uint64_t* ebar = ring.empty + kRing + kRing / 2;  // after the 8 slot ints: one per epilogue warp
@@ -865,19 +887,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   pr.count = static_cast<int>(gridDim.x >> 1);
 
   if (warp == 0 && lane == 0) {
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kSt; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], 8);  // one arrival per epilogue warp of the pair
+      mbar_init(&tempty[i], 2 * Cfg<MODE>::kEpiWarps);  // one arrival per epilogue warp of the pair
     }
     for (int i = 0; i < kRing; ++i) {
       mbar_init(&ring.full[i], 1);
       mbar_init(&ring.empty[i], kRingReaders);
     }
-    for (int i = 0; i < 4; ++i) mbar_init(&ebar[i], 1);
+    for (int i = 0; i < Cfg<MODE>::kEpiWarps; ++i) mbar_init(&ebar[i], 1);
     *abort_flag = 0;
     mbar_fence_init();
     fence_proxy_async_smem();
@@ -910,7 +932,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     if (lane == 0 && pr.rank == 0) run_mma<MODE>(p, pr, smem, full, empty, tfull, tempty, tmem_base, ring, abort_flag);
   } else {
-    run_epilogue<MODE>(maps, p, pr, smem + kSmemStagingOff, tfull, tempty, tmem_base, ring, ebar, abort_flag);
+    run_epilogue<MODE>(maps, p, pr, smem + Cfg<MODE>::kSmemStagingOff, tfull, tempty, tmem_base, ring, ebar,
+                       abort_flag);
   }
 
   tc_fence_before_sync();
@@ -1427,56 +1450,76 @@ __global__ void __launch_bounds__(kFinalizeThreads) reduce_final_kernel(int nblk
   }
 }
 
-// Top-k pass: merge the per-split candidates of each row into its best k
-// (logit, id), high to low, and its log-sum-exp.
-__global__ void __launch_bounds__(128) topk_finalize_kernel(int n, int vsplit, int k, const float* __restrict__ part_m,
+// Top-k pass: merge the per-sub-range candidates of each row into its best k
+// (logit, id), high to low, and its log-sum-exp.  One warp per row: lane s
+// merges sub-range s's (max, sum) pair; the candidates are spread over the
+// lanes (coalesced loads) and the best k taken by k rounds of a warp-wide
+// argmax (ties: the lower id first).
+__global__ void __launch_bounds__(256) topk_finalize_kernel(int n, int nsub, int k, const float* __restrict__ part_m,
                                                             const float* __restrict__ part_l,
                                                             const float* __restrict__ cand_val,
                                                             const int32_t* __restrict__ cand_idx,
                                                             float* __restrict__ lse_out, float* __restrict__ out_val,
                                                             int32_t* __restrict__ out_idx) {
   griddep_begin();
-  const int row = blockIdx.x * blockDim.x + threadIdx.x;
-  if (row >= n) return;
-  float m = -INFINITY;
-  for (int s = 0; s < vsplit; ++s) m = fmaxf(m, part_m[static_cast<int64_t>(s) * n + row]);
-  float l = 0.f;
-  for (int s = 0; s < vsplit; ++s)
-    l += part_l[static_cast<int64_t>(s) * n + row] * exp2f(part_m[static_cast<int64_t>(s) * n + row] - m);
-  lse_out[row] = (m + log2f(l)) * kLn2;
-  float bv[kTopkMax];
-  int bi[kTopkMax];
+  const int row = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  if (row >= n) return;  // whole warps
+  const float pm = lane < nsub ? part_m[static_cast<int64_t>(lane) * n + row] : -INFINITY;
+  const float pl = lane < nsub ? part_l[static_cast<int64_t>(lane) * n + row] : 0.f;
+  constexpr int kPer = kMaxSplit * kTopkMax / 32;  // candidates per lane at most
+  const int total = nsub * kTopkMax;
+  float cv[kPer];
+  int ci[kPer];
 #pragma unroll
-  for (int i = 0; i < kTopkMax; ++i) {
-    bv[i] = -INFINITY;
-    bi[i] = -1;
+  for (int q = 0; q < kPer; ++q) {
+    const int c = lane + 32 * q;
+    const bool ok = c < total;
+    const int64_t at = (static_cast<int64_t>(c / kTopkMax) * n + row) * kTopkMax + c % kTopkMax;
+    cv[q] = ok ? cand_val[at] : -INFINITY;
+    ci[q] = ok ? cand_idx[at] : -1;
   }
-  for (int s = 0; s < vsplit; ++s) {
-    const int64_t base = (static_cast<int64_t>(s) * n + row) * kTopkMax;
-    for (int c = 0; c < kTopkMax; ++c) {
-      float x = cand_val[base + c];
-      int xi = cand_idx[base + c];
-      if (!(x > bv[kTopkMax - 1])) continue;
+  float m = pm;
 #pragma unroll
-      for (int i = 0; i < kTopkMax; ++i) {
-        // ties keep the lower vocabulary id first
-        if (x > bv[i] || (x == bv[i] && xi >= 0 && (bi[i] < 0 || xi < bi[i]))) {
-          const float tv = bv[i];
-          const int ti = bi[i];
-          bv[i] = x;
-          bi[i] = xi;
-          x = tv;
-          xi = ti;
-        }
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  float l = lane < nsub ? pl * exp2f(pm - m) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+  if (lane == 0) lse_out[row] = (m + log2f(l)) * kLn2;
+  for (int r = 0; r < k; ++r) {
+    float bv = -INFINITY;
+    int bi = -1, bq = -1;
+#pragma unroll
+    for (int q = 0; q < kPer; ++q)
+      if (topk_better(cv[q], ci[q], bv, bi)) {
+        bv = cv[q];
+        bi = ci[q];
+        bq = q;
+      }
+    float wv = bv;
+    int wi = bi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, wv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, wi, o);
+      if (topk_better(ov, oi, wv, wi)) {
+        wv = ov;
+        wi = oi;
       }
     }
-  }
+    if (bq >= 0 && wi >= 0 && bi == wi) {  // ids are unique within a row: one lane holds the winner
 #pragma unroll
-  for (int i = 0; i < kTopkMax; ++i)
-    if (i < k) {
-      out_val[static_cast<int64_t>(row) * k + i] = bv[i];
-      out_idx[static_cast<int64_t>(row) * k + i] = bi[i];
+      for (int q = 0; q < kPer; ++q)
+        if (q == bq) {
+          cv[q] = -INFINITY;
+          ci[q] = -1;
+        }
     }
+    if (lane == 0) {
+      out_val[static_cast<int64_t>(row) * k + r] = wv;
+      out_idx[static_cast<int64_t>(row) * k + r] = wi;
+    }
+  }
 }
 
 __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t count8) {
@@ -1528,7 +1571,8 @@ __global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
 
 }  // namespace
 
-int tc_smem_bytes() { return kSmemBytes; }
+int tc_smem_bytes() { return Cfg<kModeForward>::kSmemBytes; }
+int tc_topk_subranges() { return Cfg<kModeTopk>::kEpiWarps / 4; }
 
 // Every launch carries the programmatic-stream-serialization attribute (see
 // griddep_begin): a kernel may be scheduled while its predecessor drains.
@@ -1555,11 +1599,11 @@ static cudaError_t launch_mode(const TcMaps& maps, const TcParams& p, int grid, 
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
-    e = cudaFuncSetAttribute(tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    e = cudaFuncSetAttribute(tc_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<MODE>::kSmemBytes);
     if (e != cudaSuccess) return e;
     configured_device = dev;
   }
-  return launch_k(tc_kernel<MODE>, dim3(grid), dim3(kThreads), kSmemBytes, stream, maps, p);
+  return launch_k(tc_kernel<MODE>, dim3(grid), dim3(Cfg<MODE>::kThreads), Cfg<MODE>::kSmemBytes, stream, maps, p);
 }
 
 cudaError_t launch_tc(int mode, const TcMaps& maps, const TcParams& p, int grid, cudaStream_t stream) {
@@ -1636,11 +1680,11 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
                   static_cast<__nv_bfloat16*>(dst), count8);
 }
 
-cudaError_t launch_topk_finalize(int n, int vsplit, int k, const float* part_m, const float* part_l,
+cudaError_t launch_topk_finalize(int n, int nsub, int k, const float* part_m, const float* part_l,
                                  const float* cand_val, const int32_t* cand_idx, float* lse, float* out_val,
                                  int32_t* out_idx, cudaStream_t stream) {
-  return launch_k(topk_finalize_kernel, dim3((n + 127) / 128), dim3(128), 0, stream,
-                  n, vsplit, k, part_m, part_l, cand_val, cand_idx, lse, out_val, out_idx);
+  return launch_k(topk_finalize_kernel, dim3((n + 7) / 8), dim3(256), 0, stream,
+                  n, nsub, k, part_m, part_l, cand_val, cand_idx, lse, out_val, out_idx);
 }
 
 cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream) {
