@@ -390,19 +390,25 @@ def run_flce(args, rank, world, local_rank):
     value = job_tflops(world, flops, args.steps, total_ms)
 
     # end to end through the public C-ABI call on host memory (flce_fwd_bwd_host): every step
-    # copies its inputs in and its results out; two device buffers on two streams let one
-    # step's copies overlap the other step's kernels
+    # copies its inputs in and its results out; the copies run on their own streams and two
+    # device buffers alternate, so one step's copies overlap the neighbouring steps' kernels
+    # while the kernels stay in order on one stream
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
     Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True); Wh.copy_(W)
     yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True); yh.copy_(y)
     hb = flce.host_buffer_bytes(n, h, v, problem.ignore_index, problem.reduction)
+    comp, cin, cout = (torch.cuda.Stream(device=dev) for _ in range(3))
     slots = [(tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out),
-              torch.empty(hb, dtype=torch.uint8, device=dev), torch.cuda.Stream(device=dev)) for _ in range(2)]
+              torch.empty(hb, dtype=torch.uint8, device=dev), torch.cuda.Event()) for _ in range(2)]
 
     def e2e_run(steps):
         for i in range(steps):
-            outs, buf, st = slots[i % 2]
-            flce.fwd_bwd_host(Xh, Wh, yh, outs, buf, problem.ignore_index, problem.reduction, stream=st)
+            outs, buf, done = slots[i % 2]
+            if i >= 2:
+                cin.wait_event(done)  # the previous call on this buffer has copied its results out
+            flce.fwd_bwd_host(Xh, Wh, yh, outs, buf, problem.ignore_index, problem.reduction, stream=comp,
+                              in_stream=cin, out_stream=cout)
+            done.record(cout)
 
     e2e_run(2)
     torch.cuda.synchronize()
@@ -410,13 +416,13 @@ def run_flce(args, rank, world, local_rank):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for _, _, st in slots:
+    for st in (comp, cin, cout):
         st.wait_event(e0)
     e2e_run(args.e2e_steps)
-    for _, _, st in slots:
-        done = torch.cuda.Event()
-        done.record(st)
-        stream.wait_event(done)
+    for st in (comp, cin, cout):
+        fin = torch.cuda.Event()
+        fin.record(st)
+        stream.wait_event(fin)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
@@ -479,8 +485,8 @@ def run_flce(args, rank, world, local_rank):
         "e2e": {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "note": "flce_fwd_bwd_host through the C-ABI: pinned host X, W, labels copied in and loss, lse, "
-                        "dX, dW copied out every step; two device buffers on two streams overlap one step's "
-                        "copies with the other's kernels"},
+                        "dX, dW copied out every step, on their own streams; two device buffers alternate so "
+                        "copies overlap the neighbouring steps' kernels"},
     }
     if naive is not None:
         line["torch_naive"] = naive

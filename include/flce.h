@@ -132,22 +132,26 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
  * whose batch lives in host memory).  Reads X, W, labels from host memory and
  * writes loss, lse, dX, dW to host memory, with the shapes and layouts of
  * flce_fwd_bwd; page-locked host memory keeps the copies asynchronous.
- * Enqueues on `stream` and returns without waiting: one cudaMemcpyAsync per
- * input to the device, the pass of flce_fwd_bwd, one cudaMemcpyAsync per
- * result back to the host.
+ * Returns without waiting, having enqueued: one cudaMemcpyAsync per input to
+ * the device on `in_stream`, the pass of flce_fwd_bwd on `stream` (after the
+ * inputs), one cudaMemcpyAsync per result back to the host on `out_stream`
+ * (after the pass).  Pass `stream` for all three to keep everything on one
+ * stream; with separate copy streams, consecutive calls on two `dev` buffers
+ * overlap one call's copies with the other's kernels while the kernels stay
+ * in order on `stream`.
  *   - dev: a device buffer of at least flce_host_buffer_bytes(p) bytes,
  *     256-byte aligned, owned by the caller: the workspace of flce_fwd_bwd at
  *     its start (so flce_read_device_status(dev, stream) reads the call's device
  *     status), then the device copies of the inputs and results.
- *   - The host buffers and `dev` must not be touched until the stream has
- *     passed the call.  Two calls on two streams with two `dev` buffers overlap
- *     one call's copies with the other's kernels.
+ *   - The host buffers and `dev` must not be touched, nor `dev` passed to
+ *     another call, until `out_stream` has passed the call's result copies.
  *   - Errors: as flce_fwd_bwd; FLCE_ERR_WORKSPACE_TOO_SMALL if dev_bytes is
  *     below flce_host_buffer_bytes(p). */
 size_t flce_host_buffer_bytes(const flce_problem_t* p);
 flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const void* W,
                                 const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
-                                void* dev, size_t dev_bytes, flce_stream_t stream);
+                                void* dev, size_t dev_bytes, flce_stream_t stream,
+                                flce_stream_t in_stream, flce_stream_t out_stream);
 
 /* dX *= g and dW *= g in place (bf16, g a device fp32 scalar): turns the
  * gradients flce_fwd_bwd computed for g = 1 into those of g * loss, so an

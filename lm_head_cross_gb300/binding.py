@@ -74,7 +74,7 @@ def lib():
     L.flce_soft_fwd_bwd.restype = ctypes.c_int
     L.flce_host_buffer_bytes.argtypes = [P]
     L.flce_host_buffer_bytes.restype = sz
-    L.flce_fwd_bwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_fwd_bwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
     L.flce_fwd_bwd_host.restype = ctypes.c_int
     L.flce_scale_grads.argtypes = [P, vp, vp, vp, vp]
     L.flce_scale_grads.restype = ctypes.c_int
@@ -247,9 +247,11 @@ def host_buffer_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
     return int(lib().flce_host_buffer_bytes(ctypes.byref(p)))
 
 
-def fwd_bwd_host(x, w, labels, out, dev, ignore_index=-100, reduction="mean", stream=None, shift=0, seq_len=0):
+def fwd_bwd_host(x, w, labels, out, dev, ignore_index=-100, reduction="mean", stream=None, shift=0, seq_len=0,
+                 in_stream=None, out_stream=None):
     """flce_fwd_bwd_host: x, w, labels and out = (loss, lse, dX, dW) are CPU tensors (pinned for
-    asynchronous copies), dev a CUDA uint8 tensor of host_buffer_bytes.  Enqueued on `stream`;
+    asynchronous copies), dev a CUDA uint8 tensor of host_buffer_bytes.  Input copies on
+    `in_stream`, the pass on `stream`, result copies on `out_stream` (each defaults to `stream`);
     synchronise before reading `out`.  Device status: read_device_status(dev)."""
     torch = _torch()
     if x.is_cuda or w.is_cuda or labels.is_cuda or any(t.is_cuda for t in out):
@@ -262,9 +264,12 @@ def fwd_bwd_host(x, w, labels, out, dev, ignore_index=-100, reduction="mean", st
     v = w.shape[0]
     p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
     loss, lse, dX, dW = out
+    s = _stream_ptr(stream)
+    si = _stream_ptr(in_stream) if in_stream is not None else s
+    so = _stream_ptr(out_stream) if out_stream is not None else s
     _call("flce_fwd_bwd_host", lib().flce_fwd_bwd_host(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
                                                        loss.data_ptr(), lse.data_ptr(), dX.data_ptr(), dW.data_ptr(),
-                                                       dev.data_ptr(), dev.numel(), _stream_ptr(stream)))
+                                                       dev.data_ptr(), dev.numel(), s, si, so))
     return out
 
 

@@ -706,6 +706,26 @@ HostLayout host_layout(const flce_problem_t& p) {
   return L;
 }
 
+// Events that order flce_fwd_bwd_host's copy streams around its pass, one pair
+// per device and host thread.  Reusing them is safe: a stream wait takes the
+// event's state at the time it is enqueued.
+struct CopyEvents {
+  cudaEvent_t in_done = nullptr, pass_done = nullptr;
+};
+
+flce_status_t copy_events(CopyEvents** out) {
+  constexpr int kMaxDevices = 64;
+  static thread_local CopyEvents ev[kMaxDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return FLCE_ERR_CUDA;
+  CopyEvents& e = ev[dev];
+  if (!e.in_done && cudaEventCreateWithFlags(&e.in_done, cudaEventDisableTiming) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (!e.pass_done && cudaEventCreateWithFlags(&e.pass_done, cudaEventDisableTiming) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  *out = &e;
+  return FLCE_OK;
+}
+
 }  // namespace
 
 int chunk_width(int64_t n) { return n <= 16384 ? 8192 : 4096; }
@@ -784,7 +804,7 @@ size_t flce_host_buffer_bytes(const flce_problem_t* p) {
 
 flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
                                 float* loss, float* lse, void* dX, void* dW, void* dev, size_t dev_bytes,
-                                flce_stream_t stream) {
+                                flce_stream_t stream, flce_stream_t in_stream, flce_stream_t out_stream) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
   if (!X || !W || !labels || !loss || !lse || !dX || !dW || !dev) return FLCE_ERR_INVALID_ARGUMENT;
@@ -793,20 +813,32 @@ flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const vo
   if (dev_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   uint8_t* d = static_cast<uint8_t*>(dev);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStream_t si = reinterpret_cast<cudaStream_t>(in_stream);
+  cudaStream_t so = reinterpret_cast<cudaStream_t>(out_stream);
+  CopyEvents* ev = nullptr;
+  if (si != s || so != s) {
+    st = copy_events(&ev);
+    if (st != FLCE_OK) return st;
+  }
   const size_t n = static_cast<size_t>(p->n), h = static_cast<size_t>(p->h), v = static_cast<size_t>(p->v);
   const size_t loss_bytes = 4 * (p->reduction == FLCE_REDUCTION_NONE ? n : 1);
-  if (cudaMemcpyAsync(d + L.x, X, 2 * n * h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d + L.w, W, 2 * v * h, cudaMemcpyHostToDevice, s) != cudaSuccess ||
-      cudaMemcpyAsync(d + L.labels, labels, 4 * n, cudaMemcpyHostToDevice, s) != cudaSuccess)
+  if (cudaMemcpyAsync(d + L.x, X, 2 * n * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.w, W, 2 * v * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
+      cudaMemcpyAsync(d + L.labels, labels, 4 * n, cudaMemcpyHostToDevice, si) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (si != s && (cudaEventRecord(ev->in_done, si) != cudaSuccess || cudaStreamWaitEvent(s, ev->in_done, 0) != cudaSuccess))
     return FLCE_ERR_CUDA;
   st = flce_fwd_bwd(p, d + L.x, d + L.w, reinterpret_cast<const int32_t*>(d + L.labels),
                     reinterpret_cast<float*>(d + L.loss), reinterpret_cast<float*>(d + L.lse), d + L.dx, d + L.dw,
                     d + L.ws, L.x - L.ws, stream);
   if (st != FLCE_OK) return st;
-  if (cudaMemcpyAsync(loss, d + L.loss, loss_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(lse, d + L.lse, 4 * n, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(dX, d + L.dx, 2 * n * h, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
-      cudaMemcpyAsync(dW, d + L.dw, 2 * v * h, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+  if (so != s &&
+      (cudaEventRecord(ev->pass_done, s) != cudaSuccess || cudaStreamWaitEvent(so, ev->pass_done, 0) != cudaSuccess))
+    return FLCE_ERR_CUDA;
+  if (cudaMemcpyAsync(loss, d + L.loss, loss_bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      cudaMemcpyAsync(lse, d + L.lse, 4 * n, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      cudaMemcpyAsync(dX, d + L.dx, 2 * n * h, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      cudaMemcpyAsync(dW, d + L.dw, 2 * v * h, cudaMemcpyDeviceToHost, so) != cudaSuccess)
     return FLCE_ERR_CUDA;
   return FLCE_OK;
 }

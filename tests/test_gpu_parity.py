@@ -322,3 +322,37 @@ def test_profile_mask_times_only_the_selected_kinds():
     assert only["forward"][0] == only["small"][0] == 0
     assert every["forward"][0] > 0 and every["small"][0] > 0
     assert every["dxdw"][2] == pytest.approx(4.0 * p.n * p.h * p.v)   # the credited flops of the contraction
+
+
+def test_fwd_bwd_host_on_copy_streams_pipelined():
+    """Four pipelined calls on two device buffers with the copies on their own
+    streams give every step the device call's results exactly."""
+    p = synth.make_problem(520, 128, 2100, seed=49, labels="zipf", ignore_frac=0.05, w_std=0.05)
+    a = run(p)
+    X, W, y = to_device(p)
+    xh, wh, yh = X.cpu().pin_memory(), W.cpu().pin_memory(), y.cpu().pin_memory()
+    hb = flce.host_buffer_bytes(p.n, p.h, p.v)
+    comp, cin, cout = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()
+    slots = []
+    for _ in range(2):
+        outs = (torch.empty(1, dtype=torch.float32).pin_memory(), torch.empty(p.n, dtype=torch.float32).pin_memory(),
+                torch.empty(xh.shape, dtype=torch.bfloat16).pin_memory(),
+                torch.empty(wh.shape, dtype=torch.bfloat16).pin_memory())
+        slots.append((outs, torch.empty(hb, dtype=torch.uint8, device="cuda"), torch.cuda.Event()))
+    results = []
+    for i in range(4):
+        outs, buf, done = slots[i % 2]
+        if i >= 2:
+            cin.wait_event(done)
+            cout.synchronize()
+            results.append(tuple(t.clone() for t in outs))
+        flce.fwd_bwd_host(xh, wh, yh, outs, buf, p.ignore_index, p.reduction, stream=comp, in_stream=cin,
+                          out_stream=cout)
+        done.record(cout)
+    torch.cuda.synchronize()
+    results += [tuple(t.clone() for t in slots[i % 2][0]) for i in (2, 3)]
+    for loss, lse, dx, dw in results:
+        assert float(loss.item()) == a["loss"]
+        assert np.array_equal(lse.numpy(), a["lse"])
+        assert np.array_equal(dx.float().numpy(), a["dX"])
+        assert np.array_equal(dw.float().numpy(), a["dW"])
