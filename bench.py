@@ -5,10 +5,10 @@ Metric: credited TFLOP/s counting 6*N*H*V per step (2NHV for the logits, 2NHV
 each for dX and dW), with the extra device memory the op needs beside it.
 A step is one flce_fwd_bwd over one synthetic batch (loss, lse, dX, dW).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config 2] [--impl flce|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload n8192_h2048_v32000] [--impl flce|reference]
 
 Default workload: N = 4 x 2048 = 8192 tokens, H = 2048, V = 32000, labels
-Zipf(1.1) with 5% ignore_index, mean reduction (synth.CONFIGS[2]).
+Zipf(1.1) with 5% ignore_index, mean reduction.
 Under torchrun each rank runs its own batch of that shape on its own GPU
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
 
@@ -42,7 +42,7 @@ def parse_args():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--config", type=int, default=2)
+    ap.add_argument("--workload", default="n8192_h2048_v32000", help="one of synth.WORKLOADS")
     ap.add_argument("--impl", choices=["flce", "reference"], default="flce")
     ap.add_argument("--e2e-steps", type=int, default=30)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
@@ -69,11 +69,11 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
-def workload_config(cfg, problem_kw, l2_note, world):
+def workload_config(name, problem_kw, l2_note, world):
     import synth
-    c = synth.CONFIGS[cfg]
+    c = synth.WORKLOADS[name]
     return {
-        "workload": f"config {cfg}: {c['name']}",
+        "workload": f"{name}: {c['name']}",
         "n_tokens_per_rank": c["n"], "hidden": c["h"], "vocab": c["v"],
         "labels": c["labels"] + ("(s=1.1)" if c["labels"] == "zipf" else ""),
         "ignore_frac": c["ignore_frac"], "reduction": c["reduction"],
@@ -198,7 +198,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return 0
     import synth
-    problem = synth.config_problem(args.config)
+    problem = synth.workload_problem(args.workload)
     total_steps = args.steps + args.warmup
     per_step_s = max(0.5, min(10.0, 150.0 / max(1, total_steps)))
     rows = calibrate_rows(problem, per_step_s, problem.n)
@@ -211,7 +211,7 @@ def run_reference(args, rank, world):
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args.config, None, "n/a (CPU)", world),
+        "config": workload_config(args.workload, None, "n/a (CPU)", world),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"each step: fp64 numpy oracle (loss, lse, dX, dW) on the first {rows} of "
                                    f"{problem.n} rows with the full W"},
@@ -271,7 +271,7 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- the CUDA arm
 
-def traffic_record(kind, cfg):
+def traffic_record(kind, workload):
     """DRAM bytes per launch of `kind` from a committed ncu capture, if it was taken
     on the kernel source as it is now (else None)."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
@@ -283,7 +283,7 @@ def traffic_record(kind, cfg):
     src = os.path.join(ROOT, "lm_head_cross_gb300", "csrc", "flce_kernels.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for r in recs:
-        if r.get("kind") == kind and r.get("config") == cfg and r.get("kernel_sha") == sha:
+        if r.get("kind") == kind and r.get("workload") == workload and r.get("kernel_sha") == sha:
             return float(r["bytes_per_launch"])
     return None
 
@@ -301,7 +301,7 @@ def run_flce(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    c = dict(synth.CONFIGS[args.config])
+    c = dict(synth.WORKLOADS[args.workload])
     c["seed"] = rank_seed(c["seed"], rank)
     problem = synth.make_problem(**c)
     n, h, v = problem.n, problem.h, problem.v
@@ -461,7 +461,7 @@ def run_flce(args, rank, world, local_rank):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(args.config, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
+        "config": workload_config(args.workload, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
                                                      "outside the per-step events)", world),
         "frac_of_peak": value / world / peak_burst, "peak_src": f"{peak_src} bf16_tflops (burst)",
         "executed_tflops": world * per_step["flops"] * args.steps / (total_ms / 1e3) / 1e12,
@@ -476,7 +476,7 @@ def run_flce(args, rank, world, local_rank):
                      "peak_note": f"{peak_src} {peak_kind} ({'power-capped' if capped else 'full clock'} during the "
                                   f"timed region); of burst {peak_burst}: {achieved / peak_burst:.3f}, of sustained "
                                   f"{peak_sust}: {achieved / peak_sust:.3f}",
-                     "traffic": traffic_record(dom, args.config)},
+                     "traffic": traffic_record(dom, args.workload)},
         "kernels": kinds,
         "kernels_note": "separate untimed pass with every launch bracketed by events (which serialises the "
                         "launches); the roofline kernel is timed inside the timed region",
@@ -546,7 +546,7 @@ def run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, strea
         "metric": names[args.op], "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": total_ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": dict(workload_config(args.config, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
+        "config": dict(workload_config(args.workload, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write)",
                                        world), op=args.op, k=args.k, reduction=args.reduction, shift=args.shift),
         "frac_of_peak": value / world / float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"])),
         "peak_src": peak_src,

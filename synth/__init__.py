@@ -120,26 +120,31 @@ def make_problem(n: int, h: int, v: int, *, seed: int, x_std: float = 1.0, w_std
                    name=name, outlier_ids=outlier_ids)
 
 
-# The five workloads: long-sequence / large-vocabulary LM-head shapes.
-CONFIGS = {
-    1: dict(n=256, h=128, v=1024, seed=0, x_std=1.0, w_std=0.02, labels="uniform",
+# The five workloads: long-sequence / large-vocabulary LM-head shapes, keyed by
+# their sizes.
+WORKLOADS = {
+    "n256_h128_v1024": dict(n=256, h=128, v=1024, seed=0, x_std=1.0, w_std=0.02, labels="uniform",
             ignore_frac=0.10, reduction="mean", name="tiny N=256 H=128 V=1024"),
-    2: dict(n=8192, h=2048, v=32000, seed=1, x_std=1.0, w_std=0.02, labels="zipf",
+    "n8192_h2048_v32000": dict(n=8192, h=2048, v=32000, seed=1, x_std=1.0, w_std=0.02, labels="zipf",
             ignore_frac=0.05, reduction="mean", name="N=4x2048 H=2048 V=32000"),
-    3: dict(n=8192, h=4096, v=128256, seed=2, x_std=4.0 / 64.0, w_std=0.02, labels="zipf",
+    "n8192_h4096_v128256": dict(n=8192, h=4096, v=128256, seed=2, x_std=4.0 / 64.0, w_std=0.02, labels="zipf",
             ignore_frac=0.02, reduction="mean", name="N=8192 H=4096 V=128256"),
-    4: dict(n=32768, h=4096, v=151936, seed=3, x_std=1.0, w_std=0.02, labels="zipf",
+    "n32768_h4096_v151936": dict(n=32768, h=4096, v=151936, seed=3, x_std=1.0, w_std=0.02, labels="zipf",
             ignore_frac=0.05, reduction="sum", outlier_rows=64, outlier_scale=10.0,
             name="N=32768 H=4096 V=151936 (64 outlier vocab rows x10, sum)"),
-    5: dict(n=131072, h=4096, v=131072, seed=4, x_std=1.0, w_std=0.02, labels="uniform",
+    "n131072_h4096_v131072": dict(n=131072, h=4096, v=131072, seed=4, x_std=1.0, w_std=0.02, labels="uniform",
             ignore_frac=0.03, reduction="mean", name="N=128K H=4096 V=128K"),
 }
 
 
-def config_problem(k: int) -> Problem:
-    return make_problem(**CONFIGS[k])
+TINY = "n256_h128_v1024"
+DEFAULT_WORKLOAD = "n8192_h2048_v32000"
 
 
-def config_shape(k: int):
-    c = CONFIGS[k]
+def workload_problem(name: str) -> Problem:
+    return make_problem(**WORKLOADS[name])
+
+
+def workload_shape(name: str):
+    c = WORKLOADS[name]
     return c["n"], c["h"], c["v"]

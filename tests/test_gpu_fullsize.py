@@ -66,10 +66,11 @@ def gpu_properties(p, X, W, dX, dW, valid):
     assert err <= 2e-2 * scale, ("X^T dX vs dW^T W", err, scale)
 
 
-@pytest.mark.parametrize("cfg", [2, 3, 4, 5])
-def test_workload_full_size(cfg):
-    p = synth.config_problem(cfg)
-    rng = np.random.default_rng(100 + cfg)
+@pytest.mark.parametrize("name", ["n8192_h2048_v32000", "n8192_h4096_v128256", "n32768_h4096_v151936",
+                                  "n131072_h4096_v131072"])
+def test_workload_full_size(name):
+    p = synth.workload_problem(name)
+    rng = np.random.default_rng(101 + synth.WORKLOADS[name]["seed"])
     X, W, y = to_device(p)
     # the recompute path (minimal workspace) must agree with the fused path
     loss_m, lse_m, dX_m, dW_m, ws = flce.fwd_bwd(X, W, y, p.ignore_index, p.reduction, minimal_workspace=True)
@@ -93,14 +94,14 @@ def test_workload_full_size(cfg):
     Xd = oracle.widen_bf16(p.X)
     Wd = oracle.widen_bf16(p.W)
     full_forward = p.n <= 32768   # the oracle's full forward: ~20 s (N=8192) to ~90 s (N=32768) on 16 cores
-    if cfg == 2:
+    if name == synth.DEFAULT_WORKLOAD:
         ref = oracle.full(Xd, Wd, p.labels, p.ignore_index, p.reduction)
         assert_loss(loss, ref["loss"])
         assert_lse(lse_g, ref["lse"])
         assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
         assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
     else:
-        rows = sample_rows(p, 256 if cfg < 5 else 192, rng)
+        rows = sample_rows(p, 256 if p.n <= 32768 else 192, rng)
         lse_r, _ = oracle.lse_and_target(Xd, Wd, p.labels, p.ignore_index, rows)
         assert_lse(lse_g[rows], lse_r)
         dx_r = oracle.backward_dx_rows(Xd, Wd, p.labels, rows, s, p.ignore_index, lse_rows=lse_r)

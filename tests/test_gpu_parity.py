@@ -42,9 +42,8 @@ PATHS = pytest.mark.parametrize("minimal", [False, True], ids=["fused", "recompu
 
 
 @PATHS
-@pytest.mark.parametrize("cfg", [1])
-def test_config_full(cfg, minimal):
-    check_full(synth.config_problem(cfg), minimal)
+def test_tiny_workload_full(minimal):
+    check_full(synth.workload_problem(synth.TINY), minimal)
 
 
 @pytest.mark.parametrize("n,h,v,red,labels", [

@@ -30,7 +30,7 @@ def _worker(rank, world, port, out):
     try:
         local_ms = [10.0, 25.0][rank]
         total = bench.max_over_ranks(local_ms, dist, "cpu")
-        c = dict(synth.CONFIGS[1])
+        c = dict(synth.WORKLOADS[synth.TINY])
         c["seed"] = bench.rank_seed(c["seed"], rank)
         p = synth.make_problem(**c)
         digest = torch.tensor([int(p.X[:4, :4].astype("int64").sum())], dtype=torch.int64)

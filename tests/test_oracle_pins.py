@@ -375,11 +375,11 @@ def test_synth_rounding_and_recipe():
     # 1 + 3*2^-8 is a tie between 1 + 2^-7 and 1 + 2^-6: goes to even (1 + 2^-6)
     np.testing.assert_array_equal(synth.bf16_bits_to_f32(bits)[:4],
                                   np.array([1.0, 1.0, 1.015625, -2.5], dtype=np.float32))
-    p = synth.config_problem(1)
+    p = synth.workload_problem(synth.TINY)
     assert p.X.shape == (256, 128) and p.W.shape == (1024, 128)
     assert int((p.labels == IGN).sum()) == 26
     assert p.labels[p.labels != IGN].min() >= 0 and p.labels.max() < 1024
-    q = synth.config_problem(1)
+    q = synth.workload_problem(synth.TINY)
     assert np.array_equal(p.X, q.X) and np.array_equal(p.W, q.W) and np.array_equal(p.labels, q.labels)
     z = synth.make_problem(4000, 8, 100, seed=5, labels="zipf", ignore_frac=0.05)
     lab = z.labels[z.labels != IGN]
@@ -391,10 +391,10 @@ def test_synth_rounding_and_recipe():
     assert set(np.argsort(norms)[-10:]) == set(o.outlier_ids.tolist())
 
 
-def test_oracle_full_on_config1_matches_torch():
+def test_oracle_full_on_tiny_workload_matches_torch():
     torch = pytest.importorskip("torch")
     import torch.nn.functional as F
-    p = synth.config_problem(1)
+    p = synth.workload_problem(synth.TINY)
     f = oracle.full_bf16(p)
     X = torch.tensor(oracle.widen_bf16(p.X), requires_grad=True)
     W = torch.tensor(oracle.widen_bf16(p.W), requires_grad=True)
