@@ -35,10 +35,14 @@
  *     vocabulary gradient and an fp32 dW accumulator) lets flce_fwd_bwd take its
  *     faster fused path.  It is the only extra device memory the library
  *     touches.  Calls that share a workspace must be ordered on one stream.
- *   - Requirements: n >= 1, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
+ *   - Requirements: n >= 0, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
  *     the tensor-memory-access engine), X / W / dX / dW 16-byte aligned,
  *     labels / lse 4-byte aligned.  Violations return an error and launch
  *     nothing.
+ *   - An empty batch (n = 0) has no valid row: the loss is 0 (mean and sum),
+ *     dW is 0, nothing else has an element, and the pointers to per-row data
+ *     (X, labels, lse, dX, per-row losses, top-k outputs, soft targets) may be
+ *     NULL.  The workspace then needs 256 bytes (the status word).
  *   - stream: a cudaStream_t (NULL = legacy default stream).  Every call is
  *     asynchronous on it.  Host-detectable errors return immediately.
  *     Errors found on the device (a label outside [0,V) that is not
@@ -62,7 +66,7 @@ typedef struct CUstream_st* flce_stream_t;
 
 typedef enum {
   FLCE_OK = 0,
-  FLCE_ERR_INVALID_ARGUMENT = 1,    /* null pointer, bad enum, n/h/v < 1 */
+  FLCE_ERR_INVALID_ARGUMENT = 1,    /* null pointer, bad enum, n < 0, h/v < 1 */
   FLCE_ERR_UNSUPPORTED_SHAPE = 2,   /* h % 8 != 0, h < 8, or sizes beyond int32 tile coordinates */
   FLCE_ERR_MISALIGNED = 3,          /* a pointer breaks the alignment rules above */
   FLCE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < flce_workspace_bytes(p) */
@@ -221,7 +225,7 @@ flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, d
  * results as flce_forward, minus ws/ws_bytes.
  *   - Scratch: one fixed array of about 4.3 MiB in the library's own device
  *     memory, held by every GPU that loads the library until the process exits.
- *   - Limit: n <= 32768 rows (FLCE_ERR_EXCEEDS_STATIC_SCRATCH above that);
+ *   - Limit: 1 <= n <= 32768 rows (FLCE_ERR_EXCEEDS_STATIC_SCRATCH above that);
  *     h and v as for the other calls.
  *   - The first call on each device looks up the array's device address (with
  *     that device current); make that first call before any stream capture.

@@ -56,6 +56,10 @@ int fused_rows(int64_t n, int64_t v) {
 
 Layout make_layout(const flce_problem_t& p, bool fused) {
   Layout L{};
+  if (p.n == 0) {  // an empty batch needs the header (status word) only
+    L.total = kAlign;
+    return L;
+  }
   const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
   L.nblk = static_cast<int>((p.n + kFinalizeThreads - 1) / kFinalizeThreads);
   L.chunk = chunk_width(p.n);
@@ -148,7 +152,7 @@ bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) %
 
 flce_status_t check_problem(const flce_problem_t* p) {
   if (!p) return FLCE_ERR_INVALID_ARGUMENT;
-  if (p->n < 1 || p->h < 1 || p->v < 1) return FLCE_ERR_INVALID_ARGUMENT;
+  if (p->n < 0 || p->h < 1 || p->v < 1) return FLCE_ERR_INVALID_ARGUMENT;
   if (p->reduction != FLCE_REDUCTION_MEAN && p->reduction != FLCE_REDUCTION_SUM &&
       p->reduction != FLCE_REDUCTION_NONE)
     return FLCE_ERR_INVALID_ARGUMENT;
@@ -266,6 +270,26 @@ struct Ctx {
 };
 
 flce_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA; }
+
+// An empty batch (n = 0) has no valid row: the loss is 0 under mean (as for
+// n_valid = 0) and under sum, dW = G^T X is 0, and no other output has an
+// element.  Clears the workspace's status word like every call.
+flce_status_t run_empty(const flce_problem_t* p, float* loss, void* dW, void* ws, size_t ws_bytes,
+                        flce_stream_t stream) {
+  if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  if (ws_bytes < kAlign) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, kAlign, s) != cudaSuccess) return FLCE_ERR_CUDA;
+  if (loss && p->reduction != FLCE_REDUCTION_NONE && cudaMemsetAsync(loss, 0, sizeof(float), s) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  if (dW && cudaMemsetAsync(dW, 0, 2 * static_cast<size_t>(p->v) * static_cast<size_t>(p->h), s) != cudaSuccess)
+    return FLCE_ERR_CUDA;
+  return FLCE_OK;
+}
+
+// Row-indexed pointers (X, labels, lse, dX, per-row losses) may be null when the batch is empty.
+bool rows_ok(const flce_problem_t* p, const void* ptr) { return ptr || (p && p->n == 0); }
 
 // ----------------------------------------------------------------------------- diagnostics: per-launch timing
 
@@ -491,10 +515,13 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
 }
 
 // Fused forward + backward over row chunks (6NHV executed, no recompute):
-// per chunk, the forward-store pass writes p~ = 2^(S - tile max) and the
-// chunk's lse; the fix-up turns p~ into G in place; one launch then computes
-// dX for the chunk's rows (K = V, bf16 out) and adds G^T X into the fp32 dW
-// accumulator (K = chunk rows).
+// per chunk, the forward-store pass writes p~ = 2^(S - ref_i) (relative to the
+// row's reference logit) and the per-range row state; the finalize turns that
+// into lse, the losses, the row factors f_i and f_i x_i, and patches each
+// row's target entry; rows whose tiles outran the reference are rewritten by
+// the list fix-up; one launch then computes dX for the chunk's rows (K = V,
+// times s f_i, bf16 out) and adds s (f x)^T p~ into the fp32 dW accumulator
+// (K = chunk rows).
 flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelView lv, float* loss, float* lse,
                         void* dX, void* dW) {
   const flce_problem_t& p = *c.p;
@@ -748,11 +775,16 @@ size_t flce_workspace_bytes_min(const flce_problem_t* p) {
 
 flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
                            float* lse, void* ws, size_t ws_bytes, flce_stream_t stream) {
-  if (!X || !W || !labels || !loss || !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!p || !W || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) ||
+      !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(labels, 4) || !aligned(lse, 4) || !aligned(loss, 4))
     return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, loss, nullptr, ws, ws_bytes, stream);
   Ctx c;
-  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
   return run_forward(c, X, W, labels, loss, lse, nullptr);
 }
@@ -760,12 +792,16 @@ flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W
 flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
                             const float* lse, const float* grad_loss, void* dX, void* dW, void* ws, size_t ws_bytes,
                             flce_stream_t stream) {
-  if (!X || !W || !labels || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!p || !W || !dW || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) || !rows_ok(p, dX))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(labels, 4) ||
       !aligned(lse, 4) || (grad_loss && !aligned(grad_loss, 4)))
     return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, nullptr, dW, ws, ws_bytes, stream);
   Ctx c;
-  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
   if (c.per_row() && !grad_loss) return FLCE_ERR_INVALID_ARGUMENT;  // reduction none needs the per-row gradient
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
@@ -784,12 +820,17 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
 
 flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
                            float* lse, void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
-  if (!X || !W || !labels || !loss || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!p || !W || !dW || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) || !rows_ok(p, dX) ||
+      !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(labels, 4) ||
       !aligned(lse, 4) || !aligned(loss, 4))
     return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
   if (c.L.rows > 0) return run_fused(c, X, W, c.labels_of(labels), loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
@@ -807,7 +848,9 @@ flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const vo
                                 flce_stream_t stream, flce_stream_t in_stream, flce_stream_t out_stream) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
-  if (!X || !W || !labels || !loss || !lse || !dX || !dW || !dev) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!W || !dW || !dev || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) || !rows_ok(p, dX) ||
+      !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(dev, kAlign)) return FLCE_ERR_MISALIGNED;
   const HostLayout L = host_layout(*p);
   if (dev_bytes < L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
@@ -822,9 +865,13 @@ flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const vo
   }
   const size_t n = static_cast<size_t>(p->n), h = static_cast<size_t>(p->h), v = static_cast<size_t>(p->v);
   const size_t loss_bytes = 4 * (p->reduction == FLCE_REDUCTION_NONE ? n : 1);
-  if (cudaMemcpyAsync(d + L.x, X, 2 * n * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
-      cudaMemcpyAsync(d + L.w, W, 2 * v * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
-      cudaMemcpyAsync(d + L.labels, labels, 4 * n, cudaMemcpyHostToDevice, si) != cudaSuccess)
+  // one copy per buffer; an empty one (n = 0) is skipped
+  auto copy = [](void* dst, const void* src, size_t bytes, cudaMemcpyKind kind, cudaStream_t cs) {
+    return bytes == 0 ? cudaSuccess : cudaMemcpyAsync(dst, src, bytes, kind, cs);
+  };
+  if (copy(d + L.x, X, 2 * n * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
+      copy(d + L.w, W, 2 * v * h, cudaMemcpyHostToDevice, si) != cudaSuccess ||
+      copy(d + L.labels, labels, 4 * n, cudaMemcpyHostToDevice, si) != cudaSuccess)
     return FLCE_ERR_CUDA;
   if (si != s && (cudaEventRecord(ev->in_done, si) != cudaSuccess || cudaStreamWaitEvent(s, ev->in_done, 0) != cudaSuccess))
     return FLCE_ERR_CUDA;
@@ -835,10 +882,10 @@ flce_status_t flce_fwd_bwd_host(const flce_problem_t* p, const void* X, const vo
   if (so != s &&
       (cudaEventRecord(ev->pass_done, s) != cudaSuccess || cudaStreamWaitEvent(so, ev->pass_done, 0) != cudaSuccess))
     return FLCE_ERR_CUDA;
-  if (cudaMemcpyAsync(loss, d + L.loss, loss_bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
-      cudaMemcpyAsync(lse, d + L.lse, 4 * n, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
-      cudaMemcpyAsync(dX, d + L.dx, 2 * n * h, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
-      cudaMemcpyAsync(dW, d + L.dw, 2 * v * h, cudaMemcpyDeviceToHost, so) != cudaSuccess)
+  if (copy(loss, d + L.loss, loss_bytes, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      copy(lse, d + L.lse, 4 * n, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      copy(dX, d + L.dx, 2 * n * h, cudaMemcpyDeviceToHost, so) != cudaSuccess ||
+      copy(dW, d + L.dw, 2 * v * h, cudaMemcpyDeviceToHost, so) != cudaSuccess)
     return FLCE_ERR_CUDA;
   return FLCE_OK;
 }
@@ -847,11 +894,13 @@ flce_status_t flce_scale_grads(const flce_problem_t* p, const float* grad_loss, 
                                flce_stream_t stream) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
-  if (!grad_loss || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!grad_loss || !rows_ok(p, dX) || !dW) return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(dX, 16) || !aligned(dW, 16) || !aligned(grad_loss, 4)) return FLCE_ERR_MISALIGNED;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  st = cuda_status(timed(3, 0.0, s, [&] { return launch_scale_bf16(dX, p->n * p->h, grad_loss, s); }));
-  if (st != FLCE_OK) return st;
+  if (p->n > 0) {
+    st = cuda_status(timed(3, 0.0, s, [&] { return launch_scale_bf16(dX, p->n * p->h, grad_loss, s); }));
+    if (st != FLCE_OK) return st;
+  }
   return cuda_status(timed(3, 0.0, s, [&] { return launch_scale_bf16(dW, p->v * p->h, grad_loss, s); }));
 }
 
@@ -881,12 +930,16 @@ size_t flce_topk_workspace_bytes(const flce_problem_t* p, int32_t k) {
 
 flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const void* W, int32_t* topk_idx,
                         float* topk_logit, float* lse, void* ws, size_t ws_bytes, flce_stream_t stream) {
-  if (!X || !W || !topk_idx || !topk_logit || !lse) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!p || !W || !rows_ok(p, X) || !rows_ok(p, topk_idx) || !rows_ok(p, topk_logit) || !rows_ok(p, lse))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (k < 1 || k > kTopkMax) return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(topk_idx, 4) || !aligned(topk_logit, 4) || !aligned(lse, 4))
     return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, nullptr, nullptr, ws, ws_bytes, stream);
   Ctx c;
-  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
   if (ws_bytes < flce_topk_workspace_bytes(p, k)) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   c.L = make_layout(*p, false);
@@ -896,14 +949,19 @@ flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const
 flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
                                 const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
                                 void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
-  if (!X || !W || !tgt_idx || !tgt_prob || !loss || !lse || !dX || !dW) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!p || !W || !dW || !rows_ok(p, X) || !rows_ok(p, tgt_idx) || !rows_ok(p, tgt_prob) || !rows_ok(p, lse) ||
+      !rows_ok(p, dX) || !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
+    return FLCE_ERR_INVALID_ARGUMENT;
   if (k < 1 || k > kTopkMax) return FLCE_ERR_INVALID_ARGUMENT;
-  if (p && p->shift) return FLCE_ERR_INVALID_ARGUMENT;  // targets are given per row
+  if (p->shift) return FLCE_ERR_INVALID_ARGUMENT;  // targets are given per row
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(tgt_idx, 4) ||
       !aligned(tgt_prob, 4) || !aligned(lse, 4) || !aligned(loss, 4))
     return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  flce_status_t st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
   if (c.L.rows == 0) return FLCE_ERR_WORKSPACE_TOO_SMALL;  // needs flce_workspace_bytes(p)
   const LabelView lv{nullptr, p->ignore_index, 0, 1, tgt_idx, tgt_prob, k};

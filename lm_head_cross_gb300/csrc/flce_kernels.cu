@@ -416,8 +416,8 @@ __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int la
 // Each epilogue thread (one row) appends (logit, id) candidates that beat its
 // row's threshold to a buffer in the warp's shared-memory staging area (entry e
 // of lane l at topk_slot(e, l)).  Whenever a lane holds more than
-// kTopkMax, the whole warp compacts that lane's buffer with one 32-wide bitonic
-// sort, keeping the best kTopkMax; the threshold becomes the smallest kept.
+// kTopkCand - 8, the whole warp ranks that lane's entries (one per lane) and
+// keeps the best kTopkMax; the threshold becomes the smallest kept.
 
 constexpr int kTopkCand = 32;
 
@@ -448,37 +448,37 @@ __device__ __forceinline__ bool topk_better(float av, int ai, float bv, int bi) 
   return av > bv || (av == bv && static_cast<unsigned>(ai) < static_cast<unsigned>(bi));
 }
 
-// Compact the buffers of every lane in `mask` (whole-warp call).
+// Compact the buffers of every lane in `mask` (whole-warp call).  Lane e holds
+// entry e of the buffer; its rank (how many entries beat it) comes from 32
+// independent shuffle rounds, and the best kTopkMax go to slots 0..15 in rank
+// order.  Entries are distinct (value, id) pairs, so the ranks of the filled
+// slots are distinct.
 __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigned mask) {
   while (mask) {
     const int L = __ffs(mask) - 1;
     mask &= mask - 1;
     const int cnt = __shfl_sync(0xffffffffu, b.count, L);
-    float v = lane < cnt ? b.val[topk_slot(lane, L)] : -INFINITY;
-    int i = lane < cnt ? b.idx[topk_slot(lane, L)] : -1;
+    const bool filled = lane < cnt;
+    const float v = filled ? b.val[topk_slot(lane, L)] : -INFINITY;
+    const int i = filled ? b.idx[topk_slot(lane, L)] : -1;
+    int rank = 0;
 #pragma unroll
-    for (int kk = 2; kk <= 32; kk <<= 1) {
-#pragma unroll
-      for (int j = kk >> 1; j > 0; j >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, v, j);
-        const int oi = __shfl_xor_sync(0xffffffffu, i, j);
-        const bool keep_better = ((lane & j) == 0) == ((lane & kk) == 0);
-        const bool other_better = topk_better(ov, oi, v, i);
-        if (keep_better ? other_better : !other_better) {
-          v = ov;
-          i = oi;
-        }
-      }
+    for (int j = 0; j < 32; ++j) {
+      const float ov = __shfl_sync(0xffffffffu, v, j);
+      const int oi = __shfl_sync(0xffffffffu, i, j);
+      rank += topk_better(ov, oi, v, i) ? 1 : 0;
     }
-    // lanes now hold the candidates high to low; keep the best kTopkMax
-    if (lane < kTopkMax) {
-      b.val[topk_slot(lane, L)] = v;
-      b.idx[topk_slot(lane, L)] = i;
+    __syncwarp();  // every entry is in registers before the slots are rewritten
+    if (filled && rank < kTopkMax) {
+      b.val[topk_slot(rank, L)] = v;
+      b.idx[topk_slot(rank, L)] = i;
     }
-    const float kth = __shfl_sync(0xffffffffu, v, kTopkMax - 1);
+    const unsigned at_k = __ballot_sync(0xffffffffu, filled && rank == kTopkMax - 1);
+    const float kth = __shfl_sync(0xffffffffu, v, at_k ? __ffs(at_k) - 1 : 0);
+    __syncwarp();
     if (lane == L) {
       b.count = min(cnt, kTopkMax);
-      if (cnt >= kTopkMax) {
+      if (cnt >= kTopkMax && at_k) {
         b.thr = kth;
         // 16 values of this row are >= kth, so any value below it, in any range, is out
         if (b.shared_thr) atomicMax(b.shared_thr, topk_key(kth));
@@ -586,6 +586,37 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         }
       }
       if (MODE == kModeTopk && tk.shared_thr) gthr = topk_unkey(*reinterpret_cast<volatile unsigned*>(tk.shared_thr));
+      if (MODE == kModeTopk && t.first) {
+        // Before a range's first tile fills the candidate buffer from nothing: each of
+        // the tile's 16 disjoint 16-column groups holds its max, so at least kTopkMax
+        // values of the row are >= the smallest of those maxima, and nothing below it
+        // can be among the row's best kTopkMax.  Raise the row's threshold to it.
+        static_assert(kChunkCols * 2 >= kTopkMax, "one warp sees kTopkMax column groups of a tile");
+        float t0 = INFINITY;
+#pragma unroll 1
+        for (int c = ehalf * kChunkCols; c < ehalf * kChunkCols + kTopkMax / 2; ++c) {
+          const int col0 = t.n0 + c * 32;
+          if (col0 >= p.v) {  // fewer than kTopkMax groups hold a value
+            t0 = -INFINITY;
+            break;
+          }
+          __syncwarp();
+          uint32_t v[32];
+          tmem_ld_32x32(tbase + c * 32, v);
+          const int nv = min(32, p.v - col0);
+          float g0 = -INFINITY, g1 = -INFINITY;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (j < nv) g0 = fmaxf(g0, __uint_as_float(v[j]));
+            if (j + 16 < nv) g1 = fmaxf(g1, __uint_as_float(v[j + 16]));
+          }
+          t0 = fminf(t0, fminf(g0, g1));
+        }
+        if (t0 > gthr) {
+          gthr = t0;
+          if (tk.shared_thr) atomicMax(tk.shared_thr, topk_key(t0));
+        }
+      }
       if (MODE == kModeForward || MODE == kModeTopk) {
 #pragma unroll 1
         for (int c = ehalf * kChunkCols; c < (ehalf + 1) * kChunkCols; ++c) {

@@ -45,7 +45,8 @@ def test_workspace_size_rules():
     assert ws(8192, 2048, 32000) - wmin(8192, 2048, 32000) <= 8192 * 32000 + 4 * 32000 * 2048 + 8192 * 125 * 4
     # invalid problems give 0
     for f in (ws, wmin):
-        assert f(0, 128, 10) == 0 and f(10, 12, 10) == 0 and f(10, 4, 10) == 0 and f(10, 128, 0) == 0
+        assert f(-1, 128, 10) == 0 and f(10, 12, 10) == 0 and f(10, 4, 10) == 0 and f(10, 128, 0) == 0
+        assert f(0, 128, 10) == 256   # an empty batch needs only the status word
     # the largest workload stays under 4 GB of extra device memory on either path
     assert ws(131072, 4096, 131072) < 4e9 and wmin(131072, 4096, 131072) < 4e9
 
@@ -69,7 +70,12 @@ def test_host_side_validation_without_gpu():
     assert _call_forward(P(256, 128, 1024, -100, 7)) == 1  # bad reduction
     assert _call_forward(P(256, 128, 1024, -100, 0, 2, 0)) == 1  # bad shift
     assert _call_forward(P(256, 128, 1024, -100, 0, 1, 100)) == 1  # n not a multiple of seq_len
-    assert _call_forward(P(0, 128, 1024, -100, 0)) == 1    # empty
+    assert _call_forward(P(-1, 128, 1024, -100, 0)) == 1   # negative row count
+    empty = P(0, 128, 1024, -100, 0)
+    assert _call_forward(empty, X=None, lab=None, lse=None, ws=None) == 1   # empty batch still needs a workspace
+    assert _call_forward(empty, X=None, lab=None, lse=None, ws=0x100010) == 3
+    assert _call_forward(empty, X=None, lab=None, lse=None, nbytes=16) == 4
+    assert _call_forward(empty, loss=None) == 1       # the scalar loss is still written
     L = flce.lib()
     assert L.flce_selftest_timeout(None, 256, 1000, None) == 1
     assert L.flce_selftest_timeout(0x100010, 256, 1000, None) == 3

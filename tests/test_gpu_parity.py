@@ -355,3 +355,53 @@ def test_fwd_bwd_host_on_copy_streams_pipelined():
         assert np.array_equal(lse.numpy(), a["lse"])
         assert np.array_equal(dx.float().numpy(), a["dX"])
         assert np.array_equal(dw.float().numpy(), a["dW"])
+
+
+@pytest.mark.parametrize("red", ["mean", "sum", "none"])
+def test_empty_batch(red):
+    """n = 0: no valid row, so the loss is 0 (mean reads as n_valid = 0), dW = 0,
+    and every per-row output is empty, on every entry point."""
+    h, v = 64, 300
+    g = torch.Generator().manual_seed(5)
+    w = (torch.randn(v, h, generator=g) * 0.05).to(torch.bfloat16).cuda()
+    x = torch.empty(0, h, dtype=torch.bfloat16, device="cuda")
+    y = torch.empty(0, dtype=torch.int32, device="cuda")
+    dW = torch.full_like(w, 3.0)
+    out = (torch.full((0 if red == "none" else 1,), 7.0, device="cuda"), torch.empty(0, device="cuda"),
+           torch.empty_like(x), dW)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(x, w, y, -100, red, out=out)
+    assert flce.read_device_status(ws) == 0
+    assert lse.numel() == 0 and dX.numel() == 0
+    assert torch.count_nonzero(dW).item() == 0
+    if red != "none":
+        assert float(loss.item()) == 0.0
+    loss_f, lse_f, ws = flce.forward(x, w, y, -100, red)
+    assert flce.read_device_status(ws) == 0 and lse_f.numel() == 0
+    if red != "none":
+        assert float(loss_f.item()) == 0.0
+    gl = torch.empty(0, device="cuda") if red == "none" else torch.ones(1, device="cuda")
+    dX_b, dW_b, ws = flce.backward(x, w, y, lse_f, gl, -100, red)
+    assert flce.read_device_status(ws) == 0 and torch.count_nonzero(dW_b).item() == 0 and dX_b.numel() == 0
+    idx, val, lse_t, ws = flce.topk(x, w, 4)
+    assert flce.read_device_status(ws) == 0 and idx.shape == (0, 4) and val.shape == (0, 4)
+    ti = torch.empty(0, 2, dtype=torch.int32, device="cuda")
+    tq = torch.empty(0, 2, dtype=torch.float32, device="cuda")
+    loss_s, _, _, dW_s, ws = flce.soft_fwd_bwd(x, w, ti, tq, red)
+    assert flce.read_device_status(ws) == 0 and torch.count_nonzero(dW_s).item() == 0
+    if red != "none":
+        assert float(loss_s.item()) == 0.0
+        xr = x.clone().requires_grad_(True)
+        wr = w.clone().requires_grad_(True)
+        l = flce.linear_cross_entropy(xr, wr, y.long(), reduction=red)
+        l.backward()
+        assert float(l.item()) == 0.0 and torch.count_nonzero(wr.grad).item() == 0
+    # host-memory entry point
+    hb = flce.host_buffer_bytes(0, h, v, -100, red)
+    dev = torch.empty(hb, dtype=torch.uint8, device="cuda")
+    outs = (torch.full((0 if red == "none" else 1,), 7.0).pin_memory(), torch.empty(0).pin_memory(),
+            torch.empty(0, h, dtype=torch.bfloat16).pin_memory(), torch.full((v, h), 3.0, dtype=torch.bfloat16).pin_memory())
+    flce.fwd_bwd_host(x.cpu(), w.cpu().pin_memory(), y.cpu(), outs, dev, -100, red)
+    torch.cuda.synchronize()
+    assert flce.read_device_status(dev) == 0 and torch.count_nonzero(outs[3]).item() == 0
+    if red != "none":
+        assert float(outs[0].item()) == 0.0
