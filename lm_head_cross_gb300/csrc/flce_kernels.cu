@@ -562,6 +562,13 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   const int row_end = p.row_end > 0 ? p.row_end : p.n;
 
   while (sched_get<MODE>(p, pr, s, t)) {
+    // top-k: the row's shared threshold, loaded before the wait so that the wait
+    // hides its latency (an older value only keeps more candidates)
+    unsigned thr_key = 0u;
+    if (MODE == kModeTopk) {
+      const int row = p.r0 + t.m0 + r;
+      if (p.topk_thr && row < row_end) thr_key = *reinterpret_cast<volatile unsigned*>(p.topk_thr + row);
+    }
     if (!mbar_wait(&tfull[acc], acc_phase, p.timeout_ns, abort_flag)) {
       record_timeout(p, pr, abort_flag);
       break;
@@ -585,7 +592,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           tk.shared_thr = (p.topk_thr && row < row_end) ? p.topk_thr + row : nullptr;
         }
       }
-      if (MODE == kModeTopk && tk.shared_thr) gthr = topk_unkey(*reinterpret_cast<volatile unsigned*>(tk.shared_thr));
+      if (MODE == kModeTopk && tk.shared_thr) gthr = topk_unkey(thr_key);
       if (MODE == kModeTopk && t.first) {
         // Before a range's first tile fills the candidate buffer from nothing: each of
         // the tile's 16 disjoint 16-column groups holds its max, so at least kTopkMax
@@ -633,17 +640,19 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             found = true;
           }
           const int nv = min(32, p.v - col0);
-          float cmax = -INFINITY;
-          if (nv == 32) {
+          if (nv < 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) cmax = fmaxf(cmax, __uint_as_float(v[j]));
-          } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
+            for (int j = 0; j < 32; ++j)
               if (j >= nv) v[j] = __float_as_uint(-INFINITY);
-              cmax = fmaxf(cmax, __uint_as_float(v[j]));
-            }
           }
+          float gmax[4];  // maxima of the chunk's four 8-column groups
+#pragma unroll
+          for (int hh = 0; hh < 4; ++hh) {
+            gmax[hh] = __uint_as_float(v[8 * hh]);
+#pragma unroll
+            for (int j = 8 * hh + 1; j < 8 * hh + 8; ++j) gmax[hh] = fmaxf(gmax[hh], __uint_as_float(v[j]));
+          }
+          const float cmax = fmaxf(fmaxf(gmax[0], gmax[1]), fmaxf(gmax[2], gmax[3]));
           const float new_m = fmaxf(run_m, cmax * kLog2e);
           float sum = 0.f;
 #pragma unroll
@@ -655,19 +664,21 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             // lane is compacted only once it has gathered more than that
             // a value must beat this range's own 16th best (ids grow along the range, so an
             // equal later value ranks after it) and be no lower than the row's shared threshold
-            // (a warp vote per value: a value that no lane keeps costs three instructions)
+            // (a group whose max no lane keeps is skipped whole)
             if (__any_sync(0xffffffffu, cmax > tk.thr && cmax >= gthr)) {
 #pragma unroll
               for (int hh = 0; hh < 4; ++hh) {
+                if (!__any_sync(0xffffffffu, gmax[hh] > tk.thr && gmax[hh] >= gthr)) continue;
 #pragma unroll
                 for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
                   const float x = __uint_as_float(v[j]);
                   const bool keep = x > tk.thr && x >= gthr;
-                  if (__any_sync(0xffffffffu, keep) && keep) {
-                    tk.val[topk_slot(tk.count, lane)] = x;
-                    tk.idx[topk_slot(tk.count, lane)] = col0 + j;
-                    ++tk.count;
+                  const int slot = topk_slot(tk.count, lane);
+                  if (keep) {  // predicated stores, no branch
+                    tk.val[slot] = x;
+                    tk.idx[slot] = col0 + j;
                   }
+                  tk.count += keep ? 1 : 0;
                 }
                 topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8));
               }
