@@ -182,22 +182,12 @@ flce_status_t device_info(Device* d) {
   return FLCE_OK;
 }
 
-// Order of a forward launch's (row tile, vocabulary range) units.  Row tile
-// fastest, the pairs of a wave share W tiles in L2 across all row tiles, which
-// pays while the X panels of all row tiles stay resident too (up to 48 MB);
-// past that, ranges fastest keeps a wave on a few row tiles' X panels.
-int units_split_fast(int row_tiles, int64_t h) {
-  return static_cast<int64_t>(row_tiles) * kPairRows * h * 2 > (int64_t{48} << 20) ? 1 : 0;
-}
-
 // Forward split count: the number of vocabulary ranges each row tile is cut
 // into.  Picks the count (4..32, at most the number of vocabulary tiles) whose
 // round-robin assignment of (row tile, range) units to `grid` pairs gives the
-// smallest largest per-pair tile count.  Units are numbered row tile fastest,
-// so the pairs of a wave work on few vocabulary ranges across all row tiles:
-// each W tile is read by many pairs at about the same time (from L2), and the
-// rows' X panels stay resident.
-int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, bool split_fast) {
+// smallest largest per-pair tile count, with units numbered as the kernels
+// take them (unit_coords: row tile fastest within groups of `group` row tiles).
+int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, int group) {
   const int hi = std::min(cap, vocab_tiles);
   const int lo = std::min(4, hi);
   int best = lo;
@@ -205,12 +195,13 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, bo
   for (int vs = lo; vs <= hi; ++vs) {
     const long long units = static_cast<long long>(row_tiles) * vs;
     const int g = static_cast<int>(std::min<long long>(grid, units));
-    // per pair b: units b, b+g, ...; unit u has split u / row_tiles (u % vs when ranges run fastest)
+    // per pair b: units b, b+g, ...
     long long worst = 0;
     for (int b = 0; b < g; ++b) {
       long long tiles = 0;
       for (long long u = b; u < units; u += g) {
-        const int sp = static_cast<int>(split_fast ? u % vs : u / row_tiles);
+        int rt = 0, sp = 0;
+        unit_coords(static_cast<int>(u), row_tiles, vs, group, &rt, &sp);
         tiles += (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
       }
       worst = std::max(worst, tiles);
@@ -223,18 +214,18 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, bo
   return best;
 }
 
-int choose_vsplit(int row_tiles, int vocab_tiles, int grid, int cap = kMaxSplit, bool split_fast = false) {
+int choose_vsplit(int row_tiles, int vocab_tiles, int grid, int cap, int group) {
   static std::mutex mu;
   static int key[5] = {-1, -1, -1, -1, -1};
   static int val = 1;
   std::lock_guard<std::mutex> lock(mu);
-  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid || key[3] != cap || key[4] != split_fast) {
-    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid, cap, split_fast);
+  if (key[0] != row_tiles || key[1] != vocab_tiles || key[2] != grid || key[3] != cap || key[4] != group) {
+    val = choose_vsplit_uncached(row_tiles, vocab_tiles, grid, cap, group);
     key[0] = row_tiles;
     key[1] = vocab_tiles;
     key[2] = grid;
     key[3] = cap;
-    key[4] = split_fast;
+    key[4] = group;
   }
   return val;
 }
@@ -415,8 +406,8 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   tp.status = c.status();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
-  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kMaxSplit, tp.units_split_fast);
+  tp.units_group = units_group_rows(tp.row_tiles, p.h);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kMaxSplit, tp.units_group);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();
@@ -571,8 +562,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.row_end = r0 + cr;
     tp.row_tiles = (cr + kPairRows - 1) / kPairRows;
     tp.vocab_tiles = vtiles;
-    tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
-    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms / 2, kMaxSplit, tp.units_split_fast);
+    tp.units_group = units_group_rows(tp.row_tiles, p.h);
+    tp.vsplit = choose_vsplit(tp.row_tiles, vtiles, c.dev.sms / 2, kMaxSplit, tp.units_group);
     tp.part_m = c.part_m();
     tp.part_l = c.part_l();
     tp.tgt = c.tgt();
@@ -683,8 +674,8 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   tp.status = c.status();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p.v + kBN - 1) / kBN);
-  tp.units_split_fast = units_split_fast(tp.row_tiles, p.h);
-  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kTopkSplit, tp.units_split_fast);
+  tp.units_group = units_group_rows(tp.row_tiles, p.h);
+  tp.vsplit = choose_vsplit(tp.row_tiles, tp.vocab_tiles, c.dev.sms / 2, kTopkSplit, tp.units_group);
   tp.part_m = c.part_m();
   tp.part_l = c.part_l();
   tp.tgt = c.tgt();

@@ -6,6 +6,12 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#if defined(__CUDACC__)
+#define FLCE_HOST_DEVICE __host__ __device__
+#else
+#define FLCE_HOST_DEVICE
+#endif
+
 namespace flce {
 
 // Tile shape of every tensor-core kernel: 128 rows (TMEM lanes) x 256 columns
@@ -89,8 +95,31 @@ struct TcParams {
   int32_t* topk_idx;
   int topk_k;
   unsigned* topk_thr;   // top-k: per row the best 16th-best value any range has reached (ordered key), zeroed
-  int units_split_fast; // forward modes: 1 numbers units range fastest, 0 row tile fastest
+  int units_group;      // forward modes: row tiles per unit group (see units_group_rows)
 };
+
+// Unit order of the forward modes: units (row tile, vocabulary range) run row
+// tile fastest within a group of this many row tiles, then range, then group.
+// A group's X panels (256 rows x H bf16 each) fit in 48 MB, so they stay in
+// L2 while the pairs of a wave share each W tile: W is read from memory about
+// once per group instead of once per row tile.
+inline int units_group_rows(int row_tiles, int64_t h) {
+  const int64_t panel = static_cast<int64_t>(kPairRows) * h * 2;
+  int64_t g = (int64_t{48} << 20) / panel;
+  if (g < 1) g = 1;
+  return static_cast<int>(g < row_tiles ? g : row_tiles);
+}
+
+// The (row tile, range) of unit u in that order.
+FLCE_HOST_DEVICE inline void unit_coords(int u, int row_tiles, int vsplit, int group, int* rt, int* sp) {
+  const int per_group = group * vsplit;
+  const int g = u / per_group;
+  const int g0 = g * group;
+  const int rows_g = row_tiles - g0 < group ? row_tiles - g0 : group;  // the last group may be short
+  const int local = u - g * per_group;
+  *rt = g0 + local % rows_g;
+  *sp = local / rows_g;
+}
 
 struct TcMaps {
   CUtensorMap a;   // forward/grad: X (K-major, box 64x128); bwd: G K-major (dX)

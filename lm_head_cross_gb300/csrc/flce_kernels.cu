@@ -118,13 +118,7 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
     s.done = true;
     return;
   }
-  if (p.units_split_fast) {  // consecutive units: the vocabulary ranges of one row tile
-    s.rt = s.unit / p.vsplit;
-    s.sp = s.unit % p.vsplit;
-  } else {  // consecutive units: one vocabulary range of every row tile
-    s.rt = s.unit % p.row_tiles;
-    s.sp = s.unit / p.row_tiles;
-  }
+  unit_coords(s.unit, p.row_tiles, p.vsplit, p.units_group, &s.rt, &s.sp);
   s.vt = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
   s.ve = static_cast<int>(static_cast<int64_t>(s.sp + 1) * p.vocab_tiles / p.vsplit);
 }

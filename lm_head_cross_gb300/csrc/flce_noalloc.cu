@@ -149,6 +149,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.row_tiles = static_cast<int>((p->n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p->v + kBN - 1) / kBN);
   tp.vsplit = std::min(kNoAllocSplit, tp.vocab_tiles);
+  tp.units_group = units_group_rows(tp.row_tiles, p->h);
   tp.part_m = part_m;
   tp.part_l = part_l;
   tp.tgt = tgt;
