@@ -530,12 +530,15 @@ def run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, strea
     torch.cuda.synchronize()
     dom = "forward" if args.op == "topk" else "dxdw"
     flce.profile_enable(True, kinds=[dom])
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
     torch.cuda.synchronize()
+    clk = clocks.stop() or {"reasons": ["no sampler"], "samples": 0}
     prof_dom = flce.profile_read()[dom]
     flce.profile_enable(False)
     prof, per_step = kernel_breakdown(flce, torch, step, flush, min(args.steps, 10))
@@ -561,6 +564,7 @@ def run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, strea
                             "tflops": prof_dom[2] / (prof_dom[1] / 1e3) / 1e12 if prof_dom[1] else None},
         "kernels": {k: {"launches": a, "ms": b, "tflop": c / 1e12} for k, (a, b, c) in prof.items()},
         "gpu_launches": per_step["launches"] * args.steps,
+        "clocks": clk,
     }), flush=True)
     return 0
 
