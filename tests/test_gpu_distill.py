@@ -105,3 +105,16 @@ def test_soft_targets_wide_logit_range_and_repeated_ids():
         rows = np.arange(n) % 3 == g
         assert_grad(got_dx[rows], ref["dX"][rows], name=f"dX rows x{[1, 16, 64][g]}")
     assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+
+
+def test_topk_across_row_tile_groups():
+    """Top-k over 28 row tiles of 256 at H = 4096 (two unit groups, the last short)."""
+    p = synth.make_problem(7000, 4096, 3000, seed=77, x_std=4.0 / 64.0)
+    X, W, _ = to_device(p)
+    idx, val, lse, ws = flce.topk(X, W, 16)
+    assert flce.read_device_status(ws) == 0
+    Xd, Wd = oracle.widen_bf16(p.X), oracle.widen_bf16(p.W)
+    ridx, rval, rlse = oracle.topk(Xd, Wd, 16)
+    assert_lse(lse.cpu().numpy(), rlse)
+    np.testing.assert_allclose(val.cpu().numpy(), rval, rtol=0, atol=2e-3)
+    assert np.mean(idx.cpu().numpy() == ridx) > 0.99

@@ -405,3 +405,20 @@ def test_empty_batch(red):
     assert flce.read_device_status(dev) == 0 and torch.count_nonzero(outs[3]).item() == 0
     if red != "none":
         assert float(outs[0].item()) == 0.0
+
+
+@PATHS
+def test_row_tile_groups_and_wide_hidden(minimal):
+    """Forward launches whose row tiles span several unit groups (H = 4096: 24 row
+    tiles of 256 per group, 28 here, the last group short), and a wide hidden size."""
+    p = synth.make_problem(7000, 4096, 1500, seed=31, labels="zipf", ignore_frac=0.05, reduction="sum",
+                           x_std=4.0 / 64.0)
+    check_full(p, minimal)
+    X, W, y = to_device(p)
+    loss, lse, ws = flce.forward(X, W, y, p.ignore_index, p.reduction)
+    assert flce.read_device_status(ws) == 0
+    f = oracle.forward(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), p.labels, p.ignore_index, p.reduction)
+    assert_loss(float(loss.item()), f["loss"])
+    assert_lse(lse.cpu().numpy(), f["lse"])
+    q = synth.make_problem(600, 8192, 3000, seed=32, labels="uniform", ignore_frac=0.1, x_std=1.0 / 16)
+    check_full(q, minimal)
