@@ -619,49 +619,56 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         }
       }
       if (MODE == kModeForward || MODE == kModeTopk) {
+        // 32 columns per TMEM load (64 measured the same for the forward and ran
+        // slower for top-k, whose candidate code then unrolls over 64 columns)
+        constexpr int kW = 32;
+        constexpr int kGroups = kChunkCols;  // groups per warp and tile
 #pragma unroll 1
-        for (int c = ehalf * kChunkCols; c < (ehalf + 1) * kChunkCols; ++c) {
-          const int col0 = t.n0 + c * 32;
+        for (int c = ehalf * kGroups; c < (ehalf + 1) * kGroups; ++c) {
+          const int col0 = t.n0 + c * kW;
           if (col0 >= p.v) break;  // same for the whole warp
           __syncwarp();
-          uint32_t v[32];
-          tmem_ld_32x32(tbase + c * 32, v);
+          uint32_t v[kW];
+          tmem_ld_32x32(tbase + c * kW, v);
           const int yi = y_fwd - col0;
-          if (static_cast<unsigned>(yi) < 32u) {
+          if (static_cast<unsigned>(yi) < static_cast<unsigned>(kW)) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kW; ++j)
               if (j == yi) z_tgt = __uint_as_float(v[j]);
             found = true;
           }
-          const int nv = min(32, p.v - col0);
-          if (nv < 32) {
+          const int nv = min(kW, p.v - col0);
+          if (nv < kW) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < kW; ++j)
               if (j >= nv) v[j] = __float_as_uint(-INFINITY);
           }
-          float gmax[4];  // maxima of the chunk's four 8-column groups
+          constexpr int kBlocks = kW / 8;
+          float gmax[kBlocks];  // maxima of the group's 8-column blocks
 #pragma unroll
-          for (int hh = 0; hh < 4; ++hh) {
+          for (int hh = 0; hh < kBlocks; ++hh) {
             gmax[hh] = __uint_as_float(v[8 * hh]);
 #pragma unroll
             for (int j = 8 * hh + 1; j < 8 * hh + 8; ++j) gmax[hh] = fmaxf(gmax[hh], __uint_as_float(v[j]));
           }
-          const float cmax = fmaxf(fmaxf(gmax[0], gmax[1]), fmaxf(gmax[2], gmax[3]));
-          const float new_m = fmaxf(run_m, cmax * kLog2e);
-          float sum = 0.f;
+          float cmax = gmax[0];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) sum += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
-          run_l = run_l * fast_exp2(run_m - new_m) + sum;
+          for (int hh = 1; hh < kBlocks; ++hh) cmax = fmaxf(cmax, gmax[hh]);
+          const float new_m = fmaxf(run_m, cmax * kLog2e);
+          float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+          for (int j = 0; j < kW; ++j) s4[j & 3] += fast_exp2(fmaf(__uint_as_float(v[j]), kLog2e, -new_m));
+          run_l = run_l * fast_exp2(run_m - new_m) + ((s4[0] + s4[1]) + (s4[2] + s4[3]));
           run_m = new_m;
           if (MODE == kModeTopk) {
-            // groups of 8: a buffer holding at most kTopkCand - 8 never overflows, and a
+            // blocks of 8: a buffer holding at most kTopkCand - 8 never overflows, and a
             // lane is compacted only once it has gathered more than that
             // a value must beat this range's own 16th best (ids grow along the range, so an
             // equal later value ranks after it) and be no lower than the row's shared threshold
-            // (a group whose max no lane keeps is skipped whole)
+            // (a block whose max no lane keeps is skipped whole)
             if (__any_sync(0xffffffffu, cmax > tk.thr && cmax >= gthr)) {
 #pragma unroll
-              for (int hh = 0; hh < 4; ++hh) {
+              for (int hh = 0; hh < kBlocks; ++hh) {
                 if (!__any_sync(0xffffffffu, gmax[hh] > tk.thr && gmax[hh] >= gthr)) continue;
 #pragma unroll
                 for (int j = 8 * hh; j < 8 * hh + 8; ++j) {
