@@ -637,8 +637,10 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
 }
 
 // Top-k pass: the forward with a per-row best-k list, then the merge.
-// Top-k candidates: per (vocabulary sub-range, row) the best kTopkMax; the
-// top-k launch reports two sub-ranges per range (two epilogue warps per row).
+// Top-k candidates: per (vocabulary sub-range, row) the best kTopkMax.  A launch
+// reports tc_topk_subranges() sub-ranges per range (one with four epilogue
+// warps; two when two warps share a row, each on half of the columns); the
+// buffer is sized for two.
 constexpr int kTopkSubranges = 2 * kTopkSplit;
 static_assert(kTopkSubranges <= kMaxSplit, "the sub-ranges' (max, sum) pairs fit the split partials");
 
