@@ -118,3 +118,25 @@ def test_topk_across_row_tile_groups():
     assert_lse(lse.cpu().numpy(), rlse)
     np.testing.assert_allclose(val.cpu().numpy(), rval, rtol=0, atol=2e-3)
     assert np.mean(idx.cpu().numpy() == ridx) > 0.99
+
+
+def test_topk_random_shapes():
+    """16 seeded random problems, k from 1 to 16, against the oracle's top-k."""
+    rng = np.random.default_rng(77)
+    for case in range(16):
+        n = int(rng.integers(1, 700))
+        h = 8 * int(rng.integers(1, 64))
+        k = int(rng.integers(1, 17))
+        v = int(rng.integers(k, 9000))
+        p = synth.make_problem(n, h, v, seed=500 + case, x_std=float(rng.choice([0.5, 1.0, 3.0])), w_std=0.05)
+        X, W, _ = to_device(p)
+        idx, val, lse, ws = flce.topk(X, W, k)
+        assert flce.read_device_status(ws) == 0, case
+        Xd, Wd = oracle.widen_bf16(p.X), oracle.widen_bf16(p.W)
+        ridx, rval, rlse = oracle.topk(Xd, Wd, k)
+        what = f"case {case}: n={n} h={h} v={v} k={k}"
+        assert_lse(lse.cpu().numpy(), rlse)
+        np.testing.assert_allclose(val.cpu().numpy(), rval, rtol=0, atol=2e-3, err_msg=what)
+        got = np.take_along_axis(Xd @ Wd.T, idx.cpu().numpy().astype(np.int64), axis=1)
+        np.testing.assert_allclose(got, val.cpu().numpy(), rtol=0, atol=2e-3, err_msg=what)
+        assert all(len(set(r)) == k for r in idx.cpu().numpy().tolist()), what

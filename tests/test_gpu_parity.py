@@ -422,3 +422,39 @@ def test_row_tile_groups_and_wide_hidden(minimal):
     assert_lse(lse.cpu().numpy(), f["lse"])
     q = synth.make_problem(600, 8192, 3000, seed=32, labels="uniform", ignore_frac=0.1, x_std=1.0 / 16)
     check_full(q, minimal)
+
+
+def test_random_shapes_and_options():
+    """48 seeded random problems (shapes, label mix, ignore fraction, reduction,
+    shift, workspace size, logit scale) against the oracle, element by element."""
+    rng = np.random.default_rng(2024)
+    for case in range(48):
+        seq = int(rng.integers(1, 5))
+        s_len = int(rng.integers(1, 200))
+        n = seq * s_len
+        h = 8 * int(rng.integers(1, 80))
+        v = int(rng.integers(1, 6000))
+        red = ["mean", "sum", "none"][case % 3]
+        shift = int(rng.integers(0, 2)) if s_len > 1 else 0
+        minimal = bool(rng.integers(0, 2))
+        p = synth.make_problem(n, h, v, seed=1000 + case, labels=["uniform", "zipf"][case % 2],
+                               ignore_frac=float(rng.choice([0.0, 0.1, 0.5])), reduction=red,
+                               x_std=float(rng.choice([0.25, 1.0, 4.0])), w_std=float(rng.choice([0.02, 0.1])))
+        X, W, y = to_device(p)
+        loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, minimal_workspace=minimal, shift=shift,
+                                             seq_len=s_len if shift else 0)
+        assert flce.read_device_status(ws) == 0, case
+        labels = oracle.shift_labels(p.labels, s_len, p.ignore_index) if shift else p.labels
+        ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), labels, p.ignore_index, red)
+        what = f"case {case}: n={n} h={h} v={v} {red} shift={shift} minimal={minimal}"
+        got_loss = loss.cpu().numpy().astype(np.float64)
+        if red == "none":
+            np.testing.assert_allclose(got_loss, ref["loss"], rtol=1e-3, atol=2e-3, err_msg=what)
+        else:
+            assert abs(float(got_loss[0]) - ref["loss"]) <= 1e-3 * max(abs(ref["loss"]), 1e-6), what
+        assert_lse(lse.cpu().numpy(), ref["lse"])
+        if np.abs(ref["dX"]).max() > 0:
+            assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX " + what)
+            assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW " + what)
+        else:
+            assert not dX.float().abs().max().item() and not dW.float().abs().max().item(), what
