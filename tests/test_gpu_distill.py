@@ -140,3 +140,34 @@ def test_topk_random_shapes():
         got = np.take_along_axis(Xd @ Wd.T, idx.cpu().numpy().astype(np.int64), axis=1)
         np.testing.assert_allclose(got, val.cpu().numpy(), rtol=0, atol=2e-3, err_msg=what)
         assert all(len(set(r)) == k for r in idx.cpu().numpy().tolist()), what
+
+
+def test_soft_targets_random_shapes():
+    """12 seeded random soft-target problems: k from 1 to 16, random ids (repeats
+    allowed), random masses (rows without mass included), every reduction."""
+    rng = np.random.default_rng(91)
+    for case in range(12):
+        n = int(rng.integers(1, 900))
+        h = 8 * int(rng.integers(1, 48))
+        v = int(rng.integers(2, 7000))
+        k = int(rng.integers(1, 17))
+        red = ["mean", "sum", "none"][case % 3]
+        idx = rng.integers(0, v, size=(n, k)).astype(np.int32)
+        q = rng.random((n, k)).astype(np.float32)
+        q /= q.sum(axis=1, keepdims=True)
+        q[rng.random(n) < 0.1] = 0.0                                # rows without targets
+        p = synth.make_problem(n, h, v, seed=900 + case, x_std=float(rng.choice([0.5, 1.0, 4.0])), w_std=0.05)
+        X, W, _ = to_device(p)
+        loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), red)
+        assert flce.read_device_status(ws) == 0, case
+        ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), red)
+        what = f"case {case}: n={n} h={h} v={v} k={k} {red}"
+        if red == "none":
+            got = loss.cpu().numpy()
+            assert np.abs(got - ref["loss"]).max() <= 2e-3 + 1e-3 * np.abs(ref["loss"]).max(), what
+        else:
+            assert abs(float(loss.item()) - ref["loss"]) <= 1e-3 * max(abs(ref["loss"]), 1e-6), what
+        assert_lse(lse.cpu().numpy(), ref["lse"])
+        if np.abs(ref["dX"]).max() > 0:
+            assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX " + what)
+            assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW " + what)
