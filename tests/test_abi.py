@@ -97,3 +97,21 @@ def test_footprint_golden():
     for b, s, v, e, want, _ in rows:
         assert logits_footprint_bytes(int(b) * int(s), int(v), int(e)) == int(want)
     assert logits_footprint_bytes(131072, 131072, 2) == 32 << 30
+
+
+def test_header_is_c_and_host_calls_link_from_c(tmp_path):
+    """include/flce.h compiles as C99, and a C program linked against libflce.so
+    runs its host-side calls (no GPU needed)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lib = flce.lib_path()
+    exe = tmp_path / "abi_host"
+    src = os.path.join(ROOT, "tests", "c", "abi_host.c")
+    r = subprocess.run([cc, "-std=c99", "-Wall", "-Werror", "-I", os.path.join(ROOT, "include"), src, "-o", str(exe),
+                        lib, "-Wl,-rpath," + os.path.dirname(lib)], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0 and r.stdout.startswith("ok"), (r.stdout, r.stderr)
