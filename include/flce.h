@@ -90,11 +90,14 @@ typedef struct {
 } flce_problem_t;
 
 /* Workspace size in bytes with which every call below takes its fastest path
- * (0 if p is invalid): the minimum size plus room for flce_fwd_bwd's fused path,
- * i.e. a chunk of R rows of the bf16 vocabulary gradient (R x V, at most 1 GiB,
- * at least two chunks once N > 256), one fp32 per (chunk row, 256-wide
- * vocabulary tile), an fp32 dW accumulator (V x H), the chunk's rows of X
- * scaled by their per-row factor (R x H bf16) and O(N) per-row words. */
+ * (0 if p is invalid): the larger of the minimum size and the layout of
+ * flce_fwd_bwd's fused path, i.e. a chunk of R rows of the bf16 vocabulary
+ * gradient (R x V, at most 1 GiB; all N rows in one chunk when N <= 4H and it
+ * fits, else at least two chunks), one fp32 per (chunk row, 256-wide
+ * vocabulary tile), with two or more chunks an fp32 dW accumulator (V x H),
+ * the chunk's rows of X scaled by their per-row factor (R x H bf16) and O(N)
+ * per-row words.  One chunk needs no accumulator, so for N <= 4H it is no
+ * larger than two chunks would be. */
 size_t flce_workspace_bytes(const flce_problem_t* p);
 
 /* Smallest workspace every call below accepts (0 if p is invalid): the device
@@ -124,8 +127,9 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
  * of the sum of the per-row losses): loss, lse, dX, dW in one call.  With
  * ws_bytes >= flce_workspace_bytes(p) it runs fused over row chunks (the logits
  * are computed once: forward ("What-Each-Parallelism-Actually-Shards" §7.4,
- * chunked CE) keeps each chunk's tile-max-scaled softmax in bf16, a fix-up turns it
- * into G once the chunk's lse is known, then dX and dW are contracted from it);
+ * chunked CE) keeps each chunk's softmax relative to each row's target logit in
+ * bf16, and once the chunk's lse is known dX and dW are contracted from it with
+ * one factor per row);
  * with less (but at least flce_workspace_bytes_min(p)) it runs flce_forward then
  * flce_backward (logits recomputed, bounded V-independent workspace). */
 flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W,

@@ -41,16 +41,21 @@ struct Layout {
   int64_t vp;                     // fused path: row pitch of the chunk buffer (V rounded up to 8)
 };
 
-// Rows per chunk of the fused path: the p~/G buffer [rows, V] stays within
-// kFusedChunkBytes, there are at least two chunks once N > 256, and rows is a
-// multiple of 256 (the finalize block size).
+// Rows per chunk of the fused path, a multiple of 256 (the finalize block
+// size); the p~/G buffer [rows, V] stays within kFusedChunkBytes.  Several
+// chunks need an fp32 dW accumulator (V x H) besides the buffer; one chunk
+// writes dW directly.  So all rows form one chunk when N <= 4H (then the
+// N x V buffer is no larger than half of it plus the accumulator, N V + 4 V H,
+// the two-chunk alternative) and it fits; otherwise there are at least two.
 constexpr size_t kFusedChunkBytes = size_t{1} << 30;
 
-int fused_rows(int64_t n, int64_t v) {
+int fused_rows(int64_t n, int64_t v, int64_t h) {
   const int64_t vp = (v + 7) / 8 * 8;
-  int64_t rows = static_cast<int64_t>(kFusedChunkBytes / (2 * static_cast<size_t>(vp))) / 256 * 256;
+  const int64_t cap = static_cast<int64_t>(kFusedChunkBytes / (2 * static_cast<size_t>(vp))) / 256 * 256;
+  const int64_t all = (n + 255) / 256 * 256;
+  if (n <= 4 * h && all <= cap) return static_cast<int>(std::max<int64_t>(256, all));
   const int64_t half = ((n + 1) / 2 + 255) / 256 * 256;
-  rows = std::min(rows, std::max<int64_t>(256, half));
+  const int64_t rows = std::min(cap, std::max<int64_t>(256, half));
   return static_cast<int>(std::max<int64_t>(256, rows));
 }
 
@@ -63,7 +68,7 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
   L.nblk = static_cast<int>((p.n + kFinalizeThreads - 1) / kFinalizeThreads);
   L.chunk = chunk_width(p.n);
-  L.rows = fused ? fused_rows(p.n, p.v) : 0;
+  L.rows = fused ? fused_rows(p.n, p.v, p.h) : 0;
   L.vp = (p.v + 7) / 8 * 8;
   const size_t vtiles = (v + kBN - 1) / kBN;
   size_t off = 0;
@@ -85,13 +90,15 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   off = align_up(off + sizeof(float) * kMaxSplit * n);
   L.tgt = off;
   off = align_up(off + sizeof(float) * n);
+  // the fused layout serves only the fused path (flce_fwd_bwd, flce_soft_fwd_bwd);
+  // every other call lays out the workspace without it
+  const bool one_chunk = fused && static_cast<int64_t>(L.rows) >= p.n;
   L.g = off;
-  size_t gbytes = 2 * n * static_cast<size_t>(L.chunk);
-  if (fused) gbytes = std::max(gbytes, 2 * static_cast<size_t>(L.rows) * static_cast<size_t>(L.vp));
+  const size_t gbytes = fused ? 2 * static_cast<size_t>(L.rows) * static_cast<size_t>(L.vp)
+                              : 2 * n * static_cast<size_t>(L.chunk);
   off = align_up(off + gbytes);
   L.dx_acc = off;
-  size_t accbytes = 4 * n * h;
-  if (fused) accbytes = std::max(accbytes, 4 * v * h);
+  const size_t accbytes = fused ? (one_chunk ? 0 : 4 * v * h) : 4 * n * h;
   off = align_up(off + accbytes);
   L.mtile = off;
   if (fused) off = align_up(off + sizeof(float) * static_cast<size_t>(L.rows) * vtiles);
@@ -105,6 +112,12 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   if (fused) off = align_up(off + 2 * static_cast<size_t>(L.rows) * h);
   L.total = off;
   return L;
+}
+
+// Workspace for every call on its fastest path: the fused layout, or the plain
+// one if that is larger (small problems).
+size_t workspace_full(const flce_problem_t& p) {
+  return std::max(make_layout(p, true).total, make_layout(p, false).total);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -370,16 +383,22 @@ cudaError_t timed(int kind, double flops, cudaStream_t stream, F&& launch) {
   return e;
 }
 
-flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes, flce_stream_t stream) {
+// `fused_call`: the call can take the fused path (flce_fwd_bwd, flce_soft_fwd_bwd),
+// which it does when the workspace holds the fused layout.
+flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes, flce_stream_t stream,
+                      bool fused_call = false) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
   if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
   c->p = p;
-  c->L = make_layout(*p, false);
-  if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   const Layout full = make_layout(*p, true);
-  if (ws_bytes >= full.total) c->L = full;  // room for the fused path
+  if (fused_call && ws_bytes >= full.total) {
+    c->L = full;  // room for the fused path
+  } else {
+    c->L = make_layout(*p, false);
+    if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  }
   c->ws = static_cast<uint8_t*>(ws);
   c->stream = reinterpret_cast<cudaStream_t>(stream);
   st = device_info(&c->dev);
@@ -537,12 +556,13 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   TcMaps bm;  // bwd: G K-major (dX A), W MN-major (dX B), dX bf16 out; G MN-major (dW A), X MN-major (dW B), dW fp32
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out, dX, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
-  CUtensorMap dw_acc_map, dw_bf16_map;
-  if (!make_map(&dw_acc_map, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32))
-    return FLCE_ERR_CUDA;
-  if (!make_map(&dw_bf16_map, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
   const uint64_t pitch = static_cast<uint64_t>(c.L.vp) * 2;
   const int nchunks = (n + c.L.rows - 1) / c.L.rows;
+  CUtensorMap dw_acc_map, dw_bf16_map;  // the fp32 accumulator exists only with several chunks
+  if (nchunks > 1 &&
+      !make_map(&dw_acc_map, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.v, p.h * 4, 32, 32))
+    return FLCE_ERR_CUDA;
+  if (!make_map(&dw_bf16_map, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
 
   for (int r0 = 0; r0 < n; r0 += c.L.rows) {
     const int cr = std::min(c.L.rows, n - r0);
@@ -706,7 +726,7 @@ struct HostLayout {
 HostLayout host_layout(const flce_problem_t& p) {
   HostLayout L{};
   const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
-  size_t off = align_up(make_layout(p, true).total);
+  size_t off = align_up(workspace_full(p));
   L.ws = 0;
   L.x = off;
   off = align_up(off + 2 * n * h);
@@ -758,7 +778,7 @@ extern "C" {
 
 size_t flce_workspace_bytes(const flce_problem_t* p) {
   if (check_problem(p) != FLCE_OK) return 0;
-  return make_layout(*p, true).total;
+  return workspace_full(*p);
 }
 
 size_t flce_workspace_bytes_min(const flce_problem_t* p) {
@@ -823,7 +843,7 @@ flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W
   if (st != FLCE_OK) return st;
   if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream, true);
   if (st != FLCE_OK) return st;
   if (c.L.rows > 0) return run_fused(c, X, W, c.labels_of(labels), loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
@@ -954,7 +974,7 @@ flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* 
   if (st != FLCE_OK) return st;
   if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  st = prepare(&c, p, ws, ws_bytes, stream);
+  st = prepare(&c, p, ws, ws_bytes, stream, true);
   if (st != FLCE_OK) return st;
   if (c.L.rows == 0) return FLCE_ERR_WORKSPACE_TOO_SMALL;  // needs flce_workspace_bytes(p)
   const LabelView lv{nullptr, p->ignore_index, 0, 1, tgt_idx, tgt_prob, k};

@@ -41,8 +41,15 @@ def test_workspace_size_rules():
     # the fused path's size is at least the minimum
     for n, h, v in ((256, 128, 1024), (8192, 2048, 32000), (32768, 4096, 151936)):
         assert ws(n, h, v) >= wmin(n, h, v)
-    # its row-chunk buffer never holds more than half of the [N, V] logits
-    assert ws(8192, 2048, 32000) - wmin(8192, 2048, 32000) <= 8192 * 32000 + 4 * 32000 * 2048 + 8192 * 125 * 4
+    # the fused path keeps one row chunk of bf16 p~ and, with several chunks, an fp32 dW
+    # accumulator; one chunk (N <= 4H) is never larger than two chunks' buffer plus it
+    n, h, v = 8192, 2048, 32000
+    one = ws(n, h, v)
+    assert 2 * n * v <= one <= 2 * n * v + 2 * n * h + 4 * n * 125 + (8 << 20)         # no accumulator
+    assert one <= n * v + 4 * v * h + 2 * n * h + 4 * n * 125 + (8 << 20)              # <= the two-chunk layout
+    two = ws(2 * n, h, v)                                                                 # N > 4H: two chunks
+    assert two >= n * v * 2 + 4 * v * h and two <= n * v * 2 + 4 * v * h + 2 * n * h + 4 * n * 125 + (16 << 20)
+    assert ws(1024, 4096, 128256) < 300e6    # one chunk: no 2.1 GB fp32 accumulator
     # invalid problems give 0
     for f in (ws, wmin):
         assert f(-1, 128, 10) == 0 and f(10, 12, 10) == 0 and f(10, 4, 10) == 0 and f(10, 128, 0) == 0
