@@ -92,12 +92,11 @@ typedef struct {
 /* Workspace size in bytes with which every call below takes its fastest path
  * (0 if p is invalid): the larger of the minimum size and the layout of
  * flce_fwd_bwd's fused path, i.e. a chunk of R rows of the bf16 vocabulary
- * gradient (R x V, at most 1 GiB; all N rows in one chunk when N <= 4H and it
- * fits, else at least two chunks), one fp32 per (chunk row, 256-wide
- * vocabulary tile), with two or more chunks an fp32 dW accumulator (V x H),
- * the chunk's rows of X scaled by their per-row factor (R x H bf16) and O(N)
- * per-row words.  One chunk needs no accumulator, so for N <= 4H it is no
- * larger than two chunks would be. */
+ * gradient (R x V), one fp32 per (chunk row, 256-wide vocabulary tile), with
+ * two or more chunks an fp32 dW accumulator (V x H), the chunk's rows of X
+ * scaled by their per-row factor (R x H bf16) and O(N) per-row words.  Several
+ * chunks have R = min(N/2, 1 GiB / 2V) rows; all N rows form one chunk (which
+ * needs no accumulator) whenever that takes no more memory. */
 size_t flce_workspace_bytes(const flce_problem_t* p);
 
 /* Smallest workspace every call below accepts (0 if p is invalid): the device

@@ -42,21 +42,22 @@ struct Layout {
 };
 
 // Rows per chunk of the fused path, a multiple of 256 (the finalize block
-// size); the p~/G buffer [rows, V] stays within kFusedChunkBytes.  Several
-// chunks need an fp32 dW accumulator (V x H) besides the buffer; one chunk
-// writes dW directly.  So all rows form one chunk when N <= 4H (then the
-// N x V buffer is no larger than half of it plus the accumulator, N V + 4 V H,
-// the two-chunk alternative) and it fits; otherwise there are at least two.
+// size).  Several chunks of R rows: R = min(half of N, the rows whose p~/G
+// buffer [R, V] fits kFusedChunkBytes), and an fp32 dW accumulator (V x H)
+// besides the buffer.  One chunk writes dW directly and needs no accumulator,
+// so all rows form one chunk whenever its N x V buffer is no larger than the
+// several-chunk buffer plus the accumulator (for R = N/2 that is N <= 4H).
 constexpr size_t kFusedChunkBytes = size_t{1} << 30;
 
 int fused_rows(int64_t n, int64_t v, int64_t h) {
   const int64_t vp = (v + 7) / 8 * 8;
-  const int64_t cap = static_cast<int64_t>(kFusedChunkBytes / (2 * static_cast<size_t>(vp))) / 256 * 256;
-  const int64_t all = (n + 255) / 256 * 256;
-  if (n <= 4 * h && all <= cap) return static_cast<int>(std::max<int64_t>(256, all));
+  const int64_t cap = std::max<int64_t>(
+      256, static_cast<int64_t>(kFusedChunkBytes / (2 * static_cast<size_t>(vp))) / 256 * 256);
   const int64_t half = ((n + 1) / 2 + 255) / 256 * 256;
   const int64_t rows = std::min(cap, std::max<int64_t>(256, half));
-  return static_cast<int>(std::max<int64_t>(256, rows));
+  const int64_t all = std::max<int64_t>(256, (n + 255) / 256 * 256);
+  if (2 * all * vp <= 2 * rows * vp + 4 * v * h) return static_cast<int>(all);
+  return static_cast<int>(rows);
 }
 
 Layout make_layout(const flce_problem_t& p, bool fused) {
