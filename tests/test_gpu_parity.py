@@ -458,3 +458,25 @@ def test_random_shapes_and_options():
             assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW " + what)
         else:
             assert not dX.float().abs().max().item() and not dW.float().abs().max().item(), what
+
+
+def test_concurrent_calls_on_two_streams():
+    """Two calls with their own workspaces on two streams at once give the same
+    bits as the same calls one after the other (no state outside the workspace)."""
+    p1 = synth.make_problem(1200, 256, 7000, seed=51, labels="zipf", ignore_frac=0.05)
+    p2 = synth.make_problem(900, 192, 5001, seed=52, labels="uniform", ignore_frac=0.1, reduction="sum")
+    a1, a2 = run(p1), run(p2)
+    X1, W1, y1 = to_device(p1)
+    X2, W2, y2 = to_device(p2)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    torch.cuda.synchronize()
+    for _ in range(3):
+        r1 = flce.fwd_bwd(X1, W1, y1, p1.ignore_index, p1.reduction, stream=s1)
+        r2 = flce.fwd_bwd(X2, W2, y2, p2.ignore_index, p2.reduction, stream=s2)
+        torch.cuda.synchronize()
+        for r, a in ((r1, a1), (r2, a2)):
+            assert flce.read_device_status(r[4]) == 0
+            assert float(r[0].item()) == a["loss"]
+            assert np.array_equal(r[1].cpu().numpy(), a["lse"])
+            assert np.array_equal(r[2].float().cpu().numpy(), a["dX"])
+            assert np.array_equal(r[3].float().cpu().numpy(), a["dW"])
