@@ -411,7 +411,7 @@ __device__ __forceinline__ void release_accumulator(uint64_t* tempty_acc, int la
 // row's threshold to a buffer in the warp's shared-memory staging area (entry e
 // of lane l at topk_slot(e, l)).  Whenever a lane holds more than
 // kTopkCand - 8, the whole warp ranks that lane's entries (one per lane) and
-// keeps the best kTopkMax; the threshold becomes the smallest kept.
+// keeps the best k; the threshold becomes the smallest kept.
 
 constexpr int kTopkCand = 32;
 
@@ -442,12 +442,12 @@ __device__ __forceinline__ bool topk_better(float av, int ai, float bv, int bi) 
   return av > bv || (av == bv && static_cast<unsigned>(ai) < static_cast<unsigned>(bi));
 }
 
-// Compact the buffers of every lane in `mask` (whole-warp call).  Lane e holds
-// entry e of the buffer; its rank (how many entries beat it) comes from 32
-// independent shuffle rounds, and the best kTopkMax go to slots 0..15 in rank
-// order.  Entries are distinct (value, id) pairs, so the ranks of the filled
-// slots are distinct.
-__device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigned mask) {
+// Compact the buffers of every lane in `mask` (whole-warp call), keeping each
+// row's best `keep` (= k, at most kTopkMax).  Lane e holds entry e of the
+// buffer; its rank (how many entries beat it) comes from 32 independent shuffle
+// rounds, and the best `keep` go to slots 0..keep-1 in rank order.  Entries are
+// distinct (value, id) pairs, so the ranks of the filled slots are distinct.
+__device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigned mask, int keep) {
   while (mask) {
     const int L = __ffs(mask) - 1;
     mask &= mask - 1;
@@ -463,18 +463,18 @@ __device__ __forceinline__ void topk_compact_lanes(TopkBuf& b, int lane, unsigne
       rank += topk_better(ov, oi, v, i) ? 1 : 0;
     }
     __syncwarp();  // every entry is in registers before the slots are rewritten
-    if (filled && rank < kTopkMax) {
+    if (filled && rank < keep) {
       b.val[topk_slot(rank, L)] = v;
       b.idx[topk_slot(rank, L)] = i;
     }
-    const unsigned at_k = __ballot_sync(0xffffffffu, filled && rank == kTopkMax - 1);
+    const unsigned at_k = __ballot_sync(0xffffffffu, filled && rank == keep - 1);
     const float kth = __shfl_sync(0xffffffffu, v, at_k ? __ffs(at_k) - 1 : 0);
     __syncwarp();
     if (lane == L) {
-      b.count = min(cnt, kTopkMax);
-      if (cnt >= kTopkMax && at_k) {
+      b.count = min(cnt, keep);
+      if (cnt >= keep && at_k) {
         b.thr = kth;
-        // 16 values of this row are >= kth, so any value below it, in any range, is out
+        // `keep` values of this row are >= kth, so any value below it, in any range, is out
         if (b.shared_thr) atomicMax(b.shared_thr, topk_key(kth));
       }
     }
@@ -681,7 +681,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
                   }
                   tk.count += keep ? 1 : 0;
                 }
-                topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8));
+                topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkCand - 8), p.topk_k);
               }
             }
           }
@@ -756,14 +756,15 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(ref - new_m);
         run_m = new_m;
       }
-      if (MODE == kModeTopk && t.last) topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > kTopkMax));
+      if (MODE == kModeTopk && t.last)
+        topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > p.topk_k), p.topk_k);
       if (t.last && row < row_end) {
         const int osplit = (Cfg<MODE>::kEpiWarps == 8) ? 2 * t.split + ehalf : t.split;
         p.part_m[static_cast<int64_t>(osplit) * p.n + row] = run_m;
         p.part_l[static_cast<int64_t>(osplit) * p.n + row] = run_l;
         if (found) p.tgt[row] = z_tgt;
         if (MODE == kModeTopk) {
-          const int kept = tk.count;  // at most kTopkMax (the merge does not need them sorted)
+          const int kept = tk.count;  // at most k (the merge does not need them sorted)
           const int64_t base = (static_cast<int64_t>(osplit) * p.n + row) * kTopkMax;
           for (int i = 0; i < kTopkMax; ++i) {
             p.topk_val[base + i] = i < kept ? tk.val[topk_slot(i, lane)] : -INFINITY;
