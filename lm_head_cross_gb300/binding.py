@@ -425,3 +425,52 @@ def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str 
     loss = _LinearCrossEntropy.get().apply(x2, w.contiguous(), lab, int(ignore_index), reduction, int(shift),
                                            seq_len)
     return loss.reshape(labels.shape) if reduction == "none" else loss
+
+
+class _SparseKL:
+    """torch.autograd.Function for the soft-target KL: the forward runs the fused
+    forward + backward (flce_soft_fwd_bwd, upstream gradient 1) and keeps dX and
+    dW; the backward multiplies them by the upstream gradient."""
+    fn = None
+
+    @classmethod
+    def get(cls):
+        if cls.fn is None:
+            torch = _torch()
+
+            class Fn(torch.autograd.Function):
+                @staticmethod
+                def forward(ctx, x2, w, tgt_idx, tgt_prob, reduction):
+                    loss, _, dX, dW, _ = soft_fwd_bwd(x2, w, tgt_idx, tgt_prob, reduction)
+                    ctx.save_for_backward(dX, dW)
+                    return loss.reshape(())
+
+                @staticmethod
+                def backward(ctx, grad):
+                    dX, dW = ctx.saved_tensors
+                    g = grad.detach().to(torch.float32).reshape(1).contiguous()
+                    scale_grads(dX, dW, g)
+                    return dX, dW, None, None, None
+
+            cls.fn = Fn
+        return cls.fn
+
+
+def sparse_kl_divergence(x, w, tgt_idx, tgt_prob, reduction: str = "mean"):
+    """KL(q || softmax(x @ w.T)) against sparse soft targets (a teacher's top-k ids
+    and probabilities per row), without materialising the logits.
+
+    x: [..., H] bf16 CUDA, w: [V, H] bf16, tgt_idx / tgt_prob: [..., k] (k <= 16)
+    integer ids and fp32 probabilities; a row whose probabilities are all 0 is
+    ignored.  reduction: 'mean' (over rows with targets) or 'sum'.  Autograd flows
+    to x and w.
+    """
+    torch = _torch()
+    if reduction not in ("mean", "sum"):
+        raise ValueError("sparse_kl_divergence takes reduction 'mean' or 'sum'")
+    h = x.shape[-1]
+    k = tgt_idx.shape[-1]
+    x2 = x.reshape(-1, h).contiguous()
+    idx = tgt_idx.reshape(-1, k).to(torch.int32).contiguous()
+    q = tgt_prob.reshape(-1, k).to(torch.float32).contiguous()
+    return _SparseKL.get().apply(x2, w.contiguous(), idx, q, reduction)

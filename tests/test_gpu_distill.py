@@ -171,3 +171,23 @@ def test_soft_targets_random_shapes():
         if np.abs(ref["dX"]).max() > 0:
             assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX " + what)
             assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW " + what)
+
+
+@pytest.mark.parametrize("red,upstream", [("mean", 1.0), ("sum", 0.5)])
+def test_sparse_kl_autograd(red, upstream):
+    """The autograd wrapper of the soft-target KL: loss and the gradients reaching
+    x and w match the oracle (times the upstream gradient)."""
+    n, h, v, k = 2 * 300, 128, 3001, 4
+    idx, q = _teacher_targets(n, h, v, k, seed=95)
+    p = synth.make_problem(n, h, v, seed=96, w_std=0.05)
+    X, W, _ = to_device(p)
+    x3 = X.reshape(2, 300, h).clone().requires_grad_(True)
+    w = W.clone().requires_grad_(True)
+    loss = flce.sparse_kl_divergence(x3, w, torch.from_numpy(idx).cuda().reshape(2, 300, k),
+                                     torch.from_numpy(q).cuda().reshape(2, 300, k), red)
+    (loss * upstream).backward()
+    ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), red,
+                           grad_output=upstream)
+    assert_loss(float(loss.item()), ref["loss"])
+    assert_grad(x3.grad.reshape(n, h).float().cpu().numpy(), ref["dX"], name="dX")
+    assert_grad(w.grad.float().cpu().numpy(), ref["dW"], name="dW")
