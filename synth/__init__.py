@@ -134,6 +134,10 @@ WORKLOADS = {
             name="N=32768 H=4096 V=151936 (64 outlier vocab rows x10, sum)"),
     "n131072_h4096_v131072": dict(n=131072, h=4096, v=131072, seed=4, x_std=1.0, w_std=0.02, labels="uniform",
             ignore_frac=0.03, reduction="mean", name="N=128K H=4096 V=128K"),
+    # not one of the five: three fused row chunks (the fp32 dW accumulator stored, added
+    # to and read back) in a few GB of device memory, small enough for a full ncu capture
+    "n24576_h2048_v65536": dict(n=24576, h=2048, v=65536, seed=5, x_std=1.0, w_std=0.02, labels="zipf",
+            ignore_frac=0.05, reduction="mean", name="N=24576 H=2048 V=65536 (3 row chunks)"),
 }
 
 
