@@ -31,9 +31,9 @@
  *     owned by the caller; the library never allocates or frees memory.
  *   - ws / ws_bytes: caller-owned device workspace, 256-byte aligned, of at
  *     least flce_workspace_bytes_min(p) bytes (grows with N and H, not with V);
- *     flce_workspace_bytes(p) bytes (also holds a bounded row chunk of the
- *     vocabulary gradient and an fp32 dW accumulator) lets flce_fwd_bwd take its
- *     faster fused path.  It is the only extra device memory the library
+ *     flce_workspace_bytes(p) bytes (also holds a row chunk of the vocabulary
+ *     gradient and, when there are several chunks, an fp32 dW accumulator) lets
+ *     flce_fwd_bwd take its faster fused path.  It is the only extra device memory the library
  *     touches.  Calls that share a workspace must be ordered on one stream.
  *   - Requirements: n >= 0, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
  *     the tensor-memory-access engine), X / W / dX / dW 16-byte aligned,
