@@ -56,6 +56,9 @@ def parse_args():
     ap.add_argument("--shift", type=int, default=0, help="1: causal next-token shift inside the kernels")
     ap.add_argument("--workspace", choices=["full", "min"], default="full",
                     help="min: flce_workspace_bytes_min, the recompute path (8NHV executed)")
+    ap.add_argument("--sustain", type=float, default=0.0,
+                    help="seconds of back-to-back calls (no L2 flush) after the timed region, reported as "
+                         "'sustained': the power-capped steady state of a long run")
     return ap.parse_args()
 
 
@@ -278,6 +281,31 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- the CUDA arm
 
+def sustained_run(step, flops, seconds, gpu_index, torch):
+    """Back-to-back steps (no L2 flush) for about `seconds` after a quarter of that
+    as warm-up into the power cap: the steady state a long run settles into."""
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(); step(); b.record(); torch.cuda.synchronize()
+    reps = max(3, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
+    for _ in range(max(1, reps // 4)):
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(gpu_index)
+    clocks.start()
+    a.record()
+    for _ in range(reps):
+        step()
+    b.record()
+    torch.cuda.synchronize()
+    clk = clocks.stop() or {}
+    ms = a.elapsed_time(b) / reps
+    tf = flops / (ms / 1e3) / 1e12
+    mhz = clk.get("sm_mhz")
+    return {"value": tf, "unit": UNIT, "ms_per_step": ms, "steps": reps, "sm_mhz": mhz,
+            "tflops_per_ghz": tf / (mhz / 1e3) if mhz else None,
+            "power_w_instant_median": clk.get("power_w_instant_median"), "reasons": clk.get("reasons")}
+
+
 def traffic_record(kind, workload):
     """DRAM bytes per launch of `kind` from a committed ncu capture, if it was taken
     on the kernel source as it is now (else None)."""
@@ -444,6 +472,7 @@ def run_flce(args, rank, world, local_rank):
     naive = None
     if rank == 0 and world == 1 and not args.no_naive:
         naive = torch_naive(X, W, y, problem, flush, stream, torch)
+    sustained = sustained_run(step, flops, args.sustain, local_rank, torch) if args.sustain > 0 else None
 
     if dist is not None:
         dist.barrier()
@@ -496,6 +525,8 @@ def run_flce(args, rank, world, local_rank):
     }
     if naive is not None:
         line["torch_naive"] = naive
+    if sustained is not None:
+        line["sustained"] = sustained
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(problem, args.cpu_seconds)
     print(json.dumps(line), flush=True)
