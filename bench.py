@@ -235,7 +235,15 @@ class ClockSampler:
     PERIOD_MS = 20
 
     def __init__(self, gpu_index):
+        # nvidia-smi numbers every GPU of the machine; CUDA may see a subset
+        # (CUDA_VISIBLE_DEVICES), so the GPU is named by its PCI bus id
         self.gpu = gpu_index
+        try:
+            import torch
+            pr = torch.cuda.get_device_properties(gpu_index)
+            self.gpu = f"{pr.pci_domain_id:08x}:{pr.pci_bus_id:02x}:{pr.pci_device_id:02x}.0"
+        except (ImportError, AttributeError, RuntimeError, AssertionError):
+            pass
         self.proc = None
         self.path = None
 
