@@ -905,7 +905,8 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
 template <int MODE>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::kThreads, 1)
     tc_kernel(const __grid_constant__ TcMaps maps, const TcParams p) {
-  griddep_begin();
+  // The prologue (barriers, TMEM, tensor-map prefetch) reads no global memory,
+  // so it runs before the wait for the previous kernel (griddep_begin below).
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   constexpr int kSt = Cfg<MODE>::kStages;
