@@ -966,8 +966,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Cfg<MODE>::kThreads,
   cluster_sync_all();  // barriers of both CTAs initialised before any cross-CTA arrival
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  griddep_begin();  // the prologue above overlaps the previous kernel's tail
-  if (p.zero_words && blockIdx.x == 0 && threadIdx.x == 0) {
+  // Wait for the previous kernel before touching memory it may write.  In the
+  // forward modes the producer and MMA threads read only X and W, which no
+  // kernel of the library writes, so they start the contraction at once and
+  // only the epilogue (which reads the row state and writes the outputs) waits.
+  if (!kUnits<MODE> || warp >= 2) griddep_wait();
+  griddep_launch();
+  if (p.zero_words && blockIdx.x == 0 && threadIdx.x == 64) {  // an epilogue thread: after the wait
     p.zero_words[0] = 0;
     p.zero_words[1] = 0;
   }
