@@ -122,3 +122,16 @@ def test_header_is_c_and_host_calls_link_from_c(tmp_path):
     assert r.returncode == 0, r.stderr
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
     assert r.returncode == 0 and r.stdout.startswith("ok"), (r.stdout, r.stderr)
+
+
+def test_workspace_sizes_on_random_shapes():
+    """For random valid shapes the fastest-path workspace is never smaller than the
+    minimum, and both are positive (the host-side layout arithmetic)."""
+    import random
+    rng = random.Random(1)
+    for _ in range(2000):
+        n = rng.choice([0, 1, 7, 255, 256, 257, rng.randint(1, 300000)])
+        h = 8 * rng.randint(1, 2048)
+        v = rng.randint(1, 300000)
+        full, mn = flce.workspace_bytes(n, h, v), flce.workspace_bytes_min(n, h, v)
+        assert 0 < mn <= full, (n, h, v, full, mn)
