@@ -79,11 +79,6 @@ def _row_blocks(n: int, v: int):
         yield np.arange(s, min(n, s + step))
 
 
-def logits(X: np.ndarray, W: np.ndarray) -> np.ndarray:
-    """``z = X W^T`` in float64 (small problems only)."""
-    return np.asarray(X, np.float64) @ np.asarray(W, np.float64).T
-
-
 def lse_and_target(X: np.ndarray, W: np.ndarray, labels: np.ndarray, ignore_index: int,
                    rows: np.ndarray | None = None):
     """Per-row ``lse`` and target logit ``z[i, y_i]`` (0 for ignored rows).
@@ -95,7 +90,7 @@ def lse_and_target(X: np.ndarray, W: np.ndarray, labels: np.ndarray, ignore_inde
     lab = np.asarray(labels, dtype=np.int64)
     rows = np.arange(X.shape[0]) if rows is None else np.asarray(rows, dtype=np.int64)
     v = W.shape[0]
-    lse = np.empty(rows.size, np.float64)
+    lse = np.full(rows.size, np.nan)       # a row no block reaches stays NaN
     tgt = np.zeros(rows.size, np.float64)
     for blk in _row_blocks(rows.size, v):
         r = rows[blk]
@@ -199,9 +194,9 @@ def topk(X, W, k: int):
     X = np.asarray(X, np.float64)
     W = np.asarray(W, np.float64)
     n = X.shape[0]
-    idx = np.empty((n, k), dtype=np.int64)
-    val = np.empty((n, k), dtype=np.float64)
-    lse = np.empty(n, dtype=np.float64)
+    idx = np.full((n, k), -1, dtype=np.int64)     # a row no block reaches stays -1 / NaN
+    val = np.full((n, k), np.nan)
+    lse = np.full(n, np.nan)
     for blk in _row_blocks(n, W.shape[0]):
         z = X[blk] @ W.T
         order = np.argsort(-z, axis=1, kind="stable")[:, :k]

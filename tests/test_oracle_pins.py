@@ -343,6 +343,68 @@ def test_topk_matches_torch():
     assert np.array_equal(oracle.topk(X, W, 1)[0][:, 0], np.argmax(X @ W.T, axis=1))
 
 
+def _multi_block_pin(orc, monkeypatch):
+    """Row blocking (the large workloads run through hundreds of blocks): with ten rows
+    per block, 103 rows make eleven blocks, the last one ragged (3 rows).  Every row's
+    lse and target logit, the loss, the top-k and a row subset must equal torch's fp64
+    logsumexp / gather / cross_entropy / topk on the whole problem."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    rng = np.random.default_rng(36)
+    n, h, v = 103, 16, 37
+    X, W, y = _rand_problem(rng, n, h, v, ignore_frac=0.2, w_std=1.0)
+    monkeypatch.setattr(orc, "_BLOCK_BYTES", 8 * v * 10)
+    z = torch.tensor(X) @ torch.tensor(W).T
+    want_lse = torch.logsumexp(z, dim=1).numpy()
+    valid = y != IGN
+    want_tgt = np.where(valid, z.numpy()[np.arange(n), np.where(valid, y, 0)], 0.0)
+    lse, tgt = orc.lse_and_target(X, W, y, IGN)
+    np.testing.assert_allclose(lse, want_lse, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(tgt, want_tgt, rtol=0, atol=1e-12)
+    rows = rng.permutation(n)[:47]
+    lse_r, tgt_r = orc.lse_and_target(X, W, y, IGN, rows)
+    np.testing.assert_allclose(lse_r, want_lse[rows], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(tgt_r, want_tgt[rows], rtol=0, atol=1e-12)
+    f = orc.forward(X, W, y, IGN, "mean")
+    ref = F.cross_entropy(z, torch.tensor(y.astype(np.int64)), ignore_index=IGN).item()
+    assert abs(f["loss"] - ref) <= 1e-12 * abs(ref)
+    idx, val, lse_k = orc.topk(X, W, 5)
+    tv, ti = torch.topk(z, 5, dim=1)
+    assert np.array_equal(idx, ti.numpy())
+    np.testing.assert_allclose(val, tv.numpy(), rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse_k, want_lse, rtol=0, atol=1e-12)
+
+
+def test_multi_block_rows_match_torch(monkeypatch):
+    assert [b.size for b in _blocks_with(monkeypatch, 103, 37, 10)] == [10] * 10 + [3]
+    _multi_block_pin(oracle, monkeypatch)
+
+
+def _blocks_with(monkeypatch, n, v, rows_per_block):
+    monkeypatch.setattr(oracle, "_BLOCK_BYTES", 8 * v * rows_per_block)
+    return list(oracle._row_blocks(n, v))
+
+
+def _drop_ragged_block(n, v):
+    step = max(1, oracle._BLOCK_BYTES // max(1, 8 * v))
+    for s in range(0, n - n % step, step):
+        yield np.arange(s, s + step)
+
+
+def _end_off_by_one(n, v):
+    step = max(1, oracle._BLOCK_BYTES // max(1, 8 * v))
+    for s in range(0, n, step):
+        yield np.arange(s, min(n - 1, s + step))
+
+
+@pytest.mark.parametrize("bad", [_drop_ragged_block, _end_off_by_one], ids=["ragged tail dropped", "last row dropped"])
+def test_multi_block_pin_catches_blocking_mistakes(monkeypatch, bad):
+    """A row-blocking mistake planted in the oracle fails the multi-block pin."""
+    monkeypatch.setattr(oracle, "_row_blocks", bad)
+    with pytest.raises(AssertionError):
+        _multi_block_pin(oracle, monkeypatch)
+
+
 def test_mean_with_no_valid_row():
     """Reading taken where the pages are silent: no valid row under mean gives 0, not NaN."""
     rng = np.random.default_rng(23)
