@@ -29,12 +29,15 @@
  *   - X, W, dX, dW are bf16, dense row-major, H contiguous.  labels is int32.
  *     loss, lse, grad_loss are fp32.  All data pointers are DEVICE pointers
  *     owned by the caller; the library never allocates or frees memory.
- *   - ws / ws_bytes: caller-owned device workspace, 256-byte aligned, of at
- *     least flce_workspace_bytes_min(p) bytes (grows with N and H, not with V);
- *     flce_workspace_bytes(p) bytes (also holds a row chunk of the vocabulary
- *     gradient and, when there are several chunks, an fp32 dW accumulator) lets
- *     flce_fwd_bwd take its faster fused path.  It is the only extra device memory the library
- *     touches.  Calls that share a workspace must be ordered on one stream.
+ *   - ws / ws_bytes: caller-owned device workspace, 256-byte aligned (the
+ *     alignment of the regions the library lays out in it), of at least
+ *     flce_workspace_bytes(p) bytes: O(N*(C + H)) for a fixed chunk width C,
+ *     independent of V.  The row-chunk calls (flce_fwd_bwd_rowchunk,
+ *     flce_soft_fwd_bwd) keep a chunk of the vocabulary gradient instead and
+ *     take flce_workspace_bytes_rowchunk(p); the vocabulary-shard calls take
+ *     flce_shard_workspace_bytes(p, shard).  The workspace is the only extra
+ *     device memory the library touches.  Calls that share a workspace must be
+ *     ordered on one stream.
  *   - Requirements: n >= 0, h >= 8, v >= 1, h % 8 == 0 (16-byte row pitch for
  *     the tensor-memory-access engine), X / W / dX / dW 16-byte aligned,
  *     labels / lse 4-byte aligned.  Violations return an error and launch
@@ -89,22 +92,25 @@ typedef struct {
   int32_t seq_len;       /* rows per sequence when shift = 1 (n must be a multiple); ignored otherwise */
 } flce_problem_t;
 
-/* Workspace size in bytes with which every call below takes its fastest path
- * (0 if p is invalid): the larger of the minimum size and the layout of
- * flce_fwd_bwd's fused path, i.e. a chunk of R rows of the bf16 vocabulary
- * gradient (R x V), one fp32 per (chunk row, 256-wide vocabulary tile), with
- * two or more chunks an fp32 dW accumulator (V x H), the chunk's rows of X
- * scaled by their per-row factor (R x H bf16) and O(N) per-row words.  Several
- * chunks have R = min(N/2, 1 GiB / 2V) rows; all N rows form one chunk (which
- * needs no accumulator) whenever that takes no more memory. */
+/* Workspace of flce_forward, flce_backward and flce_fwd_bwd (0 if p is
+ * invalid): the "extra HBM" of the fused operator, which
+ * "What-Each-Parallelism-Actually-Shards" §7.4 asks to keep bounded inside the
+ * operator instead of the [B,S,V] logits.  It holds the device status word,
+ * per-row partial (max, sum) pairs and target logits (O(N)), one vocabulary
+ * chunk of bf16 G (N x C, C = 8192 for N <= 16384 rows, else 4096) and an fp32
+ * dX accumulator (N x H).  Independent of V: the logits are recomputed in the
+ * backward pass, chunk by chunk, and never stored for a whole row. */
 size_t flce_workspace_bytes(const flce_problem_t* p);
 
-/* Smallest workspace every call below accepts (0 if p is invalid): the device
- * status word, per-row partial (max, sum) pairs, target logits, one vocabulary
- * chunk of bf16 G (N x C, C a fixed chunk width) and an fp32 dX accumulator
- * (N x H).  Independent of V.  With it, flce_fwd_bwd recomputes the logits in
- * the backward pass instead of keeping them for a row chunk. */
-size_t flce_workspace_bytes_min(const flce_problem_t* p);
+/* Workspace of the row-chunk calls (0 if p is invalid): a chunk of R rows of
+ * the bf16 vocabulary gradient (R x V), one fp32 per (chunk row, 256-wide
+ * vocabulary tile), with two or more chunks an fp32 dW accumulator (V x H),
+ * the chunk's rows of X scaled by their per-row factor (R x H bf16) and O(N)
+ * per-row words (§7.4's chunked cross-entropy, [B,C,V] per chunk).  Several
+ * chunks have R = min(N/2, 1 GiB / 2V) rows; all N rows form one chunk (no
+ * accumulator) whenever that takes no more memory than several — then the
+ * chunk buffer has the [N,V] shape of the logits, in bf16. */
+size_t flce_workspace_bytes_rowchunk(const flce_problem_t* p);
 
 /* Forward ("What-Each-Parallelism-Actually-Shards" §7.4: online log-sum-exp over
  * vocabulary tiles, target logit only).  Writes the loss (device fp32 scalar,
@@ -123,22 +129,28 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
                             void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
 
 /* Forward then backward with g = 1 (under FLCE_REDUCTION_NONE: the gradients
- * of the sum of the per-row losses): loss, lse, dX, dW in one call.  With
- * ws_bytes >= flce_workspace_bytes(p) it runs fused over row chunks (the logits
- * are computed once: forward ("What-Each-Parallelism-Actually-Shards" §7.4,
- * chunked CE) keeps each chunk's softmax relative to each row's target logit in
- * bf16, and once the chunk's lse is known dX and dW are contracted from it with
- * one factor per row);
- * with less (but at least flce_workspace_bytes_min(p)) it runs flce_forward then
- * flce_backward (logits recomputed, bounded V-independent workspace). */
+ * of the sum of the per-row losses): loss, lse, dX, dW in one call, on the
+ * bounded workspace of flce_workspace_bytes(p) ("What-Each-Parallelism-
+ * Actually-Shards" §7.4: online log-sum-exp, target logit only, logits
+ * recomputed in the backward pass).  Executes 8*N*H*V flops (the logits twice). */
 flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W,
                            const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
                            void* ws, size_t ws_bytes, flce_stream_t stream);
 
+/* The same results, fused over row chunks (§7.4's chunked cross-entropy): the
+ * logits are computed once (6*N*H*V flops).  The forward pass keeps each row
+ * chunk's softmax, relative to each row's target logit, as bf16 in the
+ * workspace, and once the chunk's lse is known dX and dW are contracted from it
+ * with one factor per row.  Needs flce_workspace_bytes_rowchunk(p) bytes of
+ * workspace, which grow with V (FLCE_ERR_WORKSPACE_TOO_SMALL below that). */
+flce_status_t flce_fwd_bwd_rowchunk(const flce_problem_t* p, const void* X, const void* W,
+                                    const int32_t* labels, float* loss, float* lse, void* dX, void* dW,
+                                    void* ws, size_t ws_bytes, flce_stream_t stream);
+
 /* End to end on host memory (no counterpart in the pages: the call for a caller
  * whose batch lives in host memory).  Reads X, W, labels from host memory and
  * writes loss, lse, dX, dW to host memory, with the shapes and layouts of
- * flce_fwd_bwd; page-locked host memory keeps the copies asynchronous.
+ * flce_fwd_bwd (the bounded path); page-locked host memory keeps the copies asynchronous.
  * Returns without waiting, having enqueued: one cudaMemcpyAsync per input to
  * the device on `in_stream`, the pass of flce_fwd_bwd on `stream` (after the
  * inputs), one cudaMemcpyAsync per result back to the host on `out_stream`
@@ -187,14 +199,18 @@ flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const
  *   loss_i = sum_k q_k log q_k - sum_k q_k log p_{id_k}      (KL(q || p) on the ids)
  *   G_ij   = s * (Q_i p_ij - sum_k q_k [j = id_k]),  Q_i = sum_k q_k
  * A row with Q_i = 0 is ignored; mean divides by the rows that are not.  k = 1,
- * q = 1 is the hard-label cross-entropy.  g = 1 as in flce_fwd_bwd; needs
- * flce_workspace_bytes(p) (the fused path).  shift must be 0; labels unused. */
+ * q = 1 is the hard-label cross-entropy.  g = 1 as in flce_fwd_bwd; runs on
+ * row chunks and needs flce_workspace_bytes_rowchunk(p).  shift must be 0;
+ * labels unused. */
 flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
                                 const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
                                 void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
 
 /* Synchronises `stream`, then returns the status word recorded in ws by the
- * kernels of earlier calls (FLCE_OK if none) and clears it. */
+ * kernels of earlier calls (FLCE_OK if none) and clears it.  The pages have no
+ * counterpart: it is how a caller learns of the errors the kernels find
+ * (labels outside [0,V), which the pages leave undefined; bounded waits that
+ * ran out) without the kernels trapping. */
 flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);
 
 /* Launches one kernel whose pipeline wait is on a barrier that nothing
@@ -220,6 +236,71 @@ flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns
 flce_status_t flce_profile_enable(int mask);
 flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, double* flops);
 
+/* ----------------------------------------------------------------------------
+ * Sharded loss ("What-Each-Parallelism-Actually-Shards" §3.2 vocab-parallel LM
+ * head, §7.2 vocab-parallel cross-entropy, §7.3 sequence-sharded loss).  The
+ * library holds no communicator: the caller runs the exchange (one all-gather
+ * of [2,N] per rank for the vocabulary split, an all-reduce of dX partials; for
+ * the sequence split, an all-reduce of the loss sum, the valid count and dW),
+ * and the calls below do every step of arithmetic on either side of it.
+ *
+ * Vocabulary split: rank r holds rows [v_offset, v_offset + v_rows) of W (the
+ * whole LM head has p->v rows; labels are global ids).  Steps:
+ *   1. flce_shard_forward: the shard's per-row lse over its ids and the target
+ *      logit where the shard holds the label (0 elsewhere);
+ *   2. gather every rank's (lse_part, tgt_part) in rank order;
+ *   3. flce_shard_combine: the global lse = log sum_r exp(lse_part_r), the
+ *      target logit sum_r tgt_part_r, the loss (the same bits on every rank);
+ *   4. flce_shard_backward with the global lse: the shard's dW rows (complete,
+ *      bf16) and its fp32 part of dX = G_shard W_shard;
+ *   5. sum the dX parts over ranks (fp32), flce_f32_to_bf16. */
+typedef struct {
+  int64_t v_offset;  /* first vocabulary id this shard holds */
+  int64_t v_rows;    /* number of ids (rows of W_shard), >= 1, v_offset + v_rows <= p->v */
+} flce_vocab_shard_t;
+
+/* Workspace of the three shard calls (0 if p or sh is invalid): O(N*(C + 1)),
+ * the bounded layout without the dX accumulator plus N shard-local labels.
+ * Any workspace that serves a shard of p also serves flce_shard_combine and
+ * flce_valid_count for p. */
+size_t flce_shard_workspace_bytes(const flce_problem_t* p, const flce_vocab_shard_t* sh);
+
+/* lse_part[N], tgt_part[N] (fp32 device): per row, log sum_{j in shard}
+ * exp(z_ij) and z_{i,y_i} when y_i is in the shard, else 0 (also for ignored
+ * rows).  Labels are checked against [0, p->v); reduction is not used. */
+flce_status_t flce_shard_forward(const flce_problem_t* p, const flce_vocab_shard_t* sh, const void* X,
+                                 const void* W_shard, const int32_t* labels, float* lse_part, float* tgt_part,
+                                 void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* lse_parts, tgt_parts: [parts, N] fp32 device, shard r in row r (1 <= parts <=
+ * 65536, summed in that order).  Writes lse[N] (global) and the loss under
+ * p->reduction (a scalar, or N per-row losses), as flce_forward would on the
+ * whole vocabulary. */
+flce_status_t flce_shard_combine(const flce_problem_t* p, int32_t parts, const float* lse_parts,
+                                 const float* tgt_parts, const int32_t* labels, float* loss, float* lse,
+                                 void* ws, size_t ws_bytes, flce_stream_t stream);
+
+/* Given the global lse, G restricted to the shard's ids:
+ * G_ij = s (exp(z_ij - lse_i) - [j = y_i]) valid_i, s from p->reduction, the
+ * global valid count and grad_loss (NULL: g = 1; N per-row values under
+ * FLCE_REDUCTION_NONE).  Writes dW_shard [v_rows, H] bf16 (= G_shard^T X) and
+ * dX_part [N, H] fp32 (= G_shard W_shard, this shard's term of dX; 16-byte
+ * aligned). */
+flce_status_t flce_shard_backward(const flce_problem_t* p, const flce_vocab_shard_t* sh, const void* X,
+                                  const void* W_shard, const int32_t* labels, const float* lse,
+                                  const float* grad_loss, float* dX_part, void* dW_shard, void* ws,
+                                  size_t ws_bytes, flce_stream_t stream);
+
+/* *count (device int32) = the number of rows whose label is not ignore_index
+ * (shift applied), with labels checked against [0, p->v).  The sequence split
+ * all-reduces it to scale a mean loss by the global count. */
+flce_status_t flce_valid_count(const flce_problem_t* p, const int32_t* labels, int32_t* count, void* ws,
+                               size_t ws_bytes, flce_stream_t stream);
+
+/* dst[i] = bf16(src[i]) (round to nearest even), i < count; both 16-byte
+ * aligned device pointers.  Casts a summed fp32 dX to the bf16 output. */
+flce_status_t flce_f32_to_bf16(const float* src, void* dst, int64_t count, flce_stream_t stream);
+
 /* Forward pass that allocates nothing and takes no workspace.  The pages have
  * no counterpart; it exists for callers that cannot allocate device memory —
  * code embedded in another runtime that owns all device allocations and hands
@@ -236,7 +317,12 @@ flce_status_t flce_profile_read(int kind, int64_t* launches, double* total_ms, d
  *     (different streams, or different host threads without ordering) race
  *     and give wrong results.  Order them on one stream.
  *   - Errors found on the device (a label outside [0,V), a bounded wait that
- *     ran out) set *loss to NaN; there is no status word to read. */
+ *     ran out, limited by FLCE_TIMEOUT_NS like every call) set the loss to NaN
+ *     — the scalar, or every one of the N per-row losses under
+ *     FLCE_REDUCTION_NONE; there is no status word to read.
+ *   - The array's address is looked up once per device and kept: do not call
+ *     this entry point on a device after cudaDeviceReset (or any reset of its
+ *     primary context) in the same process. */
 flce_status_t flce_forward_noalloc(const flce_problem_t* p, const void* X, const void* W,
                                    const int32_t* labels, float* loss, float* lse, flce_stream_t stream);
 

@@ -18,10 +18,12 @@ FLCE_ERR_LABEL_OUT_OF_RANGE = 5
 FLCE_ERR_TIMEOUT = 6
 REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 
-EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_min", "flce_forward", "flce_backward", "flce_fwd_bwd",
-            "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable", "flce_profile_read",
-            "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
-            "flce_soft_fwd_bwd", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_status_string")
+EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_rowchunk", "flce_forward", "flce_backward", "flce_fwd_bwd",
+            "flce_fwd_bwd_rowchunk", "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable",
+            "flce_profile_read", "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
+            "flce_soft_fwd_bwd", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_shard_workspace_bytes",
+            "flce_shard_forward", "flce_shard_combine", "flce_shard_backward", "flce_valid_count",
+            "flce_f32_to_bf16", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
@@ -36,6 +38,10 @@ class Problem(ctypes.Structure):
     _fields_ = [("n", ctypes.c_int64), ("h", ctypes.c_int64), ("v", ctypes.c_int64),
                 ("ignore_index", ctypes.c_int32), ("reduction", ctypes.c_int32),
                 ("shift", ctypes.c_int32), ("seq_len", ctypes.c_int32)]
+
+
+class VocabShard(ctypes.Structure):
+    _fields_ = [("v_offset", ctypes.c_int64), ("v_rows", ctypes.c_int64)]
 
 
 def lib_path() -> str:
@@ -56,8 +62,21 @@ def lib():
     P = ctypes.POINTER(Problem)
     L.flce_workspace_bytes.argtypes = [P]
     L.flce_workspace_bytes.restype = sz
-    L.flce_workspace_bytes_min.argtypes = [P]
-    L.flce_workspace_bytes_min.restype = sz
+    L.flce_workspace_bytes_rowchunk.argtypes = [P]
+    L.flce_workspace_bytes_rowchunk.restype = sz
+    S = ctypes.POINTER(VocabShard)
+    L.flce_shard_workspace_bytes.argtypes = [P, S]
+    L.flce_shard_workspace_bytes.restype = sz
+    L.flce_shard_forward.argtypes = [P, S, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_shard_forward.restype = ctypes.c_int
+    L.flce_shard_combine.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_shard_combine.restype = ctypes.c_int
+    L.flce_shard_backward.argtypes = [P, S, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_shard_backward.restype = ctypes.c_int
+    L.flce_valid_count.argtypes = [P, vp, vp, vp, sz, vp]
+    L.flce_valid_count.restype = ctypes.c_int
+    L.flce_f32_to_bf16.argtypes = [vp, vp, ctypes.c_int64, vp]
+    L.flce_f32_to_bf16.restype = ctypes.c_int
     L.flce_forward_noalloc.argtypes = [P, vp, vp, vp, vp, vp, vp]
     L.flce_forward_noalloc.restype = ctypes.c_int
     L.flce_forward.argtypes = [P, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -66,6 +85,8 @@ def lib():
     L.flce_backward.restype = ctypes.c_int
     L.flce_fwd_bwd.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_fwd_bwd.restype = ctypes.c_int
+    L.flce_fwd_bwd_rowchunk.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_fwd_bwd_rowchunk.restype = ctypes.c_int
     L.flce_topk_workspace_bytes.argtypes = [P, ctypes.c_int32]
     L.flce_topk_workspace_bytes.restype = sz
     L.flce_topk.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, sz, vp]
@@ -114,15 +135,15 @@ def _problem(n, h, v, ignore_index, reduction, shift=0, seq_len=0) -> Problem:
 
 
 def workspace_bytes(n, h, v, ignore_index=-100, reduction="mean") -> int:
-    """Workspace for the fastest path of every call (fused flce_fwd_bwd)."""
+    """Workspace of forward, backward and fwd_bwd: bounded, independent of V."""
     p = _problem(n, h, v, ignore_index, reduction)
     return int(lib().flce_workspace_bytes(ctypes.byref(p)))
 
 
-def workspace_bytes_min(n, h, v, ignore_index=-100, reduction="mean") -> int:
-    """Smallest workspace every call accepts (independent of V)."""
+def workspace_bytes_rowchunk(n, h, v, ignore_index=-100, reduction="mean") -> int:
+    """Workspace of the row-chunk calls (fwd_bwd(rowchunk=True), soft_fwd_bwd); grows with V."""
     p = _problem(n, h, v, ignore_index, reduction)
-    return int(lib().flce_workspace_bytes_min(ctypes.byref(p)))
+    return int(lib().flce_workspace_bytes_rowchunk(ctypes.byref(p)))
 
 
 def _torch():
@@ -152,9 +173,9 @@ def _check_inputs(x, w, labels):
         raise ValueError(f"shape mismatch: x {tuple(x.shape)}, w {tuple(w.shape)}, labels {tuple(labels.shape)}")
 
 
-def _alloc_ws(n, h, v, ignore_index, reduction, device, minimal=False):
+def _alloc_ws(n, h, v, ignore_index, reduction, device, rowchunk=False):
     torch = _torch()
-    nbytes = (workspace_bytes_min if minimal else workspace_bytes)(n, h, v, ignore_index, reduction)
+    nbytes = (workspace_bytes_rowchunk if rowchunk else workspace_bytes)(n, h, v, ignore_index, reduction)
     if nbytes == 0:
         raise FlceError(1, "workspace_bytes")
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
@@ -217,9 +238,11 @@ def backward(x, w, labels, lse, grad_loss=None, ignore_index=-100, reduction="me
 
 
 def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=None, out=None, check=False,
-            minimal_workspace=False, shift=0, seq_len=0):
+            rowchunk=False, shift=0, seq_len=0):
     """Returns (loss, lse, dX, dW, ws).  ``out`` may pass preallocated (loss, lse, dX, dW).
-    ``minimal_workspace`` allocates flce_workspace_bytes_min (the recompute path).  For
+    Default: flce_fwd_bwd on the bounded, V-independent workspace (logits recomputed in
+    the backward pass).  ``rowchunk=True``: flce_fwd_bwd_rowchunk (logits computed once,
+    a row chunk of the vocabulary gradient kept in a workspace that grows with V).  For
     reduction 'none' the loss is per row and the gradients are those of its sum."""
     torch = _torch()
     _check_inputs(x, w, labels)
@@ -227,15 +250,16 @@ def fwd_bwd(x, w, labels, ignore_index=-100, reduction="mean", ws=None, stream=N
     v = w.shape[0]
     p = _problem(n, h, v, ignore_index, reduction, shift, seq_len)
     if ws is None:
-        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device, minimal=minimal_workspace)
+        ws = _alloc_ws(n, h, v, ignore_index, reduction, x.device, rowchunk=rowchunk)
     if out is None:
         out = (torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device),
                torch.empty(n, dtype=torch.float32, device=x.device), torch.empty_like(x), torch.empty_like(w))
     loss, lse, dX, dW = out
     s = _stream_ptr(stream)
-    _call("flce_fwd_bwd", lib().flce_fwd_bwd(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
-                                             loss.data_ptr(), lse.data_ptr(), dX.data_ptr(), dW.data_ptr(),
-                                             ws.data_ptr(), ws.numel(), s))
+    name = "flce_fwd_bwd_rowchunk" if rowchunk else "flce_fwd_bwd"
+    _call(name, getattr(lib(), name)(ctypes.byref(p), x.data_ptr(), w.data_ptr(), labels.data_ptr(),
+                                     loss.data_ptr(), lse.data_ptr(), dX.data_ptr(), dW.data_ptr(),
+                                     ws.data_ptr(), ws.numel(), s))
     if check:
         _call("device", read_device_status(ws, stream))
     return loss, lse, dX, dW, ws
@@ -313,7 +337,7 @@ def soft_fwd_bwd(x, w, tgt_idx, tgt_prob, reduction="mean", ws=None, stream=None
     _check_inputs(x, w, torch.empty(n, dtype=torch.int32, device=x.device))
     p = _problem(n, h, v, -100, reduction)
     if ws is None:
-        ws = _alloc_ws(n, h, v, -100, reduction, x.device)
+        ws = _alloc_ws(n, h, v, -100, reduction, x.device, rowchunk=True)
     loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device)
     lse = torch.empty(n, dtype=torch.float32, device=x.device)
     dX = torch.empty_like(x)
@@ -357,6 +381,119 @@ def scale_grads(dX, dW, grad_loss, stream=None):
                                                      dW.data_ptr(), _stream_ptr(stream)))
 
 
+def _f32(t, shape, name):
+    torch = _torch()
+    if t.dtype != torch.float32 or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or not t.is_cuda:
+        raise ValueError(f"{name} must be a contiguous fp32 CUDA tensor of shape {tuple(shape)}")
+
+
+def shard_workspace_bytes(n, h, v_total, v_offset, v_rows, ignore_index=-100, reduction="mean") -> int:
+    p = _problem(n, h, v_total, ignore_index, reduction)
+    sh = VocabShard(int(v_offset), int(v_rows))
+    return int(lib().flce_shard_workspace_bytes(ctypes.byref(p), ctypes.byref(sh)))
+
+
+def _shard_ws(x, w_shard, v_total, v_offset, ignore_index, reduction, shift, seq_len, ws):
+    torch = _torch()
+    n, h = x.shape
+    if ws is not None:
+        return ws
+    p = _problem(n, h, v_total, ignore_index, reduction, shift, seq_len)
+    sh = VocabShard(int(v_offset), int(w_shard.shape[0]))
+    nbytes = int(lib().flce_shard_workspace_bytes(ctypes.byref(p), ctypes.byref(sh)))
+    if nbytes == 0:
+        raise FlceError(1, "flce_shard_workspace_bytes")
+    return torch.empty(nbytes, dtype=torch.uint8, device=x.device)
+
+
+def shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index=-100, shift=0, seq_len=0, ws=None,
+                  stream=None):
+    """Vocabulary shard [v_offset, v_offset + w_shard.shape[0]) of a v_total-row LM head:
+    (lse_part [N], tgt_part [N], ws) — the shard's per-row lse and the target logit
+    where the shard holds the label (else 0)."""
+    torch = _torch()
+    _check_inputs(x, w_shard, labels)
+    n, h = x.shape
+    p = _problem(n, h, v_total, ignore_index, "mean", shift, seq_len)
+    sh = VocabShard(int(v_offset), int(w_shard.shape[0]))
+    ws = _shard_ws(x, w_shard, v_total, v_offset, ignore_index, "mean", shift, seq_len, ws)
+    lse_p = torch.empty(n, dtype=torch.float32, device=x.device)
+    tgt_p = torch.empty(n, dtype=torch.float32, device=x.device)
+    _call("flce_shard_forward", lib().flce_shard_forward(ctypes.byref(p), ctypes.byref(sh), x.data_ptr(),
+                                                         w_shard.data_ptr(), labels.data_ptr(), lse_p.data_ptr(),
+                                                         tgt_p.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                         _stream_ptr(stream)))
+    return lse_p, tgt_p, ws
+
+
+def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index=-100, reduction="mean", shift=0,
+                  seq_len=0, ws=None, stream=None):
+    """lse_parts, tgt_parts: [P, N] fp32 (shard r in row r).  Returns (loss, lse [N], ws)."""
+    torch = _torch()
+    P, n = lse_parts.shape
+    _f32(lse_parts, (P, n), "lse_parts")
+    _f32(tgt_parts, (P, n), "tgt_parts")
+    if labels.dtype != torch.int32 or labels.shape != (n,) or not labels.is_contiguous():
+        raise ValueError("labels must be contiguous int32 [N]")
+    p = _problem(n, h, v_total, ignore_index, reduction, shift, seq_len)
+    if ws is None:
+        nbytes = int(lib().flce_workspace_bytes(ctypes.byref(p)))
+        ws = torch.empty(nbytes, dtype=torch.uint8, device=lse_parts.device)
+    loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=lse_parts.device)
+    lse = torch.empty(n, dtype=torch.float32, device=lse_parts.device)
+    _call("flce_shard_combine", lib().flce_shard_combine(ctypes.byref(p), int(P), lse_parts.data_ptr(),
+                                                         tgt_parts.data_ptr(), labels.data_ptr(), loss.data_ptr(),
+                                                         lse.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                         _stream_ptr(stream)))
+    return loss, lse, ws
+
+
+def shard_backward(x, w_shard, labels, lse, v_offset, v_total, grad_loss=None, ignore_index=-100,
+                   reduction="mean", shift=0, seq_len=0, ws=None, stream=None):
+    """Given the global lse: (dX_part [N, H] fp32, dW_shard [rows, H] bf16, ws)."""
+    torch = _torch()
+    _check_inputs(x, w_shard, labels)
+    n, h = x.shape
+    _f32(lse, (n,), "lse")
+    p = _problem(n, h, v_total, ignore_index, reduction, shift, seq_len)
+    sh = VocabShard(int(v_offset), int(w_shard.shape[0]))
+    ws = _shard_ws(x, w_shard, v_total, v_offset, ignore_index, reduction, shift, seq_len, ws)
+    dXp = torch.empty(n, h, dtype=torch.float32, device=x.device)
+    dWs = torch.empty_like(w_shard)
+    g = None if grad_loss is None else grad_loss.data_ptr()
+    _call("flce_shard_backward", lib().flce_shard_backward(ctypes.byref(p), ctypes.byref(sh), x.data_ptr(),
+                                                           w_shard.data_ptr(), labels.data_ptr(), lse.data_ptr(), g,
+                                                           dXp.data_ptr(), dWs.data_ptr(), ws.data_ptr(), ws.numel(),
+                                                           _stream_ptr(stream)))
+    return dXp, dWs, ws
+
+
+def valid_count(labels, v, h=8, ignore_index=-100, shift=0, seq_len=0, ws=None, stream=None):
+    """Rows whose label is not ignore_index, as a one-element int32 CUDA tensor."""
+    torch = _torch()
+    n = labels.shape[0]
+    p = _problem(n, h, v, ignore_index, "sum", shift, seq_len)
+    if ws is None:
+        ws = torch.empty(max(256, int(lib().flce_workspace_bytes(ctypes.byref(p)))), dtype=torch.uint8,
+                         device=labels.device)
+    out = torch.empty(1, dtype=torch.int32, device=labels.device)
+    _call("flce_valid_count", lib().flce_valid_count(ctypes.byref(p), labels.data_ptr(), out.data_ptr(),
+                                                     ws.data_ptr(), ws.numel(), _stream_ptr(stream)))
+    return out, ws
+
+
+def f32_to_bf16(src, out=None, stream=None):
+    """bf16 copy of a contiguous fp32 CUDA tensor (round to nearest even)."""
+    torch = _torch()
+    if src.dtype != torch.float32 or not src.is_contiguous() or not src.is_cuda:
+        raise ValueError("src must be a contiguous fp32 CUDA tensor")
+    if out is None:
+        out = torch.empty(src.shape, dtype=torch.bfloat16, device=src.device)
+    _call("flce_f32_to_bf16", lib().flce_f32_to_bf16(src.data_ptr(), out.data_ptr(), src.numel(),
+                                                     _stream_ptr(stream)))
+    return out
+
+
 class _LinearCrossEntropy:
     """torch.autograd.Function wrapper, built lazily so importing needs no torch.
 
@@ -373,12 +510,12 @@ class _LinearCrossEntropy:
 
             class Fn(torch.autograd.Function):
                 @staticmethod
-                def forward(ctx, x2, w, labels, ignore_index, reduction, shift, seq_len):
+                def forward(ctx, x2, w, labels, ignore_index, reduction, shift, seq_len, rowchunk):
                     ctx.reduction = reduction
                     kw = dict(shift=shift, seq_len=seq_len)
                     needs = ctx.needs_input_grad[0] or ctx.needs_input_grad[1]
                     if needs and reduction != "none":
-                        loss, _, dX, dW, _ = fwd_bwd(x2, w, labels, ignore_index, reduction, **kw)
+                        loss, _, dX, dW, _ = fwd_bwd(x2, w, labels, ignore_index, reduction, rowchunk=rowchunk, **kw)
                         ctx.save_for_backward(dX, dW)
                         return loss.reshape(())
                     loss, lse, _ = forward(x2, w, labels, ignore_index, reduction, **kw)
@@ -394,17 +531,18 @@ class _LinearCrossEntropy:
                         ignore_index, kw = ctx.args
                         g = grad.detach().to(torch.float32).reshape(-1).contiguous()
                         dX, dW, _ = backward(x2, w, labels, lse, g, ignore_index, "none", **kw)
-                        return dX, dW, None, None, None, None, None
+                        return dX, dW, None, None, None, None, None, None
                     dX, dW = ctx.saved_tensors
                     g = grad.detach().to(torch.float32).reshape(1).contiguous()
                     scale_grads(dX, dW, g)
-                    return dX, dW, None, None, None, None, None
+                    return dX, dW, None, None, None, None, None, None
 
             cls.fn = Fn
         return cls.fn
 
 
-def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str = "mean", shift: int = 0):
+def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str = "mean", shift: int = 0,
+                         rowchunk: bool = False):
     """Cross-entropy of ``x @ w.T`` against ``labels`` without materialising the logits.
 
     x: [..., H] bf16 CUDA, w: [V, H] bf16, labels: [...] integer (same leading
@@ -412,6 +550,9 @@ def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str 
     (per-row losses, shaped like labels).  shift=1 scores position t of each
     sequence against the label at t + 1 (x and labels [B, S, ...]; the last
     position of each sequence is ignored).  Autograd flows to x and w.
+    The extra device memory is bounded and independent of V (logits recomputed
+    in the backward pass); ``rowchunk=True`` computes the logits once and keeps a
+    row chunk of the vocabulary gradient instead (memory grows with V).
     """
     torch = _torch()
     h = x.shape[-1]
@@ -423,7 +564,7 @@ def linear_cross_entropy(x, w, labels, ignore_index: int = -100, reduction: str 
     x2 = x.reshape(-1, h).contiguous()
     lab = labels.reshape(-1).to(torch.int32).contiguous()
     loss = _LinearCrossEntropy.get().apply(x2, w.contiguous(), lab, int(ignore_index), reduction, int(shift),
-                                           seq_len)
+                                           seq_len, bool(rowchunk))
     return loss.reshape(labels.shape) if reduction == "none" else loss
 
 

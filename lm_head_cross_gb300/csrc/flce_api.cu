@@ -17,6 +17,7 @@ namespace flce {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr int32_t kMaxShardParts = 1 << 16;  // most vocabulary shards flce_shard_combine takes
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s; a healthy wait lasts microseconds
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -35,6 +36,7 @@ struct Layout {
   size_t mref;                    // fused path: per row of X its target logit, log2 units
   size_t rowscale, fix_list;      // fused path: per chunk row factor f_i; rows listed for the full fix-up
   size_t xs;                      // fused path: f_i x_i for the chunk's rows, bf16 [rows, H]
+  size_t lab;                     // vocabulary-shard calls: shard-local labels [N] int32
   size_t total;
   int nblk, chunk;
   int rows;                       // fused path: rows per chunk (0: layout without the fused path)
@@ -60,7 +62,10 @@ int fused_rows(int64_t n, int64_t v, int64_t h) {
   return static_cast<int>(rows);
 }
 
-Layout make_layout(const flce_problem_t& p, bool fused) {
+// `shard`: the layout of the vocabulary-shard calls — no dX accumulator (the
+// shard backward accumulates into the caller's fp32 buffer), plus the
+// shard-local labels.
+Layout make_layout(const flce_problem_t& p, bool fused, bool shard = false) {
   Layout L{};
   if (p.n == 0) {  // an empty batch needs the header (status word) only
     L.total = kAlign;
@@ -99,7 +104,7 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
                               : 2 * n * static_cast<size_t>(L.chunk);
   off = align_up(off + gbytes);
   L.dx_acc = off;
-  const size_t accbytes = fused ? (one_chunk ? 0 : 4 * v * h) : 4 * n * h;
+  const size_t accbytes = fused ? (one_chunk ? 0 : 4 * v * h) : (shard ? 0 : 4 * n * h);
   off = align_up(off + accbytes);
   L.mtile = off;
   if (fused) off = align_up(off + sizeof(float) * static_cast<size_t>(L.rows) * vtiles);
@@ -111,15 +116,12 @@ Layout make_layout(const flce_problem_t& p, bool fused) {
   if (fused) off = align_up(off + sizeof(int) * static_cast<size_t>(L.rows));
   L.xs = off;
   if (fused) off = align_up(off + 2 * static_cast<size_t>(L.rows) * h);
+  L.lab = off;
+  if (shard) off = align_up(off + sizeof(int32_t) * n);
   L.total = off;
   return L;
 }
 
-// Workspace for every call on its fastest path: the fused layout, or the plain
-// one if that is larger (small problems).
-size_t workspace_full(const flce_problem_t& p) {
-  return std::max(make_layout(p, true).total, make_layout(p, false).total);
-}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -150,6 +152,8 @@ bool make_map(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint64_t
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+}  // namespace
+
 uint64_t timeout_ns() {
   static uint64_t t = [] {
     const char* e = std::getenv("FLCE_TIMEOUT_NS");
@@ -161,6 +165,8 @@ uint64_t timeout_ns() {
   }();
   return t;
 }
+
+namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -268,6 +274,7 @@ struct Ctx {
   float* mref() const { return reinterpret_cast<float*>(ws + L.mref); }
   float* rowscale() const { return reinterpret_cast<float*>(ws + L.rowscale); }
   void* xs() const { return ws + L.xs; }
+  int32_t* lab() const { return reinterpret_cast<int32_t*>(ws + L.lab); }
   LabelView labels_of(const int32_t* labels) const {
     return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1, nullptr, nullptr, 0};
   }
@@ -384,22 +391,20 @@ cudaError_t timed(int kind, double flops, cudaStream_t stream, F&& launch) {
   return e;
 }
 
-// `fused_call`: the call can take the fused path (flce_fwd_bwd, flce_soft_fwd_bwd),
-// which it does when the workspace holds the fused layout.
+// Workspace layouts: the bounded one of every call (independent of V), the
+// row-chunk one of the calls that keep a chunk of the vocabulary gradient
+// (flce_fwd_bwd_rowchunk, flce_soft_fwd_bwd), the vocabulary-shard one.
+enum class Lay { kBounded, kRowChunk, kShard };
+
 flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes, flce_stream_t stream,
-                      bool fused_call = false) {
+                      Lay lay = Lay::kBounded) {
   flce_status_t st = check_problem(p);
   if (st != FLCE_OK) return st;
   if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
   c->p = p;
-  const Layout full = make_layout(*p, true);
-  if (fused_call && ws_bytes >= full.total) {
-    c->L = full;  // room for the fused path
-  } else {
-    c->L = make_layout(*p, false);
-    if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
-  }
+  c->L = make_layout(*p, lay == Lay::kRowChunk, lay == Lay::kShard);
+  if (ws_bytes < c->L.total) return FLCE_ERR_WORKSPACE_TOO_SMALL;
   c->ws = static_cast<uint8_t*>(ws);
   c->stream = reinterpret_cast<cudaStream_t>(stream);
   st = device_info(&c->dev);
@@ -409,8 +414,10 @@ flce_status_t prepare(Ctx* c, const flce_problem_t* p, void* ws, size_t ws_bytes
   return cuda_status(cudaMemsetAsync(c->ws + c->L.status, 0, kAlign, c->stream));
 }
 
-flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
-                          const float* grad_loss) {
+// The forward projection with the online log-sum-exp: per (vocabulary range,
+// row) partials in the workspace, target logits where a tile holds the label.
+// Returns the split count through *vsplit.
+flce_status_t run_forward_tc(const Ctx& c, const void* X, const void* W, const int32_t* labels, int* vsplit) {
   const flce_problem_t& p = *c.p;
   TcMaps maps;
   if (!make_map(&maps.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
@@ -439,13 +446,20 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = pair_grid(c.dev.sms, units);
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
-  flce_status_t st = cuda_status(
-      timed(0, flops, c.stream, [&] { return launch_tc(kModeForward, maps, tp, grid, c.stream); }));
+  *vsplit = tp.vsplit;
+  return cuda_status(timed(0, flops, c.stream, [&] { return launch_tc(kModeForward, maps, tp, grid, c.stream); }));
+}
+
+flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int32_t* labels, float* loss, float* lse,
+                          const float* grad_loss) {
+  const flce_problem_t& p = *c.p;
+  int vsplit = 0;
+  flce_status_t st = run_forward_tc(c, X, W, labels, &vsplit);
   if (st != FLCE_OK) return st;
   st = cuda_status(timed(3, 0.0, c.stream, [&] {
-    return launch_fwd_finalize_rows(0, tp.n, tp.n, tp.v, tp.vsplit, c.labels_of(labels), c.part_m(), c.part_l(),
-                                    c.tgt(), lse, c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(),
-                                    c.status(), c.stream);
+    return launch_fwd_finalize_rows(0, static_cast<int>(p.n), static_cast<int>(p.n), static_cast<int>(p.v), vsplit,
+                                    c.labels_of(labels), c.part_m(), c.part_l(), c.tgt(), lse,
+                                    c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
   }));
   if (st != FLCE_OK) return st;
   return cuda_status(timed(3, 0.0, c.stream, [&] {
@@ -455,9 +469,11 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
   }));
 }
 
-// Backward given lse and the scale already in the workspace.
+// Backward given lse and the scale already in the workspace.  dX accumulates
+// in fp32 in `dx_acc` (the workspace's accumulator, or a caller buffer) and is
+// written as bf16 to dX unless dX is null.
 flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int32_t* labels, const float* lse,
-                           const float* grad_rows, void* dX, void* dW) {
+                           const float* grad_rows, void* dX, void* dW, float* dx_acc) {
   const flce_problem_t& p = *c.p;
   const int chunk = c.L.chunk;
   TcParams tp{};
@@ -482,7 +498,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   TcMaps bm;  // bwd: W MN-major (dX B operand), X MN-major (dW B operand), dX fp32 acc, dW store
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
-  if (!make_map(&bm.out, c.dx_acc(), CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.n, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
+  if (!make_map(&bm.out, dx_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.n, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out2, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
 
   for (int64_t c0 = 0; c0 < p.v; c0 += chunk) {
@@ -522,7 +538,8 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     }));
     if (st != FLCE_OK) return st;
   }
-  return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(c.dx_acc(), dX, p.n * p.h, c.stream); }));
+  if (!dX) return FLCE_OK;
+  return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(dx_acc, dX, p.n * p.h, c.stream); }));
 }
 
 // Fused forward + backward over row chunks (6NHV executed, no recompute):
@@ -727,7 +744,7 @@ struct HostLayout {
 HostLayout host_layout(const flce_problem_t& p) {
   HostLayout L{};
   const size_t n = static_cast<size_t>(p.n), h = static_cast<size_t>(p.h), v = static_cast<size_t>(p.v);
-  size_t off = align_up(workspace_full(p));
+  size_t off = align_up(make_layout(p, false).total);  // the workspace of flce_fwd_bwd
   L.ws = 0;
   L.x = off;
   off = align_up(off + 2 * n * h);
@@ -779,12 +796,12 @@ extern "C" {
 
 size_t flce_workspace_bytes(const flce_problem_t* p) {
   if (check_problem(p) != FLCE_OK) return 0;
-  return workspace_full(*p);
+  return make_layout(*p, false).total;
 }
 
-size_t flce_workspace_bytes_min(const flce_problem_t* p) {
+size_t flce_workspace_bytes_rowchunk(const flce_problem_t* p) {
   if (check_problem(p) != FLCE_OK) return 0;
-  return make_layout(*p, false).total;
+  return make_layout(*p, true).total;
 }
 
 flce_status_t flce_forward(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
@@ -829,27 +846,45 @@ flce_status_t flce_backward(const flce_problem_t* p, const void* X, const void* 
                                c.scale(), c.stream);
   }));
   if (st != FLCE_OK) return st;
-  return run_backward(c, X, W, labels, lse, c.per_row() ? grad_loss : nullptr, dX, dW);
+  return run_backward(c, X, W, labels, lse, c.per_row() ? grad_loss : nullptr, dX, dW, c.dx_acc());
 }
 
-flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
-                           float* lse, void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+namespace {
+flce_status_t fwd_bwd_args(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
+                           const float* loss, const float* lse, const void* dX, const void* dW) {
   if (!p || !W || !dW || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) || !rows_ok(p, dX) ||
       !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
     return FLCE_ERR_INVALID_ARGUMENT;
   if (!aligned(X, 16) || !aligned(W, 16) || !aligned(dX, 16) || !aligned(dW, 16) || !aligned(labels, 4) ||
       !aligned(lse, 4) || !aligned(loss, 4))
     return FLCE_ERR_MISALIGNED;
-  flce_status_t st = check_problem(p);
+  return check_problem(p);
+}
+}  // namespace
+
+flce_status_t flce_fwd_bwd(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels, float* loss,
+                           float* lse, void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  flce_status_t st = fwd_bwd_args(p, X, W, labels, loss, lse, dX, dW);
   if (st != FLCE_OK) return st;
   if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  st = prepare(&c, p, ws, ws_bytes, stream, true);
+  st = prepare(&c, p, ws, ws_bytes, stream);
   if (st != FLCE_OK) return st;
-  if (c.L.rows > 0) return run_fused(c, X, W, c.labels_of(labels), loss, lse, dX, dW);
   st = run_forward(c, X, W, labels, loss, lse, nullptr);
   if (st != FLCE_OK) return st;
-  return run_backward(c, X, W, labels, lse, nullptr, dX, dW);
+  return run_backward(c, X, W, labels, lse, nullptr, dX, dW, c.dx_acc());
+}
+
+flce_status_t flce_fwd_bwd_rowchunk(const flce_problem_t* p, const void* X, const void* W, const int32_t* labels,
+                                    float* loss, float* lse, void* dX, void* dW, void* ws, size_t ws_bytes,
+                                    flce_stream_t stream) {
+  flce_status_t st = fwd_bwd_args(p, X, W, labels, loss, lse, dX, dW);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
+  Ctx c;
+  st = prepare(&c, p, ws, ws_bytes, stream, Lay::kRowChunk);
+  if (st != FLCE_OK) return st;
+  return run_fused(c, X, W, c.labels_of(labels), loss, lse, dX, dW);
 }
 
 size_t flce_host_buffer_bytes(const flce_problem_t* p) {
@@ -975,11 +1010,187 @@ flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* 
   if (st != FLCE_OK) return st;
   if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  st = prepare(&c, p, ws, ws_bytes, stream, true);
+  st = prepare(&c, p, ws, ws_bytes, stream, Lay::kRowChunk);
   if (st != FLCE_OK) return st;
-  if (c.L.rows == 0) return FLCE_ERR_WORKSPACE_TOO_SMALL;  // needs flce_workspace_bytes(p)
   const LabelView lv{nullptr, p->ignore_index, 0, 1, tgt_idx, tgt_prob, k};
   return run_fused(c, X, W, lv, loss, lse, dX, dW);
+}
+
+// ----------------------------------------------------------------------------- vocabulary / sequence shards
+
+namespace {
+
+// The shard of a problem as the kernels see it: v = the shard's rows of W,
+// shard-local labels (ignore_index -1, no shift).
+flce_status_t shard_problem(const flce_problem_t* p, const flce_vocab_shard_t* sh, flce_problem_t* q) {
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (!sh || sh->v_offset < 0 || sh->v_rows < 1 || sh->v_offset > p->v - sh->v_rows) return FLCE_ERR_INVALID_ARGUMENT;
+  *q = *p;
+  q->v = sh->v_rows;
+  q->ignore_index = -1;
+  q->shift = 0;
+  q->seq_len = 0;
+  return check_problem(q);
+}
+
+LabelView global_labels(const flce_problem_t* p, const int32_t* labels) {
+  return LabelView{labels, p->ignore_index, p->shift, p->shift ? p->seq_len : 1, nullptr, nullptr, 0};
+}
+
+}  // namespace
+
+size_t flce_shard_workspace_bytes(const flce_problem_t* p, const flce_vocab_shard_t* sh) {
+  flce_problem_t q;
+  if (shard_problem(p, sh, &q) != FLCE_OK) return 0;
+  return make_layout(q, false, true).total;
+}
+
+flce_status_t flce_shard_forward(const flce_problem_t* p, const flce_vocab_shard_t* sh, const void* X,
+                                 const void* W_shard, const int32_t* labels, float* lse_part, float* tgt_part,
+                                 void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!p || !W_shard || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse_part) || !rows_ok(p, tgt_part))
+    return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W_shard, 16) || !aligned(labels, 4) || !aligned(lse_part, 4) ||
+      !aligned(tgt_part, 4))
+    return FLCE_ERR_MISALIGNED;
+  flce_problem_t q;
+  flce_status_t st = shard_problem(p, sh, &q);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(&q, nullptr, nullptr, ws, ws_bytes, stream);
+  Ctx c;
+  st = prepare(&c, &q, ws, ws_bytes, stream, Lay::kShard);
+  if (st != FLCE_OK) return st;
+  const int n = static_cast<int>(p->n);
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_shard_labels(n, p->v, sh->v_offset, sh->v_rows, global_labels(p, labels), c.lab(), c.status(),
+                               c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  int vsplit = 0;
+  st = run_forward_tc(c, X, W_shard, c.lab(), &vsplit);
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_shard_finalize(n, vsplit, c.part_m(), c.part_l(), c.tgt(), c.lab(), lse_part, tgt_part, c.stream);
+  }));
+}
+
+flce_status_t flce_shard_combine(const flce_problem_t* p, int32_t parts, const float* lse_parts,
+                                 const float* tgt_parts, const int32_t* labels, float* loss, float* lse, void* ws,
+                                 size_t ws_bytes, flce_stream_t stream) {
+  if (!p || !rows_ok(p, lse_parts) || !rows_ok(p, tgt_parts) || !rows_ok(p, labels) || !rows_ok(p, lse) ||
+      !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
+    return FLCE_ERR_INVALID_ARGUMENT;
+  if (parts < 1 || parts > kMaxShardParts) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(lse_parts, 4) || !aligned(tgt_parts, 4) || !aligned(labels, 4) || !aligned(loss, 4) ||
+      !aligned(lse, 4))
+    return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(p, loss, nullptr, ws, ws_bytes, stream);
+  if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  // the header and the block partials, which every layout places first
+  Ctx c;
+  c.p = p;
+  c.L = make_layout(*p, false);
+  if (ws_bytes < c.L.part_m) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  c.ws = static_cast<uint8_t*>(ws);
+  c.stream = reinterpret_cast<cudaStream_t>(stream);
+  st = device_info(&c.dev);
+  if (st != FLCE_OK) return st;
+  st = cuda_status(cudaMemsetAsync(c.ws + c.L.status, 0, kAlign, c.stream));
+  if (st != FLCE_OK) return st;
+  const int n = static_cast<int>(p->n);
+  const int nblk = (n + kFinalizeThreads - 1) / kFinalizeThreads;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_shard_combine(n, parts, p->v, global_labels(p, labels), lse_parts, tgt_parts, lse,
+                                c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(nblk, c.blk_loss(), c.blk_valid(), p->reduction, nullptr,
+                               c.per_row() ? nullptr : loss, c.n_valid(), c.scale(), c.stream);
+  }));
+}
+
+flce_status_t flce_shard_backward(const flce_problem_t* p, const flce_vocab_shard_t* sh, const void* X,
+                                  const void* W_shard, const int32_t* labels, const float* lse,
+                                  const float* grad_loss, float* dX_part, void* dW_shard, void* ws, size_t ws_bytes,
+                                  flce_stream_t stream) {
+  if (!p || !W_shard || !dW_shard || !rows_ok(p, X) || !rows_ok(p, labels) || !rows_ok(p, lse) ||
+      !rows_ok(p, dX_part))
+    return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(X, 16) || !aligned(W_shard, 16) || !aligned(dX_part, 16) || !aligned(dW_shard, 16) ||
+      !aligned(labels, 4) || !aligned(lse, 4) || (grad_loss && !aligned(grad_loss, 4)))
+    return FLCE_ERR_MISALIGNED;
+  flce_problem_t q;
+  flce_status_t st = shard_problem(p, sh, &q);
+  if (st != FLCE_OK) return st;
+  if (p->n == 0) return run_empty(&q, nullptr, dW_shard, ws, ws_bytes, stream);
+  Ctx c;
+  st = prepare(&c, &q, ws, ws_bytes, stream, Lay::kShard);
+  if (st != FLCE_OK) return st;
+  if (c.per_row() && !grad_loss) return FLCE_ERR_INVALID_ARGUMENT;
+  const int n = static_cast<int>(p->n);
+  // the valid count and s from the global labels, then the shard-local labels
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_label_scan_view(n, static_cast<int>(p->v), global_labels(p, labels), c.blk_loss(), c.blk_valid(),
+                                  c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p->reduction,
+                               c.per_row() ? nullptr : grad_loss, nullptr, c.n_valid(), c.scale(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_shard_labels(n, p->v, sh->v_offset, sh->v_rows, global_labels(p, labels), c.lab(), c.status(),
+                               c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  return run_backward(c, X, W_shard, c.lab(), lse, c.per_row() ? grad_loss : nullptr, nullptr, dW_shard, dX_part);
+}
+
+flce_status_t flce_valid_count(const flce_problem_t* p, const int32_t* labels, int32_t* count, void* ws,
+                               size_t ws_bytes, flce_stream_t stream) {
+  if (!p || !count || !rows_ok(p, labels)) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(labels, 4) || !aligned(count, 4)) return FLCE_ERR_MISALIGNED;
+  flce_status_t st = check_problem(p);
+  if (st != FLCE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (p->n == 0) {
+    st = run_empty(p, nullptr, nullptr, ws, ws_bytes, stream);
+    if (st != FLCE_OK) return st;
+    return cuda_status(cudaMemsetAsync(count, 0, sizeof(int32_t), s));
+  }
+  if (!ws) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  Ctx c;
+  c.p = p;
+  c.L = make_layout(*p, false);
+  if (ws_bytes < c.L.part_m) return FLCE_ERR_WORKSPACE_TOO_SMALL;
+  c.ws = static_cast<uint8_t*>(ws);
+  c.stream = s;
+  st = cuda_status(cudaMemsetAsync(c.ws + c.L.status, 0, kAlign, s));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, s, [&] {
+    return launch_label_scan_view(static_cast<int>(p->n), static_cast<int>(p->v), global_labels(p, labels),
+                                  c.blk_loss(), c.blk_valid(), c.status(), s);
+  }));
+  if (st != FLCE_OK) return st;
+  return cuda_status(timed(3, 0.0, s, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), FLCE_REDUCTION_SUM, nullptr, nullptr, count,
+                               c.scale(), s);
+  }));
+}
+
+flce_status_t flce_f32_to_bf16(const float* src, void* dst, int64_t count, flce_stream_t stream) {
+  if (count < 0 || (count > 0 && (!src || !dst))) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(src, 16) || !aligned(dst, 16)) return FLCE_ERR_MISALIGNED;
+  if (count == 0) return FLCE_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  return cuda_status(timed(3, 0.0, s, [&] { return launch_f32_to_bf16(src, dst, count, s); }));
 }
 
 flce_status_t flce_profile_enable(int mask) {

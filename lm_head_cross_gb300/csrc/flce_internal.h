@@ -179,8 +179,31 @@ cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk
                                 const float* grad_loss, float* loss_out, int* n_valid_out, float* scale_out,
                                 cudaStream_t stream);
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
+// fp32 -> bf16 (round to nearest even) of any count; src and dst 16-byte aligned.
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
+
+// Vocabulary shards.  A shard's kernels read labels in shard-local form: -1 for an
+// ignored row (the shard calls run with ignore_index -1), y - v0 for a label the
+// shard holds, kNotOwned for a valid label held by another shard (it never equals
+// a column index, so no tile gathers it and no one-hot entry is subtracted).
+constexpr int kNotOwned = 0x7fffffff;
+cudaError_t launch_shard_labels(int n, int64_t v_total, int64_t v0, int64_t vs, LabelView lv, int32_t* lab_local,
+                                int* status, cudaStream_t stream);
+// Per row: the shard's lse (natural log) from the split partials, and its target
+// logit where the shard holds the label (0 elsewhere).
+cudaError_t launch_shard_finalize(int n, int vsplit, const float* part_m, const float* part_l, const float* tgt,
+                                  const int32_t* lab_local, float* lse_part, float* tgt_part, cudaStream_t stream);
+// Per row: lse = log sum_r exp(lse_parts[r]), z = sum_r tgt_parts[r] (parts in index
+// order), the loss row against the global labels, and per-block partials.
+cudaError_t launch_shard_combine(int n, int parts, int64_t v_total, LabelView lv, const float* lse_parts,
+                                 const float* tgt_parts, float* lse, float* loss_rows, double* blk_loss,
+                                 int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream);
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+
+// Limit of every bounded wait in the kernels, in nanoseconds: FLCE_TIMEOUT_NS
+// from the environment (read once), else 4 s.
+uint64_t timeout_ns();
 
 int tc_smem_bytes();
 int tc_topk_subranges();  // vocabulary sub-ranges the top-k launch reports per range

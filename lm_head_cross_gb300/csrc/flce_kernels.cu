@@ -1587,6 +1587,109 @@ __global__ void convert_bf16_kernel(const float* __restrict__ src, __nv_bfloat16
   }
 }
 
+// fp32 -> bf16 of `count` values: 8 per thread-iteration through 16-byte
+// accesses, then the tail of fewer than 8 one by one.
+__global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16* __restrict__ dst, int64_t count) {
+  griddep_begin();
+  const int64_t count8 = count / 8;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  const int64_t tid = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x;
+  for (int64_t i = tid; i < count8; i += stride) {
+    const float4 a = reinterpret_cast<const float4*>(src)[2 * i];
+    const float4 b = reinterpret_cast<const float4*>(src)[2 * i + 1];
+    reinterpret_cast<uint4*>(dst)[i] =
+        make_uint4(pack_bf16x2(a.x, a.y), pack_bf16x2(a.z, a.w), pack_bf16x2(b.x, b.y), pack_bf16x2(b.z, b.w));
+  }
+  for (int64_t i = 8 * count8 + tid; i < count; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
+}
+
+// ----------------------------------------------------------------------------- vocabulary shards
+// ("What-Each-Parallelism-Actually-Shards" §7.2: each rank covers one range of the
+// vocabulary; ranks without the label still take part in the global max and
+// sum-exp; the loss takes the target logit from the rank that holds it; the
+// backward forms the local part of the logits gradient.)
+
+// Shard-local labels (see kNotOwned): one thread per row, the global label read
+// through the view (shift included), checked against the whole vocabulary.
+__global__ void shard_labels_kernel(int n, int64_t v_total, int64_t v0, int64_t vs, LabelView lv,
+                                    int32_t* __restrict__ lab_local, int* __restrict__ status) {
+  griddep_begin();
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+  int out = -1;
+  if (y != lv.ignore_index) {
+    if (y >= 0 && y < v_total)
+      out = (y >= v0 && y - v0 < vs) ? static_cast<int>(y - v0) : kNotOwned;
+    else
+      atomicCAS(status, 0, kErrLabel);
+  }
+  lab_local[row] = out;
+}
+
+__global__ void __launch_bounds__(kFinalizeThreads) shard_finalize_kernel(
+    int n, int vsplit, const float* __restrict__ part_m, const float* __restrict__ part_l,
+    const float* __restrict__ tgt, const int32_t* __restrict__ lab_local, float* __restrict__ lse_part,
+    float* __restrict__ tgt_part) {
+  griddep_begin();
+  const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  if (row >= n) return;
+  float m;
+  lse_part[row] = merge_ranges(part_m, part_l, vsplit, n, row, &m) * kLn2;
+  const int y = lab_local[row];
+  tgt_part[row] = (y >= 0 && y != kNotOwned) ? tgt[row] : 0.f;
+}
+
+// Combine the shards' per-row (lse, target logit) pairs, parts in index order
+// (every rank that runs it on the same gathered parts gets the same bits), then
+// the loss rows and the block partials of the fixed-order loss reduction.
+__global__ void __launch_bounds__(kFinalizeThreads) shard_combine_kernel(
+    int n, int parts, int64_t v_total, LabelView lv, const float* __restrict__ lse_parts,
+    const float* __restrict__ tgt_parts, float* __restrict__ lse_out, float* __restrict__ loss_rows,
+    double* __restrict__ blk_loss, int* __restrict__ blk_valid, int* __restrict__ status) {
+  griddep_begin();
+  __shared__ double s_loss[kFinalizeThreads];
+  __shared__ int s_valid[kFinalizeThreads];
+  const int row = blockIdx.x * kFinalizeThreads + threadIdx.x;
+  double li = 0.0;
+  int valid = 0;
+  if (row < n) {
+    float m = -INFINITY;
+    for (int r = 0; r < parts; ++r) m = fmaxf(m, lse_parts[static_cast<int64_t>(r) * n + row]);
+    float l = 0.f, z = 0.f;
+    for (int r = 0; r < parts; ++r) {
+      l += exp2f((lse_parts[static_cast<int64_t>(r) * n + row] - m) * kLog2e);
+      z += tgt_parts[static_cast<int64_t>(r) * n + row];
+    }
+    const float lse = m + log2f(l) * kLn2;
+    lse_out[row] = lse;
+    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, lv.ignore_index);
+    if (y != lv.ignore_index) {
+      if (y >= 0 && y < v_total) {
+        valid = 1;
+        li = static_cast<double>(lse) - static_cast<double>(z);
+      } else {
+        atomicCAS(status, 0, kErrLabel);
+      }
+    }
+    if (loss_rows) loss_rows[row] = static_cast<float>(li);
+  }
+  s_loss[threadIdx.x] = li;
+  s_valid[threadIdx.x] = valid;
+  __syncthreads();
+  for (int w = kFinalizeThreads / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) {
+      s_loss[threadIdx.x] += s_loss[threadIdx.x + w];
+      s_valid[threadIdx.x] += s_valid[threadIdx.x + w];
+    }
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    blk_loss[blockIdx.x] = s_loss[0];
+    blk_valid[blockIdx.x] = s_valid[0];
+  }
+}
+
 // x *= g for bf16 data (8 elements per thread-iteration), g a device scalar.
 __global__ void scale_bf16_kernel(__nv_bfloat16* __restrict__ x, int64_t count8, const float* __restrict__ g) {
   griddep_begin();
@@ -1728,6 +1831,36 @@ cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cuda
   if (blocks < 1) blocks = 1;
   return launch_k(convert_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream, src,
                   static_cast<__nv_bfloat16*>(dst), count8);
+}
+
+cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream) {
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (count / 8 + 255) / 256;
+  if (blocks > 8LL * sms) blocks = 8LL * sms;
+  if (blocks < 1) blocks = 1;
+  return launch_k(f32_to_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream, src,
+                  static_cast<__nv_bfloat16*>(dst), count);
+}
+
+cudaError_t launch_shard_labels(int n, int64_t v_total, int64_t v0, int64_t vs, LabelView lv, int32_t* lab_local,
+                                int* status, cudaStream_t stream) {
+  return launch_k(shard_labels_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, n, v_total, v0, vs, lv,
+                  lab_local, status);
+}
+
+cudaError_t launch_shard_finalize(int n, int vsplit, const float* part_m, const float* part_l, const float* tgt,
+                                  const int32_t* lab_local, float* lse_part, float* tgt_part, cudaStream_t stream) {
+  return launch_k(shard_finalize_kernel, dim3((n + kFinalizeThreads - 1) / kFinalizeThreads), dim3(kFinalizeThreads),
+                  0, stream, n, vsplit, part_m, part_l, tgt, lab_local, lse_part, tgt_part);
+}
+
+cudaError_t launch_shard_combine(int n, int parts, int64_t v_total, LabelView lv, const float* lse_parts,
+                                 const float* tgt_parts, float* lse, float* loss_rows, double* blk_loss,
+                                 int* blk_valid, int* status, cudaStream_t stream) {
+  return launch_k(shard_combine_kernel, dim3((n + kFinalizeThreads - 1) / kFinalizeThreads), dim3(kFinalizeThreads),
+                  0, stream, n, parts, v_total, lv, lse_parts, tgt_parts, lse, loss_rows, blk_loss, blk_valid, status);
 }
 
 cudaError_t launch_topk_finalize(int n, int nsub, int k, const float* part_m, const float* part_l,

@@ -45,7 +45,10 @@ static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 std::mutex g_mu;
 void* g_scratch_dev[kMaxDevices] = {};
 
-// Device address of g_scratch on the current device, looked up once per device.
+// Device address of g_scratch on the current device, looked up once per device
+// and kept for the life of the process.  A device reset (cudaDeviceReset, or a
+// reset of the primary context) reloads the module elsewhere, so this entry
+// point must not be called on a device after it has been reset.
 flce_status_t scratch_address(void** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return FLCE_ERR_CUDA;
@@ -86,9 +89,12 @@ bool map_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, ui
 }
 
 // After the loss is reduced: if a label was out of range (or a wait timed out),
-// the loss is set to NaN, so the error is visible without a workspace to read.
-__global__ void poison_loss_on_error(const int* status, float* loss) {
-  if (threadIdx.x == 0 && *status != 0) *loss = __int_as_float(0x7fc00000);
+// every loss value — the scalar, or each of the n per-row losses — is set to
+// NaN, so the error is visible without a workspace to read.
+__global__ void poison_loss_on_error(const int* status, float* loss, int count) {
+  if (*status == 0) return;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < count; i += gridDim.x * blockDim.x)
+    loss[i] = __int_as_float(0x7fc00000);
 }
 
 bool aligned_to(const void* p, size_t a) { return reinterpret_cast<uintptr_t>(p) % a == 0; }
@@ -144,7 +150,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.h = static_cast<int>(p->h);
   tp.v = static_cast<int>(p->v);
   tp.ignore_index = p->ignore_index;
-  tp.timeout_ns = 4000000000ull;
+  tp.timeout_ns = timeout_ns();
   tp.status = status;
   tp.row_tiles = static_cast<int>((p->n + kPairRows - 1) / kPairRows);
   tp.vocab_tiles = static_cast<int>((p->v + kBN - 1) / kBN);
@@ -172,6 +178,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   if (launch_reduce_final(nblk, blk_loss, blk_valid, p->reduction, nullptr, per_row ? nullptr : loss, n_valid, scale,
                           cs) != cudaSuccess)
     return FLCE_ERR_CUDA;
-  poison_loss_on_error<<<1, 32, 0, cs>>>(status, loss);
+  const int nloss = per_row ? tp.n : 1;
+  poison_loss_on_error<<<std::min(64, (nloss + 255) / 256), 256, 0, cs>>>(status, loss, nloss);
   return cudaGetLastError() == cudaSuccess ? FLCE_OK : FLCE_ERR_CUDA;
 }

@@ -15,9 +15,12 @@ int main(void) {
   p.ignore_index = -100;
   p.reduction = FLCE_REDUCTION_MEAN;
   size_t full = flce_workspace_bytes(&p);
-  size_t min = flce_workspace_bytes_min(&p);
-  if (full == 0 || min == 0 || full < min) {
-    printf("bad workspace sizes %zu %zu\n", full, min);
+  size_t rowchunk = flce_workspace_bytes_rowchunk(&p);
+  p.v = 4 * 32000;
+  size_t full_wide = flce_workspace_bytes(&p);
+  p.v = 32000;
+  if (full == 0 || rowchunk == 0 || full != full_wide) {
+    printf("bad workspace sizes %zu %zu %zu\n", full, rowchunk, full_wide);
     return 1;
   }
   p.h = 12; /* not a multiple of 8 */
@@ -36,6 +39,6 @@ int main(void) {
     printf("empty status string\n");
     return 1;
   }
-  printf("ok %zu %zu\n", full, min);
+  printf("ok %zu %zu\n", full, rowchunk);
   return 0;
 }

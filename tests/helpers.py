@@ -32,3 +32,16 @@ def assert_grad(got, want, frac=GRAD_FRAC, name="grad"):
     scale = np.abs(want).max()
     err = np.abs(got - want).max()
     assert err <= frac * scale, f"{name} max abs err {err} > {frac} x max|ref| {scale}"
+
+
+def golden_forward(name, problem=None):
+    """The oracle's stored full-forward results of a large workload (per-row lse,
+    loss, n_valid), written by tests/golden/make_workload_golden.py; checked
+    against the problem's input bytes when it is given."""
+    import importlib.util
+    import os
+    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "make_workload_golden.py")
+    spec = importlib.util.spec_from_file_location("make_workload_golden", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    return mod.load(name, problem)

@@ -25,8 +25,8 @@ def run(problem, **kw):
                 dW=dW.float().cpu().numpy(), status=st)
 
 
-def check_full(problem, minimal_workspace=False):
-    got = run(problem, minimal_workspace=minimal_workspace)
+def check_full(problem, rowchunk=False):
+    got = run(problem, rowchunk=rowchunk)
     assert got["status"] == 0, flce.status_string(got["status"])
     ref = oracle.full_bf16(problem)
     assert_loss(got["loss"], ref["loss"])
@@ -38,12 +38,14 @@ def check_full(problem, minimal_workspace=False):
     return got, ref
 
 
-PATHS = pytest.mark.parametrize("minimal", [False, True], ids=["fused", "recompute"])
+# the bounded path (flce_fwd_bwd: logits recomputed, V-independent workspace) and the
+# row-chunk path (flce_fwd_bwd_rowchunk: logits computed once, a row chunk kept)
+PATHS = pytest.mark.parametrize("rowchunk", [False, True], ids=["bounded", "rowchunk"])
 
 
 @PATHS
-def test_tiny_workload_full(minimal):
-    check_full(synth.workload_problem(synth.TINY), minimal)
+def test_tiny_workload_full(rowchunk):
+    check_full(synth.workload_problem(synth.TINY), rowchunk)
 
 
 @pytest.mark.parametrize("n,h,v,red,labels", [
@@ -56,23 +58,23 @@ def test_tiny_workload_full(minimal):
     (1500, 128, 4001, "mean", "zipf"),        # fused path: two row chunks, the last one ragged; odd V
 ])
 @PATHS
-def test_ragged_shapes(n, h, v, red, labels, minimal):
+def test_ragged_shapes(n, h, v, red, labels, rowchunk):
     p = synth.make_problem(n, h, v, seed=n + h + v, labels=labels, ignore_frac=0.1, reduction=red,
                            w_std=0.05)
-    check_full(p, minimal)
+    check_full(p, rowchunk)
 
 
 @PATHS
-def test_outlier_rows_sum_reduction(minimal):
+def test_outlier_rows_sum_reduction(rowchunk):
     p = synth.make_problem(512, 256, 3000, seed=44, labels="zipf", ignore_frac=0.05, reduction="sum",
                            outlier_rows=16, outlier_scale=10.0)
-    check_full(p, minimal)
+    check_full(p, rowchunk)
 
 
 def test_fused_and_recompute_paths_agree():
     p = synth.make_problem(2048, 256, 6000, seed=45, labels="zipf", ignore_frac=0.05)
-    a = run(p)
-    b = run(p, minimal_workspace=True)
+    a = run(p, rowchunk=True)
+    b = run(p)
     assert abs(a["loss"] - b["loss"]) <= 1e-4 * abs(b["loss"])
     assert np.abs(a["lse"] - b["lse"]).max() <= 1e-4
     assert_grad(a["dX"], b["dX"], frac=1e-2, name="dX")
@@ -80,9 +82,9 @@ def test_fused_and_recompute_paths_agree():
 
 
 @PATHS
-def test_all_rows_ignored_mean_gives_zero(minimal):
+def test_all_rows_ignored_mean_gives_zero(rowchunk):
     p = synth.make_problem(200, 64, 500, seed=3, ignore_frac=1.0, reduction="mean")
-    got = run(p, minimal_workspace=minimal)
+    got = run(p, rowchunk=rowchunk)
     assert got["status"] == 0
     assert got["loss"] == 0.0
     assert np.all(got["dX"] == 0) and np.all(got["dW"] == 0)
@@ -91,11 +93,11 @@ def test_all_rows_ignored_mean_gives_zero(minimal):
 
 
 @PATHS
-def test_w_zero_closed_form(minimal):
+def test_w_zero_closed_form(rowchunk):
     """W = 0: loss = ln V exactly in the definition; dX = 0; dW from its closed form."""
     p = synth.make_problem(384, 128, 3000, seed=5, ignore_frac=0.1)
     p.W[:] = 0
-    got = run(p, minimal_workspace=minimal)
+    got = run(p, rowchunk=rowchunk)
     assert abs(got["loss"] - math.log(3000)) <= 1e-3 * math.log(3000)
     assert np.all(got["dX"] == 0)
     X = oracle.widen_bf16(p.X)
@@ -108,19 +110,19 @@ def test_w_zero_closed_form(minimal):
 
 
 @PATHS
-def test_equal_rows_give_zero_dx_and_log_v(minimal):
+def test_equal_rows_give_zero_dx_and_log_v(rowchunk):
     p = synth.make_problem(256, 128, 700, seed=6, ignore_frac=0.0)
     p.W[:] = p.W[3]
-    got = run(p, minimal_workspace=minimal)
+    got = run(p, rowchunk=rowchunk)
     assert abs(got["loss"] - math.log(700)) <= 1e-3 * math.log(700)
     # every softmax row is uniform: dX_i = s (mean_j W_j - W_{y_i}) = 0
     assert np.abs(got["dX"]).max() <= 1e-6
 
 
 @PATHS
-def test_dw_vocab_sum_is_zero(minimal):
+def test_dw_vocab_sum_is_zero(rowchunk):
     p = synth.make_problem(512, 256, 5000, seed=8, ignore_frac=0.05, reduction="sum")
-    got = run(p, minimal_workspace=minimal)
+    got = run(p, rowchunk=rowchunk)
     dW = got["dW"]
     # each row of G sums to zero, so the vocabulary sum of dW vanishes up to bf16 rounding of dW
     resid = np.abs(dW.astype(np.float64).sum(axis=0)).max()
@@ -176,10 +178,10 @@ def test_autograd_wrapper(upstream):
 
 
 @PATHS
-def test_repeat_calls_are_deterministic(minimal):
+def test_repeat_calls_are_deterministic(rowchunk):
     p = synth.make_problem(512, 256, 9000, seed=13, ignore_frac=0.05)
-    a = run(p, minimal_workspace=minimal)
-    b = run(p, minimal_workspace=minimal)
+    a = run(p, rowchunk=rowchunk)
+    b = run(p, rowchunk=rowchunk)
     assert a["loss"] == b["loss"]
     assert np.array_equal(a["lse"], b["lse"])
     assert np.array_equal(a["dW"], b["dW"])
@@ -198,11 +200,11 @@ def test_timeout_path_returns_status():
 
 
 @PATHS
-def test_reduction_none_fwd_bwd(minimal):
+def test_reduction_none_fwd_bwd(rowchunk):
     """Per-row losses; the fused call's gradients are those of their sum."""
     p = synth.make_problem(600, 128, 3000, seed=61, labels="zipf", ignore_frac=0.1, reduction="none")
     X, W, y = to_device(p)
-    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, "none", minimal_workspace=minimal)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, "none", rowchunk=rowchunk)
     assert flce.read_device_status(ws) == 0
     ref = oracle.full_bf16(p)
     rows = loss.cpu().numpy()
@@ -228,12 +230,12 @@ def test_reduction_none_backward_per_row_gradients():
 
 @PATHS
 @pytest.mark.parametrize("red", ["mean", "sum"])
-def test_shift_one(minimal, red):
+def test_shift_one(rowchunk, red):
     """Causal next-token shift inside the kernels: row i is scored against labels[i + 1]."""
     B, S = 3, 200
     p = synth.make_problem(B * S, 128, 2500, seed=63, labels="zipf", ignore_frac=0.05, reduction=red)
     X, W, y = to_device(p)
-    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, minimal_workspace=minimal, shift=1, seq_len=S)
+    loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, rowchunk=rowchunk, shift=1, seq_len=S)
     assert flce.read_device_status(ws) == 0
     shifted = oracle.shift_labels(p.labels, S, p.ignore_index)
     ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), shifted, p.ignore_index, red)
@@ -262,7 +264,8 @@ def test_autograd_none_and_shift():
 
 
 @pytest.mark.parametrize("red", ["mean", "sum"])
-def test_wide_logit_range_rows(red):
+@PATHS
+def test_wide_logit_range_rows(red, rowchunk):
     """Rows whose target logit lies far below the row's max (some tiles, or the
     whole row, stored relative to the tiles' own maxima) next to ordinary rows,
     over two row chunks.  The ordinary rows' dX is checked against its own
@@ -273,7 +276,7 @@ def test_wide_logit_range_rows(red):
     group = np.arange(p.n) % 3           # 0: x1, 1: x16, 2: x64 (powers of two: exact in bf16)
     xf = xf * np.array([1.0, 16.0, 64.0], np.float32)[group][:, None]
     p.X = synth.f32_to_bf16_bits(xf)
-    got, ref = check_full(p)
+    got, ref = check_full(p, rowchunk)
     for g in range(3):
         rows = group == g
         assert_grad(got["dX"][rows], ref["dX"][rows], name=f"dX rows x{[1, 16, 64][g]}")
@@ -408,12 +411,12 @@ def test_empty_batch(red):
 
 
 @PATHS
-def test_row_tile_groups_and_wide_hidden(minimal):
+def test_row_tile_groups_and_wide_hidden(rowchunk):
     """Forward launches whose row tiles span several unit groups (H = 4096: 24 row
     tiles of 256 per group, 28 here, the last group short), and a wide hidden size."""
     p = synth.make_problem(7000, 4096, 1500, seed=31, labels="zipf", ignore_frac=0.05, reduction="sum",
                            x_std=4.0 / 64.0)
-    check_full(p, minimal)
+    check_full(p, rowchunk)
     X, W, y = to_device(p)
     loss, lse, ws = flce.forward(X, W, y, p.ignore_index, p.reduction)
     assert flce.read_device_status(ws) == 0
@@ -421,7 +424,7 @@ def test_row_tile_groups_and_wide_hidden(minimal):
     assert_loss(float(loss.item()), f["loss"])
     assert_lse(lse.cpu().numpy(), f["lse"])
     q = synth.make_problem(600, 8192, 3000, seed=32, labels="uniform", ignore_frac=0.1, x_std=1.0 / 16)
-    check_full(q, minimal)
+    check_full(q, rowchunk)
 
 
 def test_random_shapes_and_options():
@@ -436,17 +439,17 @@ def test_random_shapes_and_options():
         v = int(rng.integers(1, 6000))
         red = ["mean", "sum", "none"][case % 3]
         shift = int(rng.integers(0, 2)) if s_len > 1 else 0
-        minimal = bool(rng.integers(0, 2))
+        rowchunk = bool(rng.integers(0, 2))
         p = synth.make_problem(n, h, v, seed=1000 + case, labels=["uniform", "zipf"][case % 2],
                                ignore_frac=float(rng.choice([0.0, 0.1, 0.5])), reduction=red,
                                x_std=float(rng.choice([0.25, 1.0, 4.0])), w_std=float(rng.choice([0.02, 0.1])))
         X, W, y = to_device(p)
-        loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, minimal_workspace=minimal, shift=shift,
+        loss, lse, dX, dW, ws = flce.fwd_bwd(X, W, y, p.ignore_index, red, rowchunk=rowchunk, shift=shift,
                                              seq_len=s_len if shift else 0)
         assert flce.read_device_status(ws) == 0, case
         labels = oracle.shift_labels(p.labels, s_len, p.ignore_index) if shift else p.labels
         ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), labels, p.ignore_index, red)
-        what = f"case {case}: n={n} h={h} v={v} {red} shift={shift} minimal={minimal}"
+        what = f"case {case}: n={n} h={h} v={v} {red} shift={shift} rowchunk={rowchunk}"
         got_loss = loss.cpu().numpy().astype(np.float64)
         if red == "none":
             np.testing.assert_allclose(got_loss, ref["loss"], rtol=1e-3, atol=2e-3, err_msg=what)
