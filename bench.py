@@ -3,12 +3,19 @@
 
 Metric: credited TFLOP/s counting 6*N*H*V per step (2NHV for the logits, 2NHV
 each for dX and dW), with the extra device memory the op needs beside it.
-A step is one flce_fwd_bwd over one synthetic batch (loss, lse, dX, dW).
+A step is one flce_fwd_bwd over one synthetic batch (loss, lse, dX, dW) on the
+bounded, V-independent workspace (logits recomputed in the backward pass:
+8NHV executed, 6NHV credited).
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload n8192_h2048_v32000] [--impl flce|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload n131072_h4096_v131072]
+                    [--path bounded|rowchunk] [--impl flce|reference]
 
-Default workload: N = 4 x 2048 = 8192 tokens, H = 2048, V = 32000, labels
-Zipf(1.1) with 5% ignore_index, mean reduction.
+Default workload: the 128K-token x 128K-vocabulary case (N = 131072, H = 4096,
+V = 131072, uniform labels with 3% ignore_index, mean reduction), whose bf16
+logits would take 32 GiB.  The line also carries the row-chunk path
+(flce_fwd_bwd_rowchunk, 6NHV executed, a workspace that grows with V) on the
+same inputs, and both paths on the three other benchmark workloads
+(``workloads``), each measured with the same timing discipline.
 Under torchrun each rank runs its own batch of that shape on its own GPU
 (weak scaling, no collective on the data path); rank 0 prints one JSON line.
 
@@ -37,28 +44,33 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_g
 L2_FLUSH_BYTES = 512 << 20
 
 
+HEADLINE = "n131072_h4096_v131072"
+OTHER_WORKLOADS = ("n8192_h2048_v32000", "n8192_h4096_v128256", "n32768_h4096_v151936")
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
-    ap.add_argument("--workload", default="n8192_h2048_v32000", help="one of synth.WORKLOADS")
+    ap.add_argument("--workload", default=HEADLINE, help="one of synth.WORKLOADS")
+    ap.add_argument("--path", choices=["bounded", "rowchunk"], default="bounded",
+                    help="bounded: flce_fwd_bwd, V-independent workspace (8NHV executed); rowchunk: "
+                         "flce_fwd_bwd_rowchunk, logits computed once (6NHV), workspace grows with V")
     ap.add_argument("--impl", choices=["flce", "reference"], default="flce")
-    ap.add_argument("--e2e-steps", type=int, default=30)
+    ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-naive", action="store_true", help="skip timing the unfused torch lm_head + cross_entropy")
+    ap.add_argument("--no-others", action="store_true",
+                    help="skip the other path and the other workloads (the 'rowchunk' and 'workloads' keys)")
+    ap.add_argument("--other-steps", type=int, default=10, help="timed steps of each other path / workload")
     ap.add_argument("--op", choices=["fwd_bwd", "topk", "soft"], default="fwd_bwd",
                     help="fwd_bwd: fused loss + gradients (the benchmark); topk: per-row top-k logits; "
                          "soft: KL against sparse soft targets, forward + backward")
     ap.add_argument("--k", type=int, default=8, help="k of --op topk / soft")
     ap.add_argument("--reduction", choices=["mean", "sum", "none"], default=None, help="override the workload's")
     ap.add_argument("--shift", type=int, default=0, help="1: causal next-token shift inside the kernels")
-    ap.add_argument("--workspace", choices=["full", "min"], default="full",
-                    help="min: flce_workspace_bytes_min, the recompute path (8NHV executed)")
-    ap.add_argument("--sustain", type=float, default=0.0,
-                    help="seconds of back-to-back calls (no L2 flush) after the timed region, reported as "
-                         "'sustained': the power-capped steady state of a long run")
     return ap.parse_args()
 
 
@@ -84,6 +96,12 @@ def workload_config(name, problem_kw, l2_note, world):
         "l2": l2_note,
         "parallelism": f"replicas x{world} (rows sharded by rank, no collective)" if world > 1 else "single GPU",
     }
+
+
+def arm_config(args, world):
+    """The `config` of the benchmark line, the same for both arms."""
+    return dict(workload_config(args.workload, None, f"inputs larger than L2, and a {L2_FLUSH_BYTES >> 20} MiB write "
+                                "between steps (outside the per-step events)", world), path=args.path)
 
 
 def credited_flops(n, h, v):
@@ -112,23 +130,21 @@ def job_tflops(world, flops_per_rank_step, steps, max_ms):
 
 # ----------------------------------------------------------------------------- CPU oracle timing
 
-def oracle_sample_seconds(problem, rows):
-    """Time the fp64 oracle (loss, lse, dX, dW) on the first `rows` rows with the full W."""
-    import numpy as np
+def oracle_sample_seconds(problem, rows, Wd=None):
+    """Time the fp64 oracle (loss, lse, dX, dW) on the first `rows` rows with the full W
+    (``Wd``: W already widened to fp64, to reuse across samples)."""
     import oracle
     X = oracle.widen_bf16(problem.X[:rows])
-    W = oracle.widen_bf16(problem.W)
+    W = oracle.widen_bf16(problem.W) if Wd is None else Wd
     lab = problem.labels[:rows]
     t0 = time.perf_counter()
     oracle.full(X, W, lab, problem.ignore_index, problem.reduction)
-    dt = time.perf_counter() - t0
-    del X, W, np
-    return dt
+    return time.perf_counter() - t0
 
 
-def calibrate_rows(problem, target_s, max_rows):
+def calibrate_rows(problem, target_s, max_rows, Wd=None):
     r = min(64, max_rows)
-    dt = oracle_sample_seconds(problem, r)
+    dt = oracle_sample_seconds(problem, r, Wd)
     per_row = dt / r
     return int(max(1, min(max_rows, target_s / max(per_row, 1e-9))))
 
@@ -189,8 +205,10 @@ def torch_naive(X, W, y, problem, flush, stream, torch, steps=5):
 
 
 def cpu_baseline(problem, target_s):
-    rows = calibrate_rows(problem, target_s, problem.n)
-    dt = oracle_sample_seconds(problem, rows)
+    import oracle
+    Wd = oracle.widen_bf16(problem.W)
+    rows = calibrate_rows(problem, target_s, problem.n, Wd)
+    dt = oracle_sample_seconds(problem, rows, Wd)
     val = credited_flops(rows, problem.h, problem.v) / dt / 1e12
     return {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
             "sample": f"fp64 numpy oracle (loss, lse, dX, dW) on the first {rows} of {problem.n} rows with the full "
@@ -200,21 +218,23 @@ def cpu_baseline(problem, target_s):
 def run_reference(args, rank, world):
     if rank != 0:
         return 0
+    import oracle
     import synth
     problem = synth.workload_problem(args.workload)
+    Wd = oracle.widen_bf16(problem.W)
     total_steps = args.steps + args.warmup
-    per_step_s = max(0.5, min(10.0, 150.0 / max(1, total_steps)))
-    rows = calibrate_rows(problem, per_step_s, problem.n)
+    per_step_s = max(0.5, min(10.0, 120.0 / max(1, total_steps)))
+    rows = calibrate_rows(problem, per_step_s, problem.n, Wd)
     for _ in range(args.warmup):
-        oracle_sample_seconds(problem, rows)
-    times = [oracle_sample_seconds(problem, rows) for _ in range(args.steps)]
+        oracle_sample_seconds(problem, rows, Wd)
+    times = [oracle_sample_seconds(problem, rows, Wd) for _ in range(args.steps)]
     t = sum(times)
     val = credited_flops(rows, problem.h, problem.v) * args.steps / t / 1e12
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * t / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": workload_config(args.workload, None, "n/a (CPU)", world),
+        "config": arm_config(args, world),
         "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
                          "sample": f"each step: fp64 numpy oracle (loss, lse, dX, dW) on the first {rows} of "
                                    f"{problem.n} rows with the full W"},
@@ -227,9 +247,11 @@ def run_reference(args, rank, world):
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
+    """nvidia-smi samples of the SM clock, throttle reasons and power every 20 ms,
+    kept only when their timestamp falls inside the marked (timed) region."""
     # power.draw.instant: the power-capping decisions follow the instantaneous draw, which on
     # a heavy tensor-core load passes the limit within ~100 ms while the averaged draw lags
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,power.draw.instant")
     PERIOD_MS = 20
@@ -246,6 +268,7 @@ class ClockSampler:
             pass
         self.proc = None
         self.path = None
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
@@ -257,6 +280,20 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def mark_start(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
+
+    @staticmethod
+    def _when(stamp):
+        import datetime
+        try:
+            return datetime.datetime.strptime(stamp.strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            return None
+
     def stop(self):
         if self.proc is None:
             return None
@@ -265,23 +302,31 @@ class ClockSampler:
             self.proc.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.proc.kill()
-        rows = []
+        rows, total = [], 0
         with open(self.path) as f:
             for line in f:
                 parts = [p.strip() for p in line.split(",")]
-                if len(parts) >= 10:
-                    rows.append(parts)
+                if len(parts) < 11:
+                    continue
+                total += 1
+                when = self._when(parts[0])
+                if self.t0 is not None and (when is None or when < self.t0 or (self.t1 and when > self.t1)):
+                    continue
+                rows.append(parts[1:])
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples in the timed region"], "samples": 0,
+                    "samples_total": total}
+        num = lambda x: x.replace(".", "").isdigit()  # noqa: E731
+        sm = [float(r[1]) for r in rows if num(r[1])]
+        smax = [float(r[2]) for r in rows if num(r[2])]
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         reasons = sorted({names[k] for r in rows for k in range(4) if r[5 + k].lower().startswith("active")})
-        power = [float(r[9]) for r in rows if r[9].replace(".", "").isdigit()]
+        power = [float(r[9]) for r in rows if num(r[9])]
         capped = sum(1 for r in rows if r[8].lower().startswith("active"))
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
                 "sm_mhz_min": min(sm) if sm else None, "reasons": reasons, "samples": len(rows),
+                "samples_total": total, "window": "samples timestamped inside the timed region only",
                 "sample_period_ms": self.PERIOD_MS, "power_cap_frac": capped / len(rows),
                 "power_w_instant_median": statistics.median(power) if power else None,
                 "power_w_instant_max": max(power) if power else None}
@@ -289,50 +334,129 @@ class ClockSampler:
 
 # ----------------------------------------------------------------------------- the CUDA arm
 
-def sustained_run(step, flops, seconds, gpu_index, torch):
-    """Back-to-back steps (no L2 flush) for about `seconds` after a quarter of that
-    as warm-up into the power cap: the steady state a long run settles into."""
-    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    a.record(); step(); b.record(); torch.cuda.synchronize()
-    reps = max(3, int(seconds * 1e3 / max(a.elapsed_time(b), 1e-3)))
-    for _ in range(max(1, reps // 4)):
-        step()
-    torch.cuda.synchronize()
-    clocks = ClockSampler(gpu_index)
-    clocks.start()
-    a.record()
-    for _ in range(reps):
-        step()
-    b.record()
-    torch.cuda.synchronize()
-    clk = clocks.stop() or {}
-    ms = a.elapsed_time(b) / reps
-    tf = flops / (ms / 1e3) / 1e12
-    mhz = clk.get("sm_mhz")
-    return {"value": tf, "unit": UNIT, "ms_per_step": ms, "steps": reps, "sm_mhz": mhz,
-            "tflops_per_ghz": tf / (mhz / 1e3) if mhz else None,
-            "power_w_instant_median": clk.get("power_w_instant_median"), "reasons": clk.get("reasons")}
-
-
-def traffic_record(kind, workload):
-    """DRAM bytes per launch of `kind` from a committed ncu capture, if it was taken
-    on the kernel source as it is now (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def traffic_record(kind, workload, path):
+    """DRAM bytes per launch of `kind` on `path` from a committed ncu capture, if it was
+    taken on the kernel source as it is now (else None)."""
+    rec = os.path.join(ROOT, "profiles", "traffic.json")
     try:
-        with open(path) as f:
+        with open(rec) as f:
             recs = json.load(f)
     except (OSError, ValueError):
         return None
     src = os.path.join(ROOT, "lm_head_cross_gb300", "csrc", "flce_kernels.cu")
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     for r in recs:
-        if r.get("kind") == kind and r.get("workload") == workload and r.get("kernel_sha") == sha:
+        if (r.get("kind") == kind and r.get("workload") == workload and r.get("path", "rowchunk") == path
+                and r.get("kernel_sha") == sha):
             return float(r["bytes_per_launch"])
     return None
 
 
-def run_flce(args, rank, world, local_rank):
+def device_problem(name, rank, dev):
     import numpy as np
+    import torch
+    import synth
+    c = dict(synth.WORKLOADS[name])
+    c["seed"] = rank_seed(c["seed"], rank)
+    problem = synth.make_problem(**c)
+    X = torch.from_numpy(problem.X.view(np.int16)).view(torch.bfloat16).to(dev)
+    W = torch.from_numpy(problem.W.view(np.int16)).view(torch.bfloat16).to(dev)
+    y = torch.from_numpy(problem.labels).to(dev)
+    return problem, X, W, y
+
+
+def ws_bytes_of(flce, rowchunk, problem, reduction=None):
+    f = flce.workspace_bytes_rowchunk if rowchunk else flce.workspace_bytes
+    return f(problem.n, problem.h, problem.v, problem.ignore_index, reduction or problem.reduction)
+
+
+def extra_memory(flce, torch, dev, X, W, y, problem, rowchunk):
+    """Device memory one call allocates beyond its inputs and outputs (the torch allocator's
+    peak delta), next to the workspace size the library asks for; fails on a device error."""
+    torch.cuda.synchronize()
+    base = torch.cuda.memory_allocated(dev)
+    torch.cuda.reset_peak_memory_stats(dev)
+    tmp = flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction, rowchunk=rowchunk)
+    torch.cuda.synchronize()
+    out_bytes = sum(t.numel() * t.element_size() for t in tmp[:4])
+    peak = torch.cuda.max_memory_allocated(dev) - base - out_bytes
+    st = flce.read_device_status(tmp[4])
+    del tmp
+    if st != 0:
+        raise RuntimeError(f"device status {flce.status_string(st)}")
+    return int(peak)
+
+
+def timed_steps(step, steps, warmup, flush, stream, torch, flce, clocks=None, dist=None):
+    """W >= 3 untimed steps, then K steps each bracketed by CUDA events on the launching
+    stream, a 512 MiB write between steps (outside the events) to evict L2; the dominant
+    kernel kind is timed live by the library's own events around its launches."""
+    for _ in range(max(3, warmup)):
+        step()
+    torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    for e in starts + ends:      # create the driver events now, not inside the timed loop
+        e.record(stream)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    flce.profile_enable(True, kinds=["dxdw"])   # the dominant kernel only: events elsewhere would serialise launches
+    if clocks is not None:
+        clocks.mark_start()
+    t_wall0 = time.perf_counter()
+    for i in range(steps):
+        flush.fill_(i & 0xFF)
+        starts[i].record(stream)
+        step()
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    if clocks is not None:
+        clocks.mark_end()
+    if dist is not None:
+        dist.barrier()
+    dom = flce.profile_read()["dxdw"]
+    flce.profile_enable(False)
+    return {"step_ms": [a.elapsed_time(b) for a, b in zip(starts, ends)], "dom": dom, "wall_s": t_wall}
+
+
+def dominant_tflops(dom):
+    n_l, ms_l, fl_l = dom
+    return (fl_l / n_l) / ((ms_l / n_l) / 1e3) / 1e12 if n_l and ms_l else None
+
+
+def measure_path(flce, torch, dev, problem, X, W, y, rowchunk, steps, warmup, flush, stream, naive=False):
+    """One (workload, path) measured with the headline's timing discipline: credited and
+    executed TFLOP/s, the dominant kernel's rate, extra device memory."""
+    wsb = ws_bytes_of(flce, rowchunk, problem)
+    peak = extra_memory(flce, torch, dev, X, W, y, problem, rowchunk)
+    ws = torch.empty(wsb, dtype=torch.uint8, device=dev)
+    out = (torch.empty(1, dtype=torch.float32, device=dev), torch.empty(problem.n, dtype=torch.float32, device=dev),
+           torch.empty_like(X), torch.empty_like(W))
+
+    def step():
+        flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction, ws=ws, out=out, rowchunk=rowchunk)
+
+    r = timed_steps(step, steps, warmup, flush, stream, torch, flce)
+    st = flce.read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {flce.status_string(st)}")
+    ms = sum(r["step_ms"]) / steps
+    n, h, v = problem.n, problem.h, problem.v
+    res = {"path": "rowchunk (6NHV executed)" if rowchunk else "bounded (8NHV executed)",
+           "value": credited_flops(n, h, v) / (ms / 1e3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+           "executed_tflops": (6.0 if rowchunk else 8.0) * n * h * v / (ms / 1e3) / 1e12,
+           "dominant_kernel_tflops": dominant_tflops(r["dom"]), "extra_hbm_bytes": wsb,
+           "peak_alloc_delta_bytes": peak}
+    del ws, out
+    if naive:
+        res["torch_naive"] = torch_naive(X, W, y, problem, flush, stream, torch)
+    return res
+
+
+def run_flce(args, rank, world, local_rank):
     import torch
     import lm_head_cross_gb300 as flce
     import synth
@@ -344,29 +468,23 @@ def run_flce(args, rank, world, local_rank):
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
 
-    c = dict(synth.WORKLOADS[args.workload])
-    c["seed"] = rank_seed(c["seed"], rank)
-    problem = synth.make_problem(**c)
+    problem, X, W, y = device_problem(args.workload, rank, dev)
     n, h, v = problem.n, problem.h, problem.v
-    X = torch.from_numpy(problem.X.view(np.int16)).view(torch.bfloat16).to(dev)
-    W = torch.from_numpy(problem.W.view(np.int16)).view(torch.bfloat16).to(dev)
-    y = torch.from_numpy(problem.labels).to(dev)
-    ws_bytes = (flce.workspace_bytes_min if args.workspace == "min" else flce.workspace_bytes)(
-        n, h, v, problem.ignore_index, problem.reduction)
-    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
-    out = (torch.empty(1, dtype=torch.float32, device=dev), torch.empty(n, dtype=torch.float32, device=dev),
-           torch.empty_like(X), torch.empty_like(W))
+    rowchunk = args.path == "rowchunk"
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
-
     reduction = args.reduction or problem.reduction
+    ws_bytes = ws_bytes_of(flce, rowchunk or args.op == "soft", problem, reduction)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    out = (torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=dev),
+           torch.empty(n, dtype=torch.float32, device=dev), torch.empty_like(X), torch.empty_like(W))
+
     if args.op == "fwd_bwd":
-        if reduction == "none":
-            out = (torch.empty(n, dtype=torch.float32, device=dev),) + out[1:]
         seq = n if args.shift else 0
 
         def step():
-            flce.fwd_bwd(X, W, y, problem.ignore_index, reduction, ws=ws, out=out, shift=args.shift, seq_len=seq)
+            flce.fwd_bwd(X, W, y, problem.ignore_index, reduction, ws=ws, out=out, shift=args.shift, seq_len=seq,
+                         rowchunk=rowchunk)
     elif args.op == "topk":
         tk_ws = torch.empty(flce.topk_workspace_bytes(n, h, v, args.k), dtype=torch.uint8, device=dev)
 
@@ -381,61 +499,34 @@ def run_flce(args, rank, world, local_rank):
         def step():
             flce.soft_fwd_bwd(X, W, sidx, sq, reduction, ws=ws)
 
-    # extra device memory of one call beyond its inputs and outputs
-    torch.cuda.synchronize()
-    base = torch.cuda.memory_allocated(dev)
-    torch.cuda.reset_peak_memory_stats(dev)
-    tmp_out = flce.fwd_bwd(X, W, y, problem.ignore_index, problem.reduction)
-    torch.cuda.synchronize()
-    out_bytes = sum(t.numel() * t.element_size() for t in tmp_out[:4])
-    peak_delta = torch.cuda.max_memory_allocated(dev) - base - out_bytes
-    st = flce.read_device_status(tmp_out[4])
-    del tmp_out
-    if st != 0:
-        raise RuntimeError(f"device status {flce.status_string(st)}")
     if args.op != "fwd_bwd" or args.reduction or args.shift:
         return run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, stream)
 
-    for _ in range(max(3, args.warmup)):
-        step()
-    torch.cuda.synchronize()
+    # extra device memory of one call beyond its inputs and outputs: exactly the workspace
+    peak_delta = extra_memory(flce, torch, dev, X, W, y, problem, rowchunk)
+    if not ws_bytes <= peak_delta <= ws_bytes + 4096:   # the allocator rounds each output up to 512 bytes
+        raise RuntimeError(f"allocation beyond the workspace: peak delta {peak_delta} vs workspace {ws_bytes}")
+    if args.workload == HEADLINE and not rowchunk and ws_bytes >= 4e9:
+        raise RuntimeError(f"workspace of the 128K x 128K workload is {ws_bytes} bytes, not under 4 GB")
 
-    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    for e in starts + ends:      # create the driver events now, not inside the timed loop
-        e.record(stream)
-    torch.cuda.synchronize()
     clocks = ClockSampler(local_rank)
-    if dist is not None:
-        dist.barrier()
-    torch.cuda.synchronize()
-    flce.profile_enable(True, kinds=["dxdw"])   # the dominant kernel only: events elsewhere would serialise launches
     clocks.start()
-    time.sleep(0.25)  # let the sampler take its first reading
-    t_wall0 = time.perf_counter()
-    for i in range(args.steps):
-        flush.fill_(i & 0xFF)                  # evict inputs from the 126 MB L2 between steps
-        starts[i].record(stream)
-        step()
-        ends[i].record(stream)
-    torch.cuda.synchronize()
-    t_wall = time.perf_counter() - t_wall0
-    if dist is not None:
-        dist.barrier()
-    clk = clocks.stop()
-    prof_dom = flce.profile_read()
-    flce.profile_enable(False)
-    prof, per_step = kernel_breakdown(flce, torch, step, flush, min(args.steps, 10))
-    step_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    r = timed_steps(step, args.steps, args.warmup, flush, stream, torch, flce, clocks=clocks, dist=dist)
+    clk = clocks.stop() or {"reasons": ["no sampler"], "samples": 0}
+    st = flce.read_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {flce.status_string(st)}")
+    prof, per_step = kernel_breakdown(flce, torch, step, flush, min(args.steps, 5))
+    step_ms = r["step_ms"]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     ms_per_step = total_ms / args.steps
     flops = credited_flops(n, h, v)
     value = job_tflops(world, flops, args.steps, total_ms)
 
-    # end to end through the public C-ABI call on host memory (flce_fwd_bwd_host): every step
-    # copies its inputs in and its results out; the copies run on their own streams and two
-    # device buffers alternate, so one step's copies overlap the neighbouring steps' kernels
-    # while the kernels stay in order on one stream
+    # end to end through the public C-ABI call on host memory (flce_fwd_bwd_host, the bounded
+    # path): every step copies its inputs in and its results out; the copies run on their own
+    # streams and two device buffers alternate, so one step's copies overlap the neighbouring
+    # steps' kernels while the kernels stay in order on one stream
     Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
     Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True); Wh.copy_(W)
     yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True); yh.copy_(y)
@@ -459,12 +550,12 @@ def run_flce(args, rank, world, local_rank):
         dist.barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
-    for st in (comp, cin, cout):
-        st.wait_event(e0)
+    for st_ in (comp, cin, cout):
+        st_.wait_event(e0)
     e2e_run(args.e2e_steps)
-    for st in (comp, cin, cout):
+    for st_ in (comp, cin, cout):
         fin = torch.cuda.Event()
-        fin.record(st)
+        fin.record(st_)
         stream.wait_event(fin)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -473,14 +564,35 @@ def run_flce(args, rank, world, local_rank):
         st_code = flce.read_device_status(buf)
         if st_code != 0:
             raise RuntimeError(f"device status {flce.status_string(st_code)}")
-    del slots
+    del slots, Xh, Wh, yh
     h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
     d2h = sum(t.numel() * t.element_size() for t in out)
 
     naive = None
     if rank == 0 and world == 1 and not args.no_naive:
         naive = torch_naive(X, W, y, problem, flush, stream, torch)
-    sustained = sustained_run(step, flops, args.sustain, local_rank, torch) if args.sustain > 0 else None
+
+    # the other path on the same inputs, then both paths on the other workloads
+    others = None
+    if world == 1 and not args.no_others:
+        del ws
+        torch.cuda.empty_cache()
+        others = {"other_path": measure_path(flce, torch, dev, problem, X, W, y, not rowchunk, args.other_steps, 3,
+                                             flush, stream)}
+        del X, W, y, out
+        torch.cuda.empty_cache()
+        wl = {}
+        for name in OTHER_WORKLOADS:
+            if name == args.workload:
+                continue
+            p_o, X_o, W_o, y_o = device_problem(name, rank, dev)
+            wl[name] = {"bounded": measure_path(flce, torch, dev, p_o, X_o, W_o, y_o, False, args.other_steps, 3,
+                                                flush, stream),
+                        "rowchunk": measure_path(flce, torch, dev, p_o, X_o, W_o, y_o, True, args.other_steps, 3,
+                                                 flush, stream, naive=not args.no_naive)}
+            del X_o, W_o, y_o, p_o
+            torch.cuda.empty_cache()
+        others["workloads"] = wl
 
     if dist is not None:
         dist.barrier()
@@ -491,50 +603,56 @@ def run_flce(args, rank, world, local_rank):
     peaks, peak_src = load_peaks()
     kinds = {k: {"launches": n_, "ms": ms_, "tflop": fl_ / 1e12} for k, (n_, ms_, fl_) in prof.items()}
     dom = "dxdw"
-    n_l, ms_l, fl_l = prof_dom[dom]
-    achieved = (fl_l / n_l) / ((ms_l / n_l) / 1e3) / 1e12
+    achieved = dominant_tflops(r["dom"])
     peak_sust = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAKS["bf16_tflops_sustained"]))
     peak_burst = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     # a timed region whose median SM clock stayed at the maximum is compared with the burst
     # peak, one that the power cap held lower (a long, heavy run) with the sustained peak
     capped = bool(clk.get("sm_mhz") and clk.get("sm_max_mhz") and clk["sm_mhz"] < 0.95 * clk["sm_max_mhz"])
     peak, peak_kind = (peak_sust, "bf16_tflops_sustained") if capped else (peak_burst, "bf16_tflops (burst)")
-    gpu_launches = per_step["launches"] * args.steps
+    path_name = "rowchunk" if rowchunk else "bounded"
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": workload_config(args.workload, None, f"flushed between steps ({L2_FLUSH_BYTES >> 20} MiB write, "
-                                                     "outside the per-step events)", world),
-        "frac_of_peak": value / world / peak_burst, "peak_src": f"{peak_src} bf16_tflops (burst)",
+        "config": arm_config(args, world),
+        "frac_of_peak": value / world / peak_burst, "frac_of_sustained_peak": value / world / peak_sust,
+        "peak_src": f"{peak_src} bf16_tflops (burst) / bf16_tflops_sustained",
         "executed_tflops": world * per_step["flops"] * args.steps / (total_ms / 1e3) / 1e12,
-        "path": "fused row chunks (6NHV executed)" if ws_bytes >= flce.workspace_bytes(n, h, v) else "recompute (8NHV)",
+        "path": ("row chunks, logits computed once (6NHV executed); workspace grows with V" if rowchunk else
+                 "bounded: logits recomputed per vocabulary chunk in the backward (8NHV executed); "
+                 "workspace independent of V"),
         "extra_hbm_bytes": ws_bytes, "peak_alloc_delta_bytes": int(peak_delta),
         "materialised_logits_bytes": {"bf16": flce.logits_footprint_bytes(n, v, 2),
                                       "fp32": flce.logits_footprint_bytes(n, v, 4)},
-        "wall_ms_per_step_incl_flush": 1e3 * t_wall / args.steps,
+        "timed_region_s": sum(step_ms) / 1e3,
+        "wall_ms_per_step_incl_flush": 1e3 * r["wall_s"] / args.steps,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak,
                      "peak_note": f"{peak_src} {peak_kind} ({'power-capped' if capped else 'full clock'} during the "
                                   f"timed region); of burst {peak_burst}: {achieved / peak_burst:.3f}, of sustained "
                                   f"{peak_sust}: {achieved / peak_sust:.3f}",
-                     "traffic": traffic_record(dom, args.workload)},
+                     "algorithmic_flops_per_launch": r["dom"][2] / r["dom"][0],
+                     "launches_timed": r["dom"][0],
+                     "traffic": traffic_record(dom, args.workload, path_name)},
         "kernels": kinds,
         "kernels_note": "separate untimed pass with every launch bracketed by events (which serialises the "
                         "launches); the roofline kernel is timed inside the timed region",
-        "gpu_launches": gpu_launches,
+        "gpu_launches": per_step["launches"] * args.steps,
         "clocks": clk,
+        "tflops_per_ghz": (value / world) / (clk["sm_mhz"] / 1e3) if clk.get("sm_mhz") else None,
         "e2e": {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "note": "flce_fwd_bwd_host through the C-ABI: pinned host X, W, labels copied in and loss, lse, "
-                        "dX, dW copied out every step, on their own streams; two device buffers alternate so "
-                        "copies overlap the neighbouring steps' kernels"},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+                "note": "flce_fwd_bwd_host (bounded path) through the C-ABI: pinned host X, W, labels copied in "
+                        "and loss, lse, dX, dW copied out every step, on their own streams; two device buffers "
+                        "alternate so copies overlap the neighbouring steps' kernels"},
     }
     if naive is not None:
         line["torch_naive"] = naive
-    if sustained is not None:
-        line["sustained"] = sustained
+    if others is not None:
+        line["other_path"] = others["other_path"]
+        line["workloads"] = others["workloads"]
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(problem, args.cpu_seconds)
     print(json.dumps(line), flush=True)
@@ -570,12 +688,14 @@ def run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, strea
     flce.profile_enable(True, kinds=[dom])
     clocks = ClockSampler(dev.index if dev.index is not None else 0)
     clocks.start()
+    clocks.mark_start()
     for i in range(args.steps):
         flush.fill_(i & 0xFF)
         starts[i].record(stream)
         step()
         ends[i].record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
     clk = clocks.stop() or {"reasons": ["no sampler"], "samples": 0}
     prof_dom = flce.profile_read()[dom]
     flce.profile_enable(False)

@@ -28,6 +28,9 @@ struct Layout {
   size_t counter;                 // tile counter of the dynamically scheduled launches
   size_t fix_count;               // fused path: rows listed for the full fix-up in the current chunk
   size_t ticket;                  // fused path: blocks of the label pass done (its last block resets it)
+  size_t fcount;                  // unit counters of the forward launches: one header word, or one per row
+                                  // chunk of the fused path (zeroed at the start of every call)
+  int nchunks;                    // fused path: row chunks
   size_t blk_loss, blk_valid;     // per-block partial sums of the finalize kernels
   size_t part_m, part_l, tgt;     // forward: per-split row state, target logits
   size_t g;                       // one chunk buffer: recompute path G [N, chunk]; fused path p~/G [rows, Vp]
@@ -84,6 +87,7 @@ Layout make_layout(const flce_problem_t& p, bool fused, bool shard = false) {
   L.counter = off + 16;
   L.fix_count = off + 20;
   L.ticket = off + 24;
+  L.fcount = off + 28;
   off += kAlign;
   const size_t nblk_alloc = std::max<size_t>(L.nblk, (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock);
   L.blk_loss = off;
@@ -118,6 +122,11 @@ Layout make_layout(const flce_problem_t& p, bool fused, bool shard = false) {
   if (fused) off = align_up(off + 2 * static_cast<size_t>(L.rows) * h);
   L.lab = off;
   if (shard) off = align_up(off + sizeof(int32_t) * n);
+  if (fused) {
+    L.nchunks = static_cast<int>((p.n + L.rows - 1) / L.rows);
+    L.fcount = off;
+    off = align_up(off + sizeof(int) * static_cast<size_t>(L.nchunks));
+  }
   L.total = off;
   return L;
 }
@@ -269,6 +278,7 @@ struct Ctx {
   float* dx_acc() const { return reinterpret_cast<float*>(ws + L.dx_acc); }
   float* mtile() const { return reinterpret_cast<float*>(ws + L.mtile); }
   int* ticket() const { return reinterpret_cast<int*>(ws + L.ticket); }
+  int* fcount() const { return reinterpret_cast<int*>(ws + L.fcount); }
   int* fix_count() const { return reinterpret_cast<int*>(ws + L.fix_count); }
   int* fix_list() const { return reinterpret_cast<int*>(ws + L.fix_list); }
   float* mref() const { return reinterpret_cast<float*>(ws + L.mref); }
@@ -443,6 +453,7 @@ flce_status_t run_forward_tc(const Ctx& c, const void* X, const void* W, const i
   tp.seq_len = p.shift ? p.seq_len : 1;
   tp.r0 = 0;
   tp.row_end = tp.n;
+  tp.tile_counter = c.fcount();  // a header word: zero since the call started
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = pair_grid(c.dev.sms, units);
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
@@ -562,7 +573,12 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
   // dX/dW epilogues, and only rows whose tiles outrun that reference get the
   // full fix-up pass.
   const int nblk = (n + kRefRowsPerBlock - 1) / kRefRowsPerBlock;
-  flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
+  // every forward-store launch takes its units from its own counter, so no launch
+  // resets a counter that a running one may still be drawing from
+  flce_status_t st = cuda_status(
+      cudaMemsetAsync(c.fcount(), 0, sizeof(int) * static_cast<size_t>(c.L.nchunks), c.stream));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
     return launch_label_prep(n, h, v, p.reduction, lv, X, W, c.mref(), c.tgt(), reinterpret_cast<int*>(c.part_l()),
                              c.ticket(), c.n_valid(), c.scale(), c.status(), c.stream);
   }));
@@ -608,6 +624,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.mtile = c.mtile();
     tp.mref = c.mref();
     tp.zero_words = c.counter();  // the backward launch's tile counter and the fix-up list count start at zero
+    tp.tile_counter = c.fcount() + r0 / c.L.rows;
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
@@ -725,6 +742,7 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   tp.topk_val = cand_val;
   tp.topk_idx = cand_idx;
   tp.topk_k = k;
+  tp.tile_counter = c.fcount();  // a header word: zero since the call started
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
   const int grid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
   flce_status_t st =

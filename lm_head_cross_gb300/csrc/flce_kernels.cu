@@ -105,10 +105,17 @@ struct Pair {
 };
 
 template <int MODE>
-constexpr bool kDynamic = (MODE == kModeBwd);
-
-template <int MODE>
 constexpr bool kUnits = (MODE == kModeForward || MODE == kModeFwdStore || MODE == kModeTopk);
+
+// Dynamic schedules hand out work through a global counter (p.tile_counter,
+// zero at launch): the backward's tiles one by one, the forward modes' units
+// (row tile, vocabulary range) one unit at a time.  A pair's first index is its
+// pair index; the even CTA's producer takes every later one from the counter
+// and publishes it to the pair through the tile ring.
+template <int MODE>
+constexpr bool kDynamic = (MODE == kModeBwd) || kUnits<MODE>;
+
+enum Role : int { kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2 };
 
 __device__ __forceinline__ int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
@@ -128,11 +135,10 @@ __device__ __forceinline__ void sched_init(const TcParams& p, const Pair& pr, Sc
   s.done = false;
   s.ridx = 0;
   s.rphase = 0;
+  s.t = pr.id;
   if (kUnits<MODE>) {
     s.unit = pr.id;
     fwd_unit_begin(p, s);
-  } else {
-    s.t = pr.id;
   }
 }
 
@@ -180,17 +186,6 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Pair& pr, con
   }
 }
 
-template <int MODE>
-__device__ __forceinline__ void sched_next(const TcParams& p, const Pair& pr, Sched& s) {
-  if (kUnits<MODE>) {
-    if (++s.vt >= s.ve) {
-      s.unit += pr.count;
-      fwd_unit_begin(p, s);
-    }
-  } else {
-    s.t += pr.count;
-  }
-}
 
 // A wait gave up: record it, and stop both CTAs of the pair.
 __device__ __forceinline__ void record_timeout(const TcParams& p, const Pair& pr, volatile int* abort_flag) {
@@ -231,10 +226,52 @@ __device__ __forceinline__ bool ring_read(const TcParams& p, TileRing& ring, Sch
   return true;
 }
 
-// Next tile index of the dynamic schedule: a pair's first tile is its pair
-// index, the rest come from the global counter in the order tiles are listed.
+// Next index of the dynamic schedule: a pair's first index is its pair index,
+// the rest come from the global counter in the order the work is listed.
 __device__ __forceinline__ int dynamic_next_index(const TcParams& p, const Pair& pr) {
   return pr.count + atomicAdd(p.tile_counter, 1);
+}
+
+// The pair's next index: the even CTA's producer draws and publishes it, every
+// other reader (the MMA thread, the epilogue warps of both CTAs, the odd CTA's
+// producer) reads it from the ring.  False if a ring wait gave up.
+template <int MODE, int ROLE>
+__device__ __forceinline__ bool sched_exchange(const TcParams& p, const Pair& pr, TileRing& ring, Sched& s, int lane,
+                                               volatile int* abort_flag, bool first) {
+  bool ok;
+  if (ROLE == kRoleProducer && pr.rank == 0) {
+    if (!first) s.t = dynamic_next_index(p, pr);
+    ok = ring_publish(p, pr, ring, s, s.t, abort_flag);
+  } else {
+    ok = ring_read<ROLE == kRoleEpilogue>(p, ring, s, ROLE == kRoleEpilogue ? lane == 0 : true, abort_flag);
+  }
+  if (ok && kUnits<MODE>) {
+    s.unit = s.t;
+    fwd_unit_begin(p, s);
+  }
+  return ok;
+}
+
+// The first position of the schedule.
+template <int MODE, int ROLE>
+__device__ __forceinline__ bool sched_start(const TcParams& p, const Pair& pr, TileRing& ring, Sched& s, int lane,
+                                            volatile int* abort_flag) {
+  sched_init<MODE>(p, pr, s);
+  if (!kDynamic<MODE>) return true;
+  return sched_exchange<MODE, ROLE>(p, pr, ring, s, lane, abort_flag, true);
+}
+
+// After a tile: the next tile of the current forward unit, else the next index
+// (static: pair-strided; dynamic: through the ring).
+template <int MODE, int ROLE>
+__device__ __forceinline__ bool sched_advance(const TcParams& p, const Pair& pr, TileRing& ring, Sched& s, int lane,
+                                              volatile int* abort_flag) {
+  if (kUnits<MODE> && ++s.vt < s.ve) return true;
+  if (!kDynamic<MODE>) {
+    s.t += pr.count;
+    return true;
+  }
+  return sched_exchange<MODE, ROLE>(p, pr, ring, s, lane, abort_flag, false);
 }
 
 // ----------------------------------------------------------------------------- producer (TMA)
@@ -243,14 +280,9 @@ template <int MODE>
 __device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& pr, uint8_t* smem, uint64_t* full,
                              uint64_t* empty, TileRing ring, volatile int* abort_flag) {
   Sched s;
-  sched_init<MODE>(p, pr, s);
-  if (kDynamic<MODE>) {
-    const bool ok = pr.rank == 0 ? ring_publish(p, pr, ring, s, s.t, abort_flag)
-                                 : ring_read<false>(p, ring, s, true, abort_flag);
-    if (!ok) {
-      record_timeout(p, pr, abort_flag);
-      return;
-    }
+  if (!sched_start<MODE, kRoleProducer>(p, pr, ring, s, 0, abort_flag)) {
+    record_timeout(p, pr, abort_flag);
+    return;
   }
   const uint32_t full_even = mapa_shared(smem_u32(full), 0);  // completion is counted in the even CTA
   const int bhalf = static_cast<int>(pr.rank) * kHalfN;
@@ -289,20 +321,9 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& 
         phase ^= 1u;
       }
     }
-    if (kDynamic<MODE>) {
-      bool ok;
-      if (pr.rank == 0) {
-        s.t = dynamic_next_index(p, pr);
-        ok = ring_publish(p, pr, ring, s, s.t, abort_flag);
-      } else {
-        ok = ring_read<false>(p, ring, s, true, abort_flag);
-      }
-      if (!ok) {
-        record_timeout(p, pr, abort_flag);
-        return;
-      }
-    } else {
-      sched_next<MODE>(p, pr, s);
+    if (!sched_advance<MODE, kRoleProducer>(p, pr, ring, s, 0, abort_flag)) {
+      record_timeout(p, pr, abort_flag);
+      return;
     }
   }
 }
@@ -314,8 +335,7 @@ __device__ void run_mma(const TcParams& p, const Pair& pr, uint8_t* smem, uint64
                         uint64_t* tfull, uint64_t* tempty, uint32_t tmem_base, TileRing ring,
                         volatile int* abort_flag) {
   Sched s;
-  sched_init<MODE>(p, pr, s);
-  if (kDynamic<MODE> && !ring_read<false>(p, ring, s, true, abort_flag)) {
+  if (!sched_start<MODE, kRoleMma>(p, pr, ring, s, 0, abort_flag)) {
     record_timeout(p, pr, abort_flag);
     return;
   }
@@ -357,13 +377,9 @@ __device__ void run_mma(const TcParams& p, const Pair& pr, uint8_t* smem, uint64
     umma_commit_pair(&tfull[acc], kPairMask);  // both CTAs' accumulators ready for their epilogues
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
-    if (kDynamic<MODE>) {
-      if (!ring_read<false>(p, ring, s, true, abort_flag)) {
-        record_timeout(p, pr, abort_flag);
-        return;
-      }
-    } else {
-      sched_next<MODE>(p, pr, s);
+    if (!sched_advance<MODE, kRoleMma>(p, pr, ring, s, 0, abort_flag)) {
+      record_timeout(p, pr, abort_flag);
+      return;
     }
   }
 }
@@ -530,8 +546,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
   uint32_t ephase = 0;
 
   Sched s;
-  sched_init<MODE>(p, pr, s);
-  if (kDynamic<MODE> && !ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
+  if (!sched_start<MODE, kRoleEpilogue>(p, pr, ring, s, lane, abort_flag)) {
     record_timeout(p, pr, abort_flag);
     return;
   }
@@ -887,13 +902,9 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
     }
     acc ^= 1;
     if (acc == 0) acc_phase ^= 1u;
-    if (kDynamic<MODE>) {
-      if (!ring_read<true>(p, ring, s, lane == 0, abort_flag)) {
-        record_timeout(p, pr, abort_flag);
-        break;
-      }
-    } else {
-      sched_next<MODE>(p, pr, s);
+    if (!sched_advance<MODE, kRoleEpilogue>(p, pr, ring, s, lane, abort_flag)) {
+      record_timeout(p, pr, abort_flag);
+      break;
     }
   }
   if (lane == 0) bulk_wait_group_all();

@@ -29,7 +29,7 @@ constexpr int kMaxDevices = 64;
 constexpr size_t round256(size_t x) { return (x + 255) / 256 * 256; }
 constexpr size_t kMaxBlocks = (kNoAllocMaxRows + kFinalizeThreads - 1) / kFinalizeThreads;
 // Scratch layout (byte offsets into the static array).
-constexpr size_t kOffStatus = 0;             // int status, int n_valid, float scale
+constexpr size_t kOffStatus = 0;             // int status, int n_valid, float scale, int unit counter
 constexpr size_t kOffBlkLoss = 256;
 constexpr size_t kOffBlkValid = kOffBlkLoss + round256(8 * kMaxBlocks);
 constexpr size_t kOffPartM = kOffBlkValid + round256(4 * kMaxBlocks);
@@ -159,15 +159,16 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.part_m = part_m;
   tp.part_l = part_l;
   tp.tgt = tgt;
+  tp.tile_counter = reinterpret_cast<int*>(s + kOffStatus + 12);
   tp.labels = labels;
   tp.shift = p->shift;
   tp.seq_len = p->shift ? p->seq_len : 1;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = pair_grid(sms, units);
 
-  // Only the status word must start at zero; every other region the kernels
-  // read is written earlier in the same call.
-  if (cudaMemsetAsync(status, 0, sizeof(int), cs) != cudaSuccess) return FLCE_ERR_CUDA;
+  // Only the status word and the forward launch's unit counter must start at
+  // zero; every other region the kernels read is written earlier in the same call.
+  if (cudaMemsetAsync(status, 0, 16, cs) != cudaSuccess) return FLCE_ERR_CUDA;
   if (launch_tc(kModeForward, maps, tp, grid, cs) != cudaSuccess) return FLCE_ERR_CUDA;
   const bool per_row = p->reduction == FLCE_REDUCTION_NONE;
   const LabelView lv{labels, p->ignore_index, tp.shift, tp.seq_len};

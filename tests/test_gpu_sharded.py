@@ -161,7 +161,7 @@ def _worker(rank, world, port, out):
 
 def test_sharded_cross_entropy_two_processes_one_gpu():
     import torch.multiprocessing as mp
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     try:
         mp.spawn(_worker, args=(2, _free_port(), out), nprocs=2, join=True)

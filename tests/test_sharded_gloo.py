@@ -144,7 +144,7 @@ def _worker(rank, world, port, layout, reduction, shift, out):
 
 def _run(layout, reduction, shift):
     world = layout[0] * layout[1]
-    mgr = mp.Manager()
+    mgr = mp.get_context("spawn").Manager()
     out = mgr.dict()
     try:
         mp.spawn(_worker, args=(world, _free_port(), layout, reduction, shift, out), nprocs=world, join=True)
