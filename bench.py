@@ -456,6 +456,60 @@ def measure_path(flce, torch, dev, problem, X, W, y, rowchunk, steps, warmup, fl
     return res
 
 
+def e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, world, flops):
+    """End to end through the public C-ABI call on host memory (flce_fwd_bwd_host, the
+    bounded path): every step copies its inputs in and its results out; the copies run on
+    their own streams and two device buffers alternate, so one step's copies overlap the
+    neighbouring steps' kernels while the kernels stay in order on one stream."""
+    n, h, v = problem.n, problem.h, problem.v
+    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
+    Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True); Wh.copy_(W)
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True); yh.copy_(y)
+    hb = flce.host_buffer_bytes(n, h, v, problem.ignore_index, problem.reduction)
+    comp, cin, cout = (torch.cuda.Stream(device=dev) for _ in range(3))
+    slots = [(tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out),
+              torch.empty(hb, dtype=torch.uint8, device=dev), torch.cuda.Event()) for _ in range(2)]
+
+    def e2e_run(steps):
+        for i in range(steps):
+            outs, buf, done = slots[i % 2]
+            if i >= 2:
+                cin.wait_event(done)  # the previous call on this buffer has copied its results out
+            flce.fwd_bwd_host(Xh, Wh, yh, outs, buf, problem.ignore_index, problem.reduction, stream=comp,
+                              in_stream=cin, out_stream=cout)
+            done.record(cout)
+
+    e2e_run(2)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for st_ in (comp, cin, cout):
+        st_.wait_event(e0)
+    e2e_run(args.e2e_steps)
+    for st_ in (comp, cin, cout):
+        fin = torch.cuda.Event()
+        fin.record(st_)
+        stream.wait_event(fin)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+    for _, buf, _ in slots:
+        st_code = flce.read_device_status(buf)
+        if st_code != 0:
+            raise RuntimeError(f"device status {flce.status_string(st_code)}")
+    del slots, Xh, Wh, yh
+    h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
+    d2h = sum(t.numel() * t.element_size() for t in out)
+
+    return {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "note": "flce_fwd_bwd_host (bounded path) through the C-ABI: pinned host X, W, labels copied in "
+                    "and loss, lse, dX, dW copied out every step, on their own streams; two device buffers "
+                    "alternate so copies overlap the neighbouring steps' kernels"}
+
+
 def run_flce(args, rank, world, local_rank):
     import torch
     import lm_head_cross_gb300 as flce
@@ -502,9 +556,11 @@ def run_flce(args, rank, world, local_rank):
     if args.op != "fwd_bwd" or args.reduction or args.shift:
         return run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, stream)
 
-    # extra device memory of one call beyond its inputs and outputs: exactly the workspace
+    # extra device memory of one call beyond its inputs and outputs: the workspace, up to the
+    # caching allocator's rounding (512-byte sizes; a reused cached block that is not split
+    # keeps up to 1 MiB of slack per allocation, five allocations per call)
     peak_delta = extra_memory(flce, torch, dev, X, W, y, problem, rowchunk)
-    if not ws_bytes <= peak_delta <= ws_bytes + 4096:   # the allocator rounds each output up to 512 bytes
+    if not ws_bytes <= peak_delta <= ws_bytes + (5 << 20) + 4096:
         raise RuntimeError(f"allocation beyond the workspace: peak delta {peak_delta} vs workspace {ws_bytes}")
     if args.workload == HEADLINE and not rowchunk and ws_bytes >= 4e9:
         raise RuntimeError(f"workspace of the 128K x 128K workload is {ws_bytes} bytes, not under 4 GB")
@@ -523,50 +579,9 @@ def run_flce(args, rank, world, local_rank):
     flops = credited_flops(n, h, v)
     value = job_tflops(world, flops, args.steps, total_ms)
 
-    # end to end through the public C-ABI call on host memory (flce_fwd_bwd_host, the bounded
-    # path): every step copies its inputs in and its results out; the copies run on their own
-    # streams and two device buffers alternate, so one step's copies overlap the neighbouring
-    # steps' kernels while the kernels stay in order on one stream
-    Xh = torch.empty(X.shape, dtype=X.dtype, pin_memory=True); Xh.copy_(X)
-    Wh = torch.empty(W.shape, dtype=W.dtype, pin_memory=True); Wh.copy_(W)
-    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True); yh.copy_(y)
-    hb = flce.host_buffer_bytes(n, h, v, problem.ignore_index, problem.reduction)
-    comp, cin, cout = (torch.cuda.Stream(device=dev) for _ in range(3))
-    slots = [(tuple(torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in out),
-              torch.empty(hb, dtype=torch.uint8, device=dev), torch.cuda.Event()) for _ in range(2)]
-
-    def e2e_run(steps):
-        for i in range(steps):
-            outs, buf, done = slots[i % 2]
-            if i >= 2:
-                cin.wait_event(done)  # the previous call on this buffer has copied its results out
-            flce.fwd_bwd_host(Xh, Wh, yh, outs, buf, problem.ignore_index, problem.reduction, stream=comp,
-                              in_stream=cin, out_stream=cout)
-            done.record(cout)
-
-    e2e_run(2)
-    torch.cuda.synchronize()
-    if dist is not None:
-        dist.barrier()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for st_ in (comp, cin, cout):
-        st_.wait_event(e0)
-    e2e_run(args.e2e_steps)
-    for st_ in (comp, cin, cout):
-        fin = torch.cuda.Event()
-        fin.record(st_)
-        stream.wait_event(fin)
-    e1.record(stream)
-    torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-    for _, buf, _ in slots:
-        st_code = flce.read_device_status(buf)
-        if st_code != 0:
-            raise RuntimeError(f"device status {flce.status_string(st_code)}")
-    del slots, Xh, Wh, yh
-    h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
-    d2h = sum(t.numel() * t.element_size() for t in out)
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e = e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, world, flops)
 
     naive = None
     if rank == 0 and world == 1 and not args.no_naive:
@@ -642,11 +657,7 @@ def run_flce(args, rank, world, local_rank):
         "gpu_launches": per_step["launches"] * args.steps,
         "clocks": clk,
         "tflops_per_ghz": (value / world) / (clk["sm_mhz"] / 1e3) if clk.get("sm_mhz") else None,
-        "e2e": {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
-                "note": "flce_fwd_bwd_host (bounded path) through the C-ABI: pinned host X, W, labels copied in "
-                        "and loss, lse, dX, dW copied out every step, on their own streams; two device buffers "
-                        "alternate so copies overlap the neighbouring steps' kernels"},
+        "e2e": e2e,
     }
     if naive is not None:
         line["torch_naive"] = naive

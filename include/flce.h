@@ -77,7 +77,8 @@ typedef enum {
   FLCE_ERR_TIMEOUT = 6,             /* device: a bounded pipeline wait gave up (no hang, no trap) */
   FLCE_ERR_CUDA = 7,                /* a CUDA runtime/driver call failed, or no sm_100-family GPU */
   FLCE_ERR_NO_DEVICE_STATUS = 8,    /* flce_read_device_status could not read the word */
-  FLCE_ERR_EXCEEDS_STATIC_SCRATCH = 9 /* flce_forward_noalloc: n above its fixed maximum */
+  FLCE_ERR_EXCEEDS_STATIC_SCRATCH = 9, /* flce_forward_noalloc: n above its fixed maximum */
+  FLCE_ERR_BOUNDS = 10              /* device, debug build only: an index or TMA coordinate failed its check */
 } flce_status_t;
 
 typedef enum { FLCE_REDUCTION_MEAN = 0, FLCE_REDUCTION_SUM = 1, FLCE_REDUCTION_NONE = 2 } flce_reduction_t;
@@ -218,6 +219,19 @@ flce_status_t flce_read_device_status(void* ws, flce_stream_t stream);
  * FLCE_ERR_TIMEOUT in ws and the kernel returns.  Exercises the error path of
  * the bounded waits used by every kernel. */
 flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream);
+
+/* Debug build.  The library also builds as libflce_debug.so (compiled with
+ * FLCE_DEBUG_CHECKS): every index the kernels compute into a workspace or
+ * output buffer is tested against that buffer's size, and every TMA coordinate
+ * against the 16-byte rule, before the access; a failed test records
+ * FLCE_ERR_BOUNDS in the status word and skips the access (no trap; a skipped
+ * load then ends in a bounded wait).  The pages have no counterpart.
+ * flce_debug_checks returns 1 in that build, 0 in the release one.
+ * flce_selftest_bounds launches one thread that tests an index one past a
+ * one-element buffer: in the debug build the status word then reads
+ * FLCE_ERR_BOUNDS, in the release build FLCE_OK; no memory is accessed. */
+int flce_debug_checks(void);
+flce_status_t flce_selftest_bounds(void* ws, size_t ws_bytes, flce_stream_t stream);
 
 /* Diagnostics: per-launch device timing.  `mask` selects the kernel kinds to
  * time (bit k for kind k; 0 turns profiling off, -1 times every kind).  Each

@@ -23,7 +23,7 @@ EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_rowchunk", "flce_forwa
             "flce_profile_read", "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
             "flce_soft_fwd_bwd", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_shard_workspace_bytes",
             "flce_shard_forward", "flce_shard_combine", "flce_shard_backward", "flce_valid_count",
-            "flce_f32_to_bf16", "flce_status_string")
+            "flce_f32_to_bf16", "flce_debug_checks", "flce_selftest_bounds", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
 
 
@@ -108,6 +108,10 @@ def lib():
     L.flce_profile_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_double),
                                     ctypes.POINTER(ctypes.c_double)]
     L.flce_profile_read.restype = ctypes.c_int
+    L.flce_debug_checks.argtypes = []
+    L.flce_debug_checks.restype = ctypes.c_int
+    L.flce_selftest_bounds.argtypes = [vp, sz, vp]
+    L.flce_selftest_bounds.restype = ctypes.c_int
     L.flce_status_string.argtypes = [ctypes.c_int]
     L.flce_status_string.restype = ctypes.c_char_p
     _LIB = L

@@ -1,4 +1,7 @@
-"""Builds ``libflce.so`` in-tree with nvcc for sm_103a (no cmake, no torch).
+"""Builds ``libflce.so`` in-tree with nvcc for sm_103a (no cmake, no torch), and
+beside it ``libflce_debug.so``, the same sources compiled with FLCE_DEBUG_CHECKS
+(every computed index and TMA coordinate checked before use, failures recorded
+in the status word).
 
     python -m lm_head_cross_gb300.build
 """
@@ -15,6 +18,7 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libflce.so")
+DEBUG_LIB = os.path.join(HERE, "libflce_debug.so")
 BUILD_DIR = os.path.join(HERE, "_build")
 SOURCES = ["flce_kernels.cu", "flce_api.cu", "flce_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -27,10 +31,13 @@ def nvcc() -> str:
     raise RuntimeError("nvcc not found")
 
 
-def _compile(src: str, verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD_DIR, os.path.splitext(src)[0] + ".o")
+def _compile(src: str, verbose_ptxas: bool, debug: bool) -> str:
+    out_dir = os.path.join(BUILD_DIR, "debug") if debug else BUILD_DIR
+    obj = os.path.join(out_dir, os.path.splitext(src)[0] + ".o")
     cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC,
            "-c", os.path.join(CSRC, src), "-o", obj]
+    if debug:
+        cmd.insert(1, "-DFLCE_DEBUG_CHECKS")
     if verbose_ptxas:
         cmd.insert(1, "-Xptxas=-v")
     r = subprocess.run(cmd, capture_output=True, text=True)
@@ -41,22 +48,29 @@ def _compile(src: str, verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(force: bool = False, verbose_ptxas: bool = False) -> str:
-    srcs = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
-    srcs.append(os.path.join(INCLUDE, "flce.h"))
-    if not force and os.path.exists(LIB):
-        lib_m = os.path.getmtime(LIB)
-        if all(os.path.getmtime(s) <= lib_m for s in srcs):
-            return LIB
-    os.makedirs(BUILD_DIR, exist_ok=True)
-    with ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, verbose_ptxas), SOURCES))
-    tmp = LIB + ".tmp"
+def _link(objs, lib):
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+
+
+def build(force: bool = False, verbose_ptxas: bool = False) -> str:
+    srcs = [os.path.join(CSRC, s) for s in SOURCES] + [os.path.join(CSRC, h) for h in os.listdir(CSRC) if h.endswith((".h", ".cuh"))]
+    srcs.append(os.path.join(INCLUDE, "flce.h"))
+    srcs.append(os.path.abspath(__file__))
+    if not force and all(os.path.exists(lib) for lib in (LIB, DEBUG_LIB)):
+        lib_m = min(os.path.getmtime(LIB), os.path.getmtime(DEBUG_LIB))
+        if all(os.path.getmtime(s) <= lib_m for s in srcs):
+            return LIB
+    os.makedirs(os.path.join(BUILD_DIR, "debug"), exist_ok=True)
+    jobs = [(s, d) for d in (False, True) for s in SOURCES]
+    with ThreadPoolExecutor(max_workers=len(jobs)) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], verbose_ptxas and not j[1], j[1]), jobs))
+    _link(objs[:len(SOURCES)], LIB)
+    _link(objs[len(SOURCES):], DEBUG_LIB)
     return LIB
 
 

@@ -18,6 +18,11 @@ namespace {
 
 constexpr size_t kAlign = 256;
 constexpr int32_t kMaxShardParts = 1 << 16;  // most vocabulary shards flce_shard_combine takes
+#ifdef FLCE_DEBUG_CHECKS
+constexpr int kDebugChecksBuild = 1;
+#else
+constexpr int kDebugChecksBuild = 0;
+#endif
 constexpr uint64_t kDefaultTimeoutNs = 4000000000ull;  // 4 s; a healthy wait lasts microseconds
 
 size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
@@ -212,31 +217,41 @@ flce_status_t device_info(Device* d) {
 }
 
 // Forward split count: the number of vocabulary ranges each row tile is cut
-// into.  Picks the count (4..32, at most the number of vocabulary tiles) whose
-// round-robin assignment of (row tile, range) units to `grid` pairs gives the
-// smallest largest per-pair tile count, with units numbered as the kernels
-// take them (unit_coords: row tile fastest within groups of `group` row tiles).
+// into.  The forward modes hand out (row tile, range) units in the order
+// unit_coords gives them (row tile fastest within groups of `group` row
+// tiles), each pair taking the next unit when it finishes its current one; a
+// pair's finishing time is the tiles of the units it took.  Picks the count
+// (4..cap, at most the number of vocabulary tiles) whose list schedule over
+// `grid` pairs ends earliest; among those, the one whose least loaded pair
+// idles least (then the fewest ranges to merge).
 int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, int group) {
   const int hi = std::min(cap, vocab_tiles);
   const int lo = std::min(4, hi);
   int best = lo;
-  long long best_cost = -1;
+  long long best_cost = -1, best_min = -1;
   for (int vs = lo; vs <= hi; ++vs) {
     const long long units = static_cast<long long>(row_tiles) * vs;
     const int g = static_cast<int>(std::min<long long>(grid, units));
-    // per pair b: units b, b+g, ...
-    long long worst = 0;
-    for (int b = 0; b < g; ++b) {
-      long long tiles = 0;
-      for (long long u = b; u < units; u += g) {
-        int rt = 0, sp = 0;
-        unit_coords(static_cast<int>(u), row_tiles, vs, group, &rt, &sp);
-        tiles += (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
-      }
-      worst = std::max(worst, tiles);
+    // min-heap of (busy until, pair): the pair that frees first takes the next unit
+    std::vector<std::pair<long long, int>> heap;
+    for (int b = 0; b < g; ++b) heap.emplace_back(0, b);
+    auto cmp = [](const std::pair<long long, int>& a, const std::pair<long long, int>& b) { return a > b; };
+    std::make_heap(heap.begin(), heap.end(), cmp);
+    long long makespan = 0;
+    for (long long u = 0; u < units; ++u) {
+      int rt = 0, sp = 0;
+      unit_coords(static_cast<int>(u), row_tiles, vs, group, &rt, &sp);
+      const long long tiles =
+          (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
+      std::pop_heap(heap.begin(), heap.end(), cmp);
+      heap.back().first += tiles;
+      makespan = std::max(makespan, heap.back().first);
+      std::push_heap(heap.begin(), heap.end(), cmp);
     }
-    if (best_cost < 0 || worst < best_cost) {
-      best_cost = worst;
+    const long long least = heap.front().first;  // the heap's top: the least loaded pair
+    if (best_cost < 0 || makespan < best_cost || (makespan == best_cost && least > best_min)) {
+      best_cost = makespan;
+      best_min = least;
       best = vs;
     }
   }
@@ -454,6 +469,7 @@ flce_status_t run_forward_tc(const Ctx& c, const void* X, const void* W, const i
   tp.r0 = 0;
   tp.row_end = tp.n;
   tp.tile_counter = c.fcount();  // a header word: zero since the call started
+  tp.part_count = static_cast<int64_t>(kMaxSplit) * p.n;
   const long long units = static_cast<long long>(tp.row_tiles) * tp.vsplit;
   const int grid = pair_grid(c.dev.sms, units);
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
@@ -625,6 +641,8 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     tp.mref = c.mref();
     tp.zero_words = c.counter();  // the backward launch's tile counter and the fix-up list count start at zero
     tp.tile_counter = c.fcount() + r0 / c.L.rows;
+    tp.part_count = static_cast<int64_t>(kMaxSplit) * p.n;
+    tp.mtile_count = static_cast<int64_t>(c.L.rows) * vtiles;
     const double fflops = 2.0 * cr * static_cast<double>(v) * h;
     const int fgrid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
     st = cuda_status(timed(0, fflops, c.stream, [&] { return launch_tc(kModeFwdStore, fm, tp, fgrid, c.stream); }));
@@ -656,6 +674,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
     bp.row_end = r0 + cr;
     bp.b2_r0 = 0;
     bp.rowscale = c.rowscale();
+    bp.rowscale_count = c.L.rows;
     bp.scale = c.scale();
     bp.c0 = 0;
     bp.cw = v;
@@ -743,6 +762,8 @@ flce_status_t run_topk(const Ctx& c, int k, const void* X, const void* W, int32_
   tp.topk_idx = cand_idx;
   tp.topk_k = k;
   tp.tile_counter = c.fcount();  // a header word: zero since the call started
+  tp.part_count = static_cast<int64_t>(kMaxSplit) * p.n;
+  tp.topk_count = static_cast<int64_t>(kTopkSubranges) * p.n * kTopkMax;
   const double flops = 2.0 * static_cast<double>(p.n) * static_cast<double>(p.v) * static_cast<double>(p.h);
   const int grid = pair_grid(c.dev.sms, static_cast<long long>(tp.row_tiles) * tp.vsplit);
   flce_status_t st =
@@ -980,6 +1001,16 @@ flce_status_t flce_read_device_status(void* ws, flce_stream_t stream) {
   const int zero = 0;
   if (cudaMemcpy(ws, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return FLCE_ERR_NO_DEVICE_STATUS;
   return static_cast<flce_status_t>(word);
+}
+
+int flce_debug_checks(void) { return kDebugChecksBuild; }
+
+flce_status_t flce_selftest_bounds(void* ws, size_t ws_bytes, flce_stream_t stream) {
+  if (!ws || ws_bytes < kAlign) return FLCE_ERR_INVALID_ARGUMENT;
+  if (!aligned(ws, kAlign)) return FLCE_ERR_MISALIGNED;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(int), s) != cudaSuccess) return FLCE_ERR_CUDA;
+  return cuda_status(launch_bounds_selftest(static_cast<int*>(ws), s));
 }
 
 flce_status_t flce_selftest_timeout(void* ws, size_t ws_bytes, uint64_t limit_ns, flce_stream_t stream) {
@@ -1250,6 +1281,7 @@ const char* flce_status_string(flce_status_t s) {
     case FLCE_ERR_CUDA: return "CUDA error or unsupported device";
     case FLCE_ERR_NO_DEVICE_STATUS: return "could not read the device status word";
     case FLCE_ERR_EXCEEDS_STATIC_SCRATCH: return "n exceeds the fixed scratch of flce_forward_noalloc (32768 rows)";
+    case FLCE_ERR_BOUNDS: return "device: an index or TMA coordinate failed a check of the debug build";
     default: return "unknown status";
   }
 }

@@ -15,7 +15,34 @@ enum : int {
   kOk = 0,
   kErrLabel = 5,
   kErrTimeout = 6,
+  kErrBounds = 10,
 };
+
+// Builds with FLCE_DEBUG_CHECKS test every index the kernels compute against the
+// size of the buffer it addresses, and every TMA coordinate against its
+// alignment rule, before the access; a failed check records kErrBounds in the
+// status word and the access is skipped (no trap).  Release builds compile the
+// checks away.
+#ifdef FLCE_DEBUG_CHECKS
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+
+__device__ __forceinline__ bool in_bounds(int64_t i, int64_t n, int* status) {
+  if (!kDebugChecks) return true;
+  if (i >= 0 && i < n) return true;
+  atomicCAS(status, 0, kErrBounds);
+  return false;
+}
+
+// The innermost coordinate of a tiled TMA copy must start on a 16-byte boundary.
+__device__ __forceinline__ bool tma_x_ok(int x, int elem_bytes, int* status) {
+  if (!kDebugChecks) return true;
+  if ((x * elem_bytes) % 16 == 0) return true;
+  atomicCAS(status, 0, kErrBounds);
+  return false;
+}
 
 // Label of `row`: labels[row], or with shift labels[row + 1] and ignore_index
 // for the last row of each sequence of seq_len rows.

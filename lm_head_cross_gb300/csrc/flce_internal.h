@@ -96,6 +96,9 @@ struct TcParams {
   int topk_k;
   unsigned* topk_thr;   // top-k: per row the best 16th-best value any range has reached (ordered key), zeroed
   int units_group;      // forward modes: row tiles per unit group (see units_group_rows)
+  // element counts of the buffers above that are indexed by computed offsets (checked in
+  // builds with FLCE_DEBUG_CHECKS): part_m / part_l, mtile, topk_val / topk_idx, rowscale
+  int64_t part_count, mtile_count, topk_count, rowscale_count;
 };
 
 // Unit order of the forward modes: units (row tile, vocabulary range) run row
@@ -200,6 +203,9 @@ cudaError_t launch_shard_combine(int n, int parts, int64_t v_total, LabelView lv
                                  int* blk_valid, int* status, cudaStream_t stream);
 cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream_t stream);
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream);
+// One thread tests index 1 against a buffer of one element: builds with
+// FLCE_DEBUG_CHECKS record kErrBounds (and touch no memory), release builds nothing.
+cudaError_t launch_bounds_selftest(int* status, cudaStream_t stream);
 
 // Limit of every bounded wait in the kernels, in nanoseconds: FLCE_TIMEOUT_NS
 // from the environment (read once), else 4 s.

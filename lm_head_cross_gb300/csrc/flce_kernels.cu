@@ -300,21 +300,29 @@ __device__ void run_producer(const TcMaps& maps, const TcParams& p, const Pair& 
       const uint32_t bar = full_even + 8u * stage;
       if (pr.rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * kStageBytes);
       const int k0 = kb * kBK;
+      // (debug builds: a load whose inner coordinate breaks the 16-byte rule is skipped and
+      // recorded; the stage's transaction count then stays short and the bounded wait ends)
       if (t.kind <= 1 || t.kind == 4) {  // A = X [N,H] K-major, B = W [V,H] K-major
         const int vcol = (t.kind == 1) ? p.c0 + t.n0 : t.n0;
-        tma_load_2d_pair(sa, &maps.a, bar, k0, p.r0 + t.m0);
-        tma_load_2d_pair(sb, &maps.b, bar, k0, vcol + bhalf);
+        if (tma_x_ok(k0, 2, p.status)) {
+          tma_load_2d_pair(sa, &maps.a, bar, k0, p.r0 + t.m0);
+          tma_load_2d_pair(sb, &maps.b, bar, k0, vcol + bhalf);
+        }
       } else if (t.kind == 2) {  // dX: A = G K-major, B = W rows of the chunk, MN-major
-        tma_load_2d_pair(sa, &maps.a, bar, k0, t.m0);
+        if (tma_x_ok(k0, 2, p.status)) tma_load_2d_pair(sa, &maps.a, bar, k0, t.m0);
 #pragma unroll
         for (int j = 0; j < kHalfN / 64; ++j)
-          tma_load_2d_pair(sb + j * kMnBlock, &maps.b, bar, t.n0 + bhalf + 64 * j, p.c0 + k0);
+          if (tma_x_ok(t.n0 + bhalf + 64 * j, 2, p.status))
+            tma_load_2d_pair(sb + j * kMnBlock, &maps.b, bar, t.n0 + bhalf + 64 * j, p.c0 + k0);
       } else {  // dW: A = G^T (G MN-major), B = X MN-major; K runs over token rows
 #pragma unroll
-        for (int j = 0; j < kBM / 64; ++j) tma_load_2d_pair(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
+        for (int j = 0; j < kBM / 64; ++j)
+          if (tma_x_ok(t.m0 + 64 * j, 2, p.status))
+            tma_load_2d_pair(sa + j * kMnBlock, &maps.a2, bar, t.m0 + 64 * j, k0);
 #pragma unroll
         for (int j = 0; j < kHalfN / 64; ++j)
-          tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.b2_r0 + k0);
+          if (tma_x_ok(t.n0 + bhalf + 64 * j, 2, p.status))
+            tma_load_2d_pair(sb + j * kMnBlock, &maps.b2, bar, t.n0 + bhalf + 64 * j, p.b2_r0 + k0);
       }
       if (++stage == Cfg<MODE>::kStages) {
         stage = 0;
@@ -398,7 +406,9 @@ __device__ __forceinline__ void stage_rows(uint8_t* buf, int lane, const uint32_
 // Stage 32 rows x 128 B and hand them to TMA (store or reduce-add); two
 // alternating buffers per warp so the next tile overlaps the previous copy.
 __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t* stg, int& sbuf, int lane,
-                                                const uint32_t (&w)[32], int x, int y, bool reduce) {
+                                                const uint32_t (&w)[32], int x, int y, bool reduce,
+                                                int* status) {
+  if (!tma_x_ok(x, 4, status) || !in_bounds(y, INT32_MAX, status)) return;  // (y >= 0: no store starts above the tensor)
   uint8_t* buf = stg + sbuf * kStagingBuf;
   if (lane == 0) bulk_wait_group_read<1>();
   __syncwarp();
@@ -727,7 +737,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           const int nv = p.v - col0;
           uint32_t w[32];
           sum += exp_pack_group(v, w, nv, ref);
-          stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
+          stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false, p.status);
         }
         const bool over = !(sum <= kRefSumMax);  // also true for a non-finite sum
         if (__any_sync(0xffffffffu, over)) {
@@ -762,11 +772,12 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             uint32_t w[32];
             const float gs = exp_pack_group(v, w, p.v - col0, ref);
             if (over) sum += gs;
-            stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false);
+            stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false, p.status);
           }
         }
         release_accumulator(&tempty[acc], lane);
-        if (row < row_end) p.mtile[static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN] = ref;
+        const int64_t mi = static_cast<int64_t>(lrow) * p.vocab_tiles + t.n0 / kBN;
+        if (row < row_end && in_bounds(mi, p.mtile_count, p.status)) p.mtile[mi] = ref;
         const float new_m = fmaxf(run_m, ref);
         run_l = run_l * fast_exp2(run_m - new_m) + sum * fast_exp2(ref - new_m);
         run_m = new_m;
@@ -775,13 +786,17 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         topk_compact_lanes(tk, lane, __ballot_sync(0xffffffffu, tk.count > p.topk_k), p.topk_k);
       if (t.last && row < row_end) {
         const int osplit = (Cfg<MODE>::kEpiWarps == 8) ? 2 * t.split + ehalf : t.split;
-        p.part_m[static_cast<int64_t>(osplit) * p.n + row] = run_m;
-        p.part_l[static_cast<int64_t>(osplit) * p.n + row] = run_l;
-        if (found) p.tgt[row] = z_tgt;
+        const int64_t pi = static_cast<int64_t>(osplit) * p.n + row;
+        if (in_bounds(pi, p.part_count, p.status)) {
+          p.part_m[pi] = run_m;
+          p.part_l[pi] = run_l;
+        }
+        if (found && in_bounds(row, p.n, p.status)) p.tgt[row] = z_tgt;
         if (MODE == kModeTopk) {
           const int kept = tk.count;  // at most k (the merge does not need them sorted)
           const int64_t base = (static_cast<int64_t>(osplit) * p.n + row) * kTopkMax;
           for (int i = 0; i < kTopkMax; ++i) {
+            if (!in_bounds(base + i, p.topk_count, p.status)) break;
             p.topk_val[base + i] = i < kept ? tk.val[topk_slot(i, lane)] : -INFINITY;
             p.topk_idx[base + i] = i < kept ? tk.idx[topk_slot(i, lane)] : -1;
           }
@@ -811,7 +826,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           w[j] = pack_bf16x2(a, b);
         }
         // columns at or beyond the chunk width fall outside the store box's tensor and are dropped by TMA
-        stage_and_store(&maps.out, stg, sbuf, lane, w, t.n0 + g * 64, t.m0 + quarter * 32, false);
+        stage_and_store(&maps.out, stg, sbuf, lane, w, t.n0 + g * 64, t.m0 + quarter * 32, false, p.status);
       }
       release_accumulator(&tempty[acc], lane);
     } else {
@@ -828,7 +843,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
         osc = *p.scale;
         if (is_dx) {
           const int lr = t.m0 + quarter * 32 + lane;
-          osc = (p.r0 + lr < p.row_end) ? osc * p.rowscale[lr] : 0.f;
+          osc = (p.r0 + lr < p.row_end && in_bounds(lr, p.rowscale_count, p.status)) ? osc * p.rowscale[lr] : 0.f;
         }
       }
       if (omode == kOutF32AccToBF16) {
@@ -884,7 +899,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * osc, __uint_as_float(v[2 * j + 1]) * osc);
-          stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, false);
+          stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, false, p.status);
         }
       } else {
 #pragma unroll 1
@@ -895,7 +910,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           tmem_ld_32x32(tbase + c * 32, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * osc);
-          stage_and_store(omap, stg, sbuf, lane, v, t.n0 + c * 32, y0, omode == kOutF32Add);
+          stage_and_store(omap, stg, sbuf, lane, v, t.n0 + c * 32, y0, omode == kOutF32Add, p.status);
         }
       }
       release_accumulator(&tempty[acc], lane);
@@ -1341,7 +1356,8 @@ __global__ void __launch_bounds__(kRefRowsPerBlock * 32) finalize_ref_kernel(
       if (valid) {
         __nv_bfloat16* prow = P + static_cast<int64_t>(lrow) * vp;
         if (m > ref) {
-          fix_list[atomicAdd(fix_count, 1)] = lrow;
+          const int slot = atomicAdd(fix_count, 1);
+          if (in_bounds(slot, rows, status)) fix_list[slot] = lrow;
         } else if (k == 0) {
           // (p_iy - 1) 2^(lse2 - ref), p_iy = 2^(z_iy log2 e - lse2), from the fp32 logit
           prow[y] = __float2bfloat16_rn(exp2f(fmaf(z, kLog2e, -ref)) - exp2f(lse2 - ref));
@@ -1733,6 +1749,11 @@ __global__ void timeout_selftest_kernel(int* status, uint64_t limit_ns) {
   }
 }
 
+__global__ void bounds_selftest_kernel(int* status) {
+  griddep_begin();
+  if (threadIdx.x == 0) (void)in_bounds(1, 1, status);
+}
+
 }  // namespace
 
 int tc_smem_bytes() { return Cfg<kModeForward>::kSmemBytes; }
@@ -1891,6 +1912,10 @@ cudaError_t launch_scale_bf16(void* x, int64_t count, const float* g, cudaStream
   if (blocks < 1) blocks = 1;
   return launch_k(scale_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream,
                   static_cast<__nv_bfloat16*>(x), count8, g);
+}
+
+cudaError_t launch_bounds_selftest(int* status, cudaStream_t stream) {
+  return launch_k(bounds_selftest_kernel, dim3(1), dim3(32), 0, stream, status);
 }
 
 cudaError_t launch_timeout_selftest(int* status, uint64_t limit_ns, cudaStream_t stream) {

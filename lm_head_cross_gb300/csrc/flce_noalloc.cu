@@ -160,6 +160,7 @@ extern "C" flce_status_t flce_forward_noalloc(const flce_problem_t* p, const voi
   tp.part_l = part_l;
   tp.tgt = tgt;
   tp.tile_counter = reinterpret_cast<int*>(s + kOffStatus + 12);
+  tp.part_count = static_cast<int64_t>(kNoAllocSplit) * kNoAllocMaxRows;
   tp.labels = labels;
   tp.shift = p->shift;
   tp.seq_len = p->shift ? p->seq_len : 1;

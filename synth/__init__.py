@@ -138,6 +138,10 @@ WORKLOADS = {
     # to and read back) in a few GB of device memory, small enough for a full ncu capture
     "n24576_h2048_v65536": dict(n=24576, h=2048, v=65536, seed=5, x_std=1.0, w_std=0.02, labels="zipf",
             ignore_frac=0.05, reduction="mean", name="N=24576 H=2048 V=65536 (3 row chunks)"),
+    # not one of the five: the bounded path's kernels at the 128K x 128K workload's hidden size and
+    # vocabulary chunk width (4096, as for N > 16384), in about 1.4 GB of device memory
+    "n24576_h4096_v16384": dict(n=24576, h=4096, v=16384, seed=6, x_std=1.0, w_std=0.02, labels="uniform",
+            ignore_frac=0.03, reduction="mean", name="N=24576 H=4096 V=16384 (4 vocabulary chunks)"),
 }
 
 

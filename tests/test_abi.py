@@ -179,3 +179,18 @@ def test_shard_host_validation_without_gpu():
     assert L.flce_f32_to_bf16(None, None, 0, None) == 0
     assert L.flce_fwd_bwd_rowchunk(ctypes.byref(p), z, z, z, z, z, z, z, ws,
                                    flce.workspace_bytes(256, 128, 1000), None) in (4, 7)  # bounded size: too small
+
+
+def test_debug_build_loads_and_exports_the_same_symbols():
+    """libflce_debug.so (FLCE_DEBUG_CHECKS) is built beside the release library,
+    exports every declared symbol and reports its checks; the release build does not."""
+    lib = os.path.join(os.path.dirname(flce.lib_path()), "libflce_debug.so")
+    assert os.path.exists(lib), "build() makes the debug library too"
+    D = ctypes.CDLL(lib)
+    for name in _declared():
+        assert hasattr(D, name), name
+    assert D.flce_debug_checks() == 1
+    assert flce.lib().flce_debug_checks() == 0
+    D.flce_selftest_bounds.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_void_p]
+    assert D.flce_selftest_bounds(None, 256, None) == 1
+    assert D.flce_selftest_bounds(ctypes.c_void_p(0x100010), 256, None) == 3
