@@ -467,6 +467,31 @@ def test_oracle_full_on_tiny_workload_matches_torch():
     np.testing.assert_allclose(f["dW"], W.grad.numpy(), rtol=1e-9, atol=1e-15)
 
 
+def test_oracle_full_on_workload_8k_32k_matches_torch():
+    """The library special case at a benchmark size: the first 2500 rows of the
+    N 8192 x V 32000 workload (three row blocks of the oracle, the last one
+    ragged) against torch's fp64 cross_entropy and autograd on the CPU."""
+    torch = pytest.importorskip("torch")
+    import torch.nn.functional as F
+    p = synth.workload_problem(synth.DEFAULT_WORKLOAD)
+    rows = 2500
+    X = oracle.widen_bf16(p.X[:rows])
+    W = oracle.widen_bf16(p.W)
+    lab = p.labels[:rows]
+    blocks = list(oracle._row_blocks(rows, p.v))
+    assert len(blocks) == 3 and blocks[-1].size < blocks[0].size
+    f = oracle.full(X, W, lab, p.ignore_index, p.reduction)
+    Xt = torch.tensor(X, requires_grad=True)
+    Wt = torch.tensor(W, requires_grad=True)
+    z = Xt @ Wt.T
+    loss = F.cross_entropy(z, torch.tensor(lab.astype(np.int64)), ignore_index=p.ignore_index)
+    loss.backward()
+    assert abs(f["loss"] - loss.item()) <= 1e-12 * abs(loss.item())
+    np.testing.assert_allclose(f["lse"], torch.logsumexp(z.detach(), dim=1).numpy(), rtol=0, atol=1e-10)
+    np.testing.assert_allclose(f["dX"], Xt.grad.numpy(), rtol=0, atol=1e-12 * np.abs(Xt.grad.numpy()).max())
+    np.testing.assert_allclose(f["dW"], Wt.grad.numpy(), rtol=0, atol=1e-12 * np.abs(Wt.grad.numpy()).max())
+
+
 # ---------------------------------------------------------------- planted mistakes
 
 def _mutant(**overrides):
