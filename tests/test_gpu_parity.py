@@ -161,12 +161,13 @@ def test_separate_forward_backward_with_upstream_gradient():
 
 
 @pytest.mark.parametrize("upstream", [1.0, 2.5])
-def test_autograd_wrapper(upstream):
+@PATHS
+def test_autograd_wrapper(upstream, rowchunk):
     p = synth.make_problem(2 * 150, 128, 1500, seed=12, labels="zipf", ignore_frac=0.1)
     X, W, y = to_device(p)
     x3 = X.reshape(2, 150, 128).clone().requires_grad_(True)
     w = W.clone().requires_grad_(True)
-    loss = flce.linear_cross_entropy(x3, w, y.reshape(2, 150).long())
+    loss = flce.linear_cross_entropy(x3, w, y.reshape(2, 150).long(), rowchunk=rowchunk)
     (loss * upstream).backward()
     ref = oracle.full_bf16(p, grad_output=upstream)
     assert_loss(float(loss.item()), ref["loss"])

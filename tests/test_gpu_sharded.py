@@ -91,6 +91,35 @@ def test_vocab_shards_match_oracle(bounds_frac, reduction, shift):
         assert np.all(got["tgt_parts"][r][~own] == 0.0)
 
 
+def test_vocab_shards_random_shapes():
+    """12 seeded random problems (rows, hidden size, vocabulary, 2-5 uneven shards,
+    reduction, shift, ignore fraction) through the shard calls against the oracle."""
+    rng = np.random.default_rng(65)
+    for case in range(12):
+        seq = int(rng.integers(1, 4))
+        s_len = int(rng.integers(2, 160))
+        n = seq * s_len
+        h = 8 * int(rng.integers(1, 40))
+        v = int(rng.integers(8, 5000))
+        parts = int(rng.integers(2, 6))
+        cuts = np.sort(rng.choice(np.arange(1, v), size=min(parts - 1, v - 1), replace=False)).tolist()
+        bounds = [0] + cuts + [v]
+        red = ["mean", "sum"][case % 2]
+        shift = int(rng.integers(0, 2))
+        p = synth.make_problem(n, h, v, seed=2000 + case, labels=["uniform", "zipf"][case % 2],
+                               ignore_frac=float(rng.choice([0.0, 0.1, 0.4])), reduction=red,
+                               w_std=float(rng.choice([0.02, 0.1])))
+        got = run_shards(p, bounds, red, shift, s_len if shift else 0)
+        lab = oracle.shift_labels(p.labels, s_len, p.ignore_index) if shift else p.labels
+        ref = oracle.full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), lab, p.ignore_index, red)
+        what = f"case {case}: n={n} h={h} v={v} bounds={bounds} {red} shift={shift}"
+        assert abs(float(got["loss"][0]) - ref["loss"]) <= 1e-3 * max(abs(ref["loss"]), 1e-6), what
+        assert_lse(got["lse"], ref["lse"])
+        if np.abs(ref["dX"]).max() > 0:
+            assert_grad(got["dX"], ref["dX"], name="dX " + what)
+            assert_grad(got["dW"], ref["dW"], name="dW " + what)
+
+
 def test_shard_label_out_of_range_sets_status():
     p = synth.make_problem(300, 64, 1000, seed=62)
     p.labels[7] = 1000
