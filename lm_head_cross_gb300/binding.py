@@ -432,7 +432,8 @@ def shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index=-100, shif
 
 def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index=-100, reduction="mean", shift=0,
                   seq_len=0, ws=None, stream=None):
-    """lse_parts, tgt_parts: [P, N] fp32 (shard r in row r).  Returns (loss, lse [N], ws)."""
+    """lse_parts, tgt_parts: [P, N] fp32 (shard r in row r).  Returns (loss, lse [N], ws).
+    ``ws``: any workspace of a shard call (or of fwd_bwd) on the same rows serves."""
     torch = _torch()
     P, n = lse_parts.shape
     _f32(lse_parts, (P, n), "lse_parts")
@@ -473,7 +474,8 @@ def shard_backward(x, w_shard, labels, lse, v_offset, v_total, grad_loss=None, i
 
 
 def valid_count(labels, v, h=8, ignore_index=-100, shift=0, seq_len=0, ws=None, stream=None):
-    """Rows whose label is not ignore_index, as a one-element int32 CUDA tensor."""
+    """Rows whose label is not ignore_index, as a one-element int32 CUDA tensor.
+    ``ws``: any workspace of another call on the same rows serves."""
     torch = _torch()
     n = labels.shape[0]
     p = _problem(n, h, v, ignore_index, "sum", shift, seq_len)

@@ -27,34 +27,37 @@ from . import binding
 
 
 class LibraryOps:
-    """The per-rank steps, on the CUDA library."""
+    """The per-rank steps, on the CUDA library.  One workspace serves every step
+    of a call (``ws``: allocated by the first step, passed to the rest)."""
 
     @staticmethod
-    def shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index, shift, seq_len):
-        lse_p, tgt_p, _ = binding.shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index, shift, seq_len)
-        return lse_p, tgt_p
+    def shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index, shift, seq_len, ws=None):
+        lse_p, tgt_p, ws = binding.shard_forward(x, w_shard, labels, v_offset, v_total, ignore_index, shift,
+                                                 seq_len, ws=ws)
+        return lse_p, tgt_p, ws
 
     @staticmethod
-    def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift, seq_len):
-        loss, lse, _ = binding.shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, "sum", shift,
-                                             seq_len)
-        return loss, lse
+    def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift, seq_len, ws=None):
+        loss, lse, ws = binding.shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, "sum", shift,
+                                              seq_len, ws=ws)
+        return loss, lse, ws
 
     @staticmethod
-    def shard_backward(x, w_shard, labels, lse, v_offset, v_total, scale, ignore_index, shift, seq_len):
-        dXp, dWs, _ = binding.shard_backward(x, w_shard, labels, lse, v_offset, v_total, scale, ignore_index, "sum",
-                                             shift, seq_len)
-        return dXp, dWs
+    def shard_backward(x, w_shard, labels, lse, v_offset, v_total, scale, ignore_index, shift, seq_len, ws=None):
+        dXp, dWs, ws = binding.shard_backward(x, w_shard, labels, lse, v_offset, v_total, scale, ignore_index, "sum",
+                                              shift, seq_len, ws=ws)
+        return dXp, dWs, ws
 
     @staticmethod
-    def fwd_bwd(x, w, labels, ignore_index, shift, seq_len):
-        loss, lse, dX, dW, _ = binding.fwd_bwd(x, w, labels, ignore_index, "sum", shift=shift, seq_len=seq_len)
-        return loss, lse, dX, dW
+    def fwd_bwd(x, w, labels, ignore_index, shift, seq_len, ws=None):
+        loss, lse, dX, dW, ws = binding.fwd_bwd(x, w, labels, ignore_index, "sum", ws=ws, shift=shift,
+                                                seq_len=seq_len)
+        return loss, lse, dX, dW, ws
 
     @staticmethod
-    def valid_count(labels, v_total, ignore_index, shift, seq_len):
-        count, _ = binding.valid_count(labels, v_total, 8, ignore_index, shift, seq_len)
-        return count
+    def valid_count(labels, v_total, ignore_index, shift, seq_len, ws=None):
+        count, ws = binding.valid_count(labels, v_total, 8, ignore_index, shift, seq_len, ws=ws)
+        return count, ws
 
     @staticmethod
     def scale_grads(dX, dW, scale):
@@ -71,7 +74,7 @@ def _world(group):
 
 
 def sharded_cross_entropy(x, w, labels, *, v_offset=0, v_total=None, vocab_group=None, seq_group=None,
-                          ignore_index=-100, reduction="mean", shift=0, seq_len=0, ops=None):
+                          ignore_index=-100, reduction="mean", shift=0, seq_len=0, ops=None, check=False):
     """Loss, lse and gradients of this rank's piece of a sharded LM-head cross-entropy.
 
     x: [N_r, H] bf16, this rank's rows (its slice of the sequence when
@@ -86,12 +89,20 @@ def sharded_cross_entropy(x, w, labels, *, v_offset=0, v_total=None, vocab_group
     Returns (loss [1] fp32, lse [N_r] fp32 over the whole vocabulary,
     dX [N_r, H] bf16, dW [V_r, H] bf16): the loss is the same on every rank, dX
     covers this rank's rows, dW this rank's vocabulary rows summed over the
-    sequence group.
+    sequence group.  ``check=True`` reads the device status word after each
+    library step (a stream synchronisation each) and raises on a device error
+    (a label outside the vocabulary, a bounded wait that ran out).
     """
     import torch
     import torch.distributed as dist
 
     ops = ops or LibraryOps
+
+    def status(ws, step):
+        if check and ops is LibraryOps:
+            code = binding.read_device_status(ws)
+            if code != binding.FLCE_OK:
+                raise binding.FlceError(code, step)
     if reduction not in ("mean", "sum"):
         raise ValueError("sharded_cross_entropy takes reduction 'mean' or 'sum'")
     if shift and seq_group is not None and _world(seq_group) > 1:
@@ -103,16 +114,21 @@ def sharded_cross_entropy(x, w, labels, *, v_offset=0, v_total=None, vocab_group
         raise ValueError("a vocabulary shard needs the vocab_group it is part of")
 
     if vocab_split:
-        lse_p, tgt_p = ops.shard_forward(x, w, labels, v_offset, v_total, ignore_index, shift, seq_len)
+        lse_p, tgt_p, ws = ops.shard_forward(x, w, labels, v_offset, v_total, ignore_index, shift, seq_len)
+        status(ws, "shard_forward")
         mine = torch.stack([lse_p, tgt_p])                      # [2, N]
         parts = [torch.empty_like(mine) for _ in range(_world(vocab_group))]
         dist.all_gather(parts, mine, group=vocab_group)
         lse_parts = torch.stack([t[0] for t in parts]).contiguous()
         tgt_parts = torch.stack([t[1] for t in parts]).contiguous()
-        loss_sum, lse = ops.shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift, seq_len)
+        loss_sum, lse, ws = ops.shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift,
+                                              seq_len, ws=ws)
+        status(ws, "shard_combine")
     else:
-        loss_sum, lse, dX, dW = ops.fwd_bwd(x, w, labels, ignore_index, shift, seq_len)
-    count = ops.valid_count(labels, v_total, ignore_index, shift, seq_len)
+        loss_sum, lse, dX, dW, ws = ops.fwd_bwd(x, w, labels, ignore_index, shift, seq_len)
+        status(ws, "fwd_bwd")
+    count, ws = ops.valid_count(labels, v_total, ignore_index, shift, seq_len, ws=ws)
+    status(ws, "valid_count")
 
     # the loss sum and the valid count of the whole sequence
     totals = torch.cat([loss_sum.reshape(1).to(torch.float64), count.reshape(1).to(torch.float64)])
@@ -126,7 +142,9 @@ def sharded_cross_entropy(x, w, labels, *, v_offset=0, v_total=None, vocab_group
     scale32 = scale.to(torch.float32).reshape(1).contiguous()
 
     if vocab_split:
-        dXp, dW = ops.shard_backward(x, w, labels, lse, v_offset, v_total, scale32, ignore_index, shift, seq_len)
+        dXp, dW, ws = ops.shard_backward(x, w, labels, lse, v_offset, v_total, scale32, ignore_index, shift,
+                                         seq_len, ws=ws)
+        status(ws, "shard_backward")
         dist.all_reduce(dXp, group=vocab_group)
         dX = ops.f32_to_bf16(dXp)
     else:

@@ -171,7 +171,7 @@ def _worker(rank, world, port, out):
         bounds = [0, 900, p.v]
         a, b = bounds[rank], bounds[rank + 1]
         loss, lse, dX, dW = f.sharded_cross_entropy(X, W[a:b].contiguous(), y, v_offset=a, v_total=p.v,
-                                                    vocab_group=dist.group.WORLD)
+                                                    vocab_group=dist.group.WORLD, check=True)
         torch.cuda.synchronize()
         ref = oracle.full_bf16(p)
         assert abs(float(loss.item()) - ref["loss"]) <= 1e-3 * abs(ref["loss"])

@@ -36,7 +36,7 @@ class Float64Ops:
     """The per-rank steps in float64 on CPU tensors: what the library's calls compute."""
 
     @staticmethod
-    def shard_forward(x, w, labels, v_offset, v_total, ignore_index, shift, seq_len):
+    def shard_forward(x, w, labels, v_offset, v_total, ignore_index, shift, seq_len, ws=None):
         X, Wd = x.numpy(), w.numpy()
         y = _labels(labels, ignore_index, shift, seq_len)
         z = X @ Wd.T
@@ -45,20 +45,20 @@ class Float64Ops:
         own = (y != ignore_index) & (y >= v_offset) & (y < v_offset + w.shape[0])
         tgt = np.zeros(X.shape[0])
         tgt[own] = z[np.nonzero(own)[0], y[own] - v_offset]
-        return torch.from_numpy(lse), torch.from_numpy(tgt)
+        return torch.from_numpy(lse), torch.from_numpy(tgt), "ws"
 
     @staticmethod
-    def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift, seq_len):
+    def shard_combine(lse_parts, tgt_parts, labels, v_total, h, ignore_index, shift, seq_len, ws=None):
         lp, tp = lse_parts.numpy(), tgt_parts.numpy()
         m = lp.max(axis=0)
         lse = m + np.log(np.exp(lp - m).sum(axis=0))
         z = tp.sum(axis=0)
         y = _labels(labels, ignore_index, shift, seq_len)
         valid = y != ignore_index
-        return torch.tensor([np.where(valid, lse - z, 0.0).sum()]), torch.from_numpy(lse)
+        return torch.tensor([np.where(valid, lse - z, 0.0).sum()]), torch.from_numpy(lse), ws
 
     @staticmethod
-    def shard_backward(x, w, labels, lse, v_offset, v_total, scale, ignore_index, shift, seq_len):
+    def shard_backward(x, w, labels, lse, v_offset, v_total, scale, ignore_index, shift, seq_len, ws=None):
         X, Wd = x.numpy(), w.numpy()
         y = _labels(labels, ignore_index, shift, seq_len)
         valid = y != ignore_index
@@ -67,19 +67,19 @@ class Float64Ops:
         G[np.nonzero(own)[0], y[own] - v_offset] -= 1.0
         G[~valid] = 0.0
         G *= float(scale.item())
-        return torch.from_numpy(G @ Wd), torch.from_numpy(G.T @ X)
+        return torch.from_numpy(G @ Wd), torch.from_numpy(G.T @ X), ws
 
     @staticmethod
-    def fwd_bwd(x, w, labels, ignore_index, shift, seq_len):
+    def fwd_bwd(x, w, labels, ignore_index, shift, seq_len, ws=None):
         import oracle
         f = oracle.full(x.numpy(), w.numpy(), _labels(labels, ignore_index, shift, seq_len), ignore_index, "sum")
         return (torch.tensor([f["loss"]]), torch.from_numpy(f["lse"]), torch.from_numpy(f["dX"]),
-                torch.from_numpy(f["dW"]))
+                torch.from_numpy(f["dW"]), "ws")
 
     @staticmethod
-    def valid_count(labels, v_total, ignore_index, shift, seq_len):
+    def valid_count(labels, v_total, ignore_index, shift, seq_len, ws=None):
         return torch.tensor([int((_labels(labels, ignore_index, shift, seq_len) != ignore_index).sum())],
-                            dtype=torch.int32)
+                            dtype=torch.int32), ws
 
     @staticmethod
     def scale_grads(dX, dW, scale):
