@@ -72,7 +72,8 @@ typedef enum {
   FLCE_ERR_INVALID_ARGUMENT = 1,    /* null pointer, bad enum, n < 0, h/v < 1 */
   FLCE_ERR_UNSUPPORTED_SHAPE = 2,   /* h % 8 != 0, h < 8, or sizes beyond int32 tile coordinates */
   FLCE_ERR_MISALIGNED = 3,          /* a pointer breaks the alignment rules above */
-  FLCE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes < flce_workspace_bytes(p) */
+  FLCE_ERR_WORKSPACE_TOO_SMALL = 4, /* ws_bytes below the call's workspace size (flce_workspace_bytes(p), or
+                                       the row-chunk / shard / top-k / host-buffer size for those calls) */
   FLCE_ERR_LABEL_OUT_OF_RANGE = 5,  /* device: some label not in [0,V) and not ignore_index */
   FLCE_ERR_TIMEOUT = 6,             /* device: a bounded pipeline wait gave up (no hang, no trap) */
   FLCE_ERR_CUDA = 7,                /* a CUDA runtime/driver call failed, or no sm_100-family GPU */
