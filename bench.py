@@ -513,7 +513,6 @@ def e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, wor
 def run_flce(args, rank, world, local_rank):
     import torch
     import lm_head_cross_gb300 as flce
-    import synth
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
