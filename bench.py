@@ -527,7 +527,7 @@ def run_flce(args, rank, world, local_rank):
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream()
     reduction = args.reduction or problem.reduction
-    ws_bytes = ws_bytes_of(flce, rowchunk or args.op == "soft", problem, reduction)
+    ws_bytes = ws_bytes_of(flce, rowchunk, problem, reduction)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     out = (torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=dev),
            torch.empty(n, dtype=torch.float32, device=dev), torch.empty_like(X), torch.empty_like(W))
@@ -550,7 +550,7 @@ def run_flce(args, rank, world, local_rank):
         sq = torch.softmax(torch.randn(n, args.k, generator=g), dim=1).to(torch.float32).contiguous().to(dev)
 
         def step():
-            flce.soft_fwd_bwd(X, W, sidx, sq, reduction, ws=ws)
+            flce.soft_fwd_bwd(X, W, sidx, sq, reduction, ws=ws, rowchunk=rowchunk)
 
     if args.op != "fwd_bwd" or args.reduction or args.shift:
         return run_variant(args, step, n, h, v, world, dev, dist, torch, flce, flush, stream)

@@ -33,7 +33,7 @@
  *     alignment of the regions the library lays out in it), of at least
  *     flce_workspace_bytes(p) bytes: O(N*(C + H)) for a fixed chunk width C,
  *     independent of V.  The row-chunk calls (flce_fwd_bwd_rowchunk,
- *     flce_soft_fwd_bwd) keep a chunk of the vocabulary gradient instead and
+ *     flce_soft_fwd_bwd_rowchunk) keep a chunk of the vocabulary gradient instead and
  *     take flce_workspace_bytes_rowchunk(p); the vocabulary-shard calls take
  *     flce_shard_workspace_bytes(p, shard).  The workspace is the only extra
  *     device memory the library touches.  Calls that share a workspace must be
@@ -201,12 +201,17 @@ flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const
  *   loss_i = sum_k q_k log q_k - sum_k q_k log p_{id_k}      (KL(q || p) on the ids)
  *   G_ij   = s * (Q_i p_ij - sum_k q_k [j = id_k]),  Q_i = sum_k q_k
  * A row with Q_i = 0 is ignored; mean divides by the rows that are not.  k = 1,
- * q = 1 is the hard-label cross-entropy.  g = 1 as in flce_fwd_bwd; runs on
- * row chunks and needs flce_workspace_bytes_rowchunk(p).  shift must be 0;
- * labels unused. */
+ * q = 1 is the hard-label cross-entropy.  g = 1 as in flce_fwd_bwd.  shift must
+ * be 0; labels unused.  Like flce_fwd_bwd it runs on the bounded workspace of
+ * flce_workspace_bytes(p), the logits recomputed in the backward pass (each
+ * chunk of G formed as s Q_i p_ij, then the targets' -s q_k entered in place);
+ * flce_soft_fwd_bwd_rowchunk takes the row-chunk path and workspace instead. */
 flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
                                 const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
                                 void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
+flce_status_t flce_soft_fwd_bwd_rowchunk(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                                         const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse,
+                                         void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream);
 
 /* Synchronises `stream`, then returns the status word recorded in ws by the
  * kernels of earlier calls (FLCE_OK if none) and clears it.  The pages have no

@@ -21,7 +21,7 @@ REDUCTIONS = {"mean": 0, "sum": 1, "none": 2}
 EXPORTED = ("flce_workspace_bytes", "flce_workspace_bytes_rowchunk", "flce_forward", "flce_backward", "flce_fwd_bwd",
             "flce_fwd_bwd_rowchunk", "flce_read_device_status", "flce_selftest_timeout", "flce_profile_enable",
             "flce_profile_read", "flce_forward_noalloc", "flce_scale_grads", "flce_topk_workspace_bytes", "flce_topk",
-            "flce_soft_fwd_bwd", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_shard_workspace_bytes",
+            "flce_soft_fwd_bwd", "flce_soft_fwd_bwd_rowchunk", "flce_host_buffer_bytes", "flce_fwd_bwd_host", "flce_shard_workspace_bytes",
             "flce_shard_forward", "flce_shard_combine", "flce_shard_backward", "flce_valid_count",
             "flce_f32_to_bf16", "flce_debug_checks", "flce_selftest_bounds", "flce_status_string")
 KERNEL_KINDS = ("forward", "grad", "dxdw", "small")
@@ -93,6 +93,8 @@ def lib():
     L.flce_topk.restype = ctypes.c_int
     L.flce_soft_fwd_bwd.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
     L.flce_soft_fwd_bwd.restype = ctypes.c_int
+    L.flce_soft_fwd_bwd_rowchunk.argtypes = [P, ctypes.c_int32, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]
+    L.flce_soft_fwd_bwd_rowchunk.restype = ctypes.c_int
     L.flce_host_buffer_bytes.argtypes = [P]
     L.flce_host_buffer_bytes.restype = sz
     L.flce_fwd_bwd_host.argtypes = [P, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp, vp, vp]
@@ -328,9 +330,10 @@ def topk(x, w, k, ws=None, stream=None):
     return idx, val, lse, ws
 
 
-def soft_fwd_bwd(x, w, tgt_idx, tgt_prob, reduction="mean", ws=None, stream=None):
+def soft_fwd_bwd(x, w, tgt_idx, tgt_prob, reduction="mean", ws=None, stream=None, rowchunk=False):
     """KL of sparse soft targets (k ids and probabilities per row) against softmax(x @ w.T),
-    forward and backward.  Returns (loss, lse, dX, dW, ws)."""
+    forward and backward.  Returns (loss, lse, dX, dW, ws).  Bounded workspace by default;
+    ``rowchunk=True``: flce_soft_fwd_bwd_rowchunk."""
     torch = _torch()
     n, h = x.shape
     v = w.shape[0]
@@ -341,15 +344,15 @@ def soft_fwd_bwd(x, w, tgt_idx, tgt_prob, reduction="mean", ws=None, stream=None
     _check_inputs(x, w, torch.empty(n, dtype=torch.int32, device=x.device))
     p = _problem(n, h, v, -100, reduction)
     if ws is None:
-        ws = _alloc_ws(n, h, v, -100, reduction, x.device, rowchunk=True)
+        ws = _alloc_ws(n, h, v, -100, reduction, x.device, rowchunk=rowchunk)
     loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=x.device)
     lse = torch.empty(n, dtype=torch.float32, device=x.device)
     dX = torch.empty_like(x)
     dW = torch.empty_like(w)
-    _call("flce_soft_fwd_bwd", lib().flce_soft_fwd_bwd(ctypes.byref(p), k, x.data_ptr(), w.data_ptr(),
-                                                       tgt_idx.data_ptr(), tgt_prob.data_ptr(), loss.data_ptr(),
-                                                       lse.data_ptr(), dX.data_ptr(), dW.data_ptr(), ws.data_ptr(),
-                                                       ws.numel(), _stream_ptr(stream)))
+    name = "flce_soft_fwd_bwd_rowchunk" if rowchunk else "flce_soft_fwd_bwd"
+    _call(name, getattr(lib(), name)(ctypes.byref(p), k, x.data_ptr(), w.data_ptr(), tgt_idx.data_ptr(),
+                                     tgt_prob.data_ptr(), loss.data_ptr(), lse.data_ptr(), dX.data_ptr(),
+                                     dW.data_ptr(), ws.data_ptr(), ws.numel(), _stream_ptr(stream)))
     return loss, lse, dX, dW, ws
 
 
@@ -587,8 +590,8 @@ class _SparseKL:
 
             class Fn(torch.autograd.Function):
                 @staticmethod
-                def forward(ctx, x2, w, tgt_idx, tgt_prob, reduction):
-                    loss, _, dX, dW, _ = soft_fwd_bwd(x2, w, tgt_idx, tgt_prob, reduction)
+                def forward(ctx, x2, w, tgt_idx, tgt_prob, reduction, rowchunk):
+                    loss, _, dX, dW, _ = soft_fwd_bwd(x2, w, tgt_idx, tgt_prob, reduction, rowchunk=rowchunk)
                     ctx.save_for_backward(dX, dW)
                     return loss.reshape(())
 
@@ -597,20 +600,21 @@ class _SparseKL:
                     dX, dW = ctx.saved_tensors
                     g = grad.detach().to(torch.float32).reshape(1).contiguous()
                     scale_grads(dX, dW, g)
-                    return dX, dW, None, None, None
+                    return dX, dW, None, None, None, None
 
             cls.fn = Fn
         return cls.fn
 
 
-def sparse_kl_divergence(x, w, tgt_idx, tgt_prob, reduction: str = "mean"):
+def sparse_kl_divergence(x, w, tgt_idx, tgt_prob, reduction: str = "mean", rowchunk: bool = False):
     """KL(q || softmax(x @ w.T)) against sparse soft targets (a teacher's top-k ids
     and probabilities per row), without materialising the logits.
 
     x: [..., H] bf16 CUDA, w: [V, H] bf16, tgt_idx / tgt_prob: [..., k] (k <= 16)
     integer ids and fp32 probabilities; a row whose probabilities are all 0 is
     ignored.  reduction: 'mean' (over rows with targets) or 'sum'.  Autograd flows
-    to x and w.
+    to x and w.  Bounded, V-independent extra memory by default; ``rowchunk=True``
+    computes the logits once and keeps a row chunk of the vocabulary gradient.
     """
     torch = _torch()
     if reduction not in ("mean", "sum"):
@@ -620,4 +624,4 @@ def sparse_kl_divergence(x, w, tgt_idx, tgt_prob, reduction: str = "mean"):
     x2 = x.reshape(-1, h).contiguous()
     idx = tgt_idx.reshape(-1, k).to(torch.int32).contiguous()
     q = tgt_prob.reshape(-1, k).to(torch.float32).contiguous()
-    return _SparseKL.get().apply(x2, w.contiguous(), idx, q, reduction)
+    return _SparseKL.get().apply(x2, w.contiguous(), idx, q, reduction, bool(rowchunk))

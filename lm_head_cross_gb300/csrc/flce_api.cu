@@ -499,8 +499,12 @@ flce_status_t run_forward(const Ctx& c, const void* X, const void* W, const int3
 // Backward given lse and the scale already in the workspace.  dX accumulates
 // in fp32 in `dx_acc` (the workspace's accumulator, or a caller buffer) and is
 // written as bf16 to dX unless dX is null.
+// With soft targets (`soft`), grad_rows holds s Q_i per row, the grad launches
+// form s Q_i p_ij, and each chunk's target entries are subtracted in place before
+// its dX/dW launch.
 flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int32_t* labels, const float* lse,
-                           const float* grad_rows, void* dX, void* dW, float* dx_acc) {
+                           const float* grad_rows, void* dX, void* dW, float* dx_acc,
+                           const LabelView* soft = nullptr) {
   const flce_problem_t& p = *c.p;
   const int chunk = c.L.chunk;
   TcParams tp{};
@@ -514,6 +518,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   tp.shift = p.shift;
   tp.seq_len = p.shift ? p.seq_len : 1;
   tp.grad_rows = grad_rows;
+  tp.soft_grad = soft ? 1 : 0;
   tp.lse = lse;
   tp.scale = c.scale();
   tp.row_tiles = static_cast<int>((p.n + kPairRows - 1) / kPairRows);
@@ -543,6 +548,13 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
       return launch_tc(kModeGrad, gm, tp, pair_grid(c.dev.sms, gtiles), c.stream);
     }));
     if (st != FLCE_OK) return st;
+    if (soft) {
+      st = cuda_status(timed(3, 0.0, c.stream, [&] {
+        return launch_soft_chunk_targets(tp.n, soft->soft_k, soft->soft_idx, soft->soft_prob, c.scale(), tp.c0, cw,
+                                         chunk, c.g(), tp.v, c.status(), c.stream);
+      }));
+      if (st != FLCE_OK) return st;
+    }
 
     if (!make_map(&bm.a, c.g(), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, cw, p.n, static_cast<uint64_t>(chunk) * 2, kBK, kBM))
       return FLCE_ERR_CUDA;
@@ -567,6 +579,43 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   }
   if (!dX) return FLCE_OK;
   return cuda_status(timed(3, 0.0, c.stream, [&] { return launch_convert_bf16(dx_acc, dX, p.n * p.h, c.stream); }));
+}
+
+// Soft targets on the bounded workspace (8NHV executed): the targets' q-weighted
+// logits and the valid count (label_prep_kernel, its row references and block
+// counts going to the free chunk buffer), the forward's log-sum-exp, the KL
+// rows and their reduction, then the recompute backward with the per-row
+// coefficient s Q_i and each chunk's target entries subtracted in place.
+flce_status_t run_soft_bounded(const Ctx& c, const void* X, const void* W, const LabelView lv, float* loss, float* lse,
+                               void* dX, void* dW) {
+  const flce_problem_t& p = *c.p;
+  const int n = static_cast<int>(p.n);
+  float* scratch = static_cast<float*>(c.g());  // free until the first grad launch
+  flce_status_t st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_label_prep(n, static_cast<int>(p.h), static_cast<int>(p.v), p.reduction, lv, X, W, scratch,
+                             c.tgt(), reinterpret_cast<int*>(scratch + p.n), c.ticket(), c.n_valid(), c.scale(),
+                             c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  int vsplit = 0;
+  st = run_forward_tc(c, X, W, nullptr, &vsplit);
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_fwd_finalize_rows(0, n, n, static_cast<int>(p.v), vsplit, lv, c.part_m(), c.part_l(), c.tgt(), lse,
+                                    c.per_row() ? loss : nullptr, c.blk_loss(), c.blk_valid(), c.status(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_reduce_final(c.L.nblk, c.blk_loss(), c.blk_valid(), p.reduction, nullptr,
+                               c.per_row() ? nullptr : loss, c.n_valid(), c.scale(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  // the target logits are consumed: their array now holds s Q_i
+  st = cuda_status(timed(3, 0.0, c.stream, [&] {
+    return launch_soft_rowcoef(n, lv.soft_k, lv.soft_prob, c.scale(), c.tgt(), c.stream);
+  }));
+  if (st != FLCE_OK) return st;
+  return run_backward(c, X, W, nullptr, lse, c.tgt(), dX, dW, c.dx_acc(), &lv);
 }
 
 // Fused forward + backward over row chunks (6NHV executed, no recompute):
@@ -1044,9 +1093,10 @@ flce_status_t flce_topk(const flce_problem_t* p, int32_t k, const void* X, const
   return run_topk(c, k, X, W, topk_idx, topk_logit, lse);
 }
 
-flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
-                                const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
-                                void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+namespace {
+flce_status_t soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                           const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
+                           void* dW, void* ws, size_t ws_bytes, flce_stream_t stream, bool rowchunk) {
   if (!p || !W || !dW || !rows_ok(p, X) || !rows_ok(p, tgt_idx) || !rows_ok(p, tgt_prob) || !rows_ok(p, lse) ||
       !rows_ok(p, dX) || !(loss || (p->n == 0 && p->reduction == FLCE_REDUCTION_NONE)))
     return FLCE_ERR_INVALID_ARGUMENT;
@@ -1059,10 +1109,24 @@ flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* 
   if (st != FLCE_OK) return st;
   if (p->n == 0) return run_empty(p, loss, dW, ws, ws_bytes, stream);
   Ctx c;
-  st = prepare(&c, p, ws, ws_bytes, stream, Lay::kRowChunk);
+  st = prepare(&c, p, ws, ws_bytes, stream, rowchunk ? Lay::kRowChunk : Lay::kBounded);
   if (st != FLCE_OK) return st;
   const LabelView lv{nullptr, p->ignore_index, 0, 1, tgt_idx, tgt_prob, k};
-  return run_fused(c, X, W, lv, loss, lse, dX, dW);
+  if (rowchunk) return run_fused(c, X, W, lv, loss, lse, dX, dW);
+  return run_soft_bounded(c, X, W, lv, loss, lse, dX, dW);
+}
+}  // namespace
+
+flce_status_t flce_soft_fwd_bwd(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                                const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse, void* dX,
+                                void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  return soft_fwd_bwd(p, k, X, W, tgt_idx, tgt_prob, loss, lse, dX, dW, ws, ws_bytes, stream, false);
+}
+
+flce_status_t flce_soft_fwd_bwd_rowchunk(const flce_problem_t* p, int32_t k, const void* X, const void* W,
+                                         const int32_t* tgt_idx, const float* tgt_prob, float* loss, float* lse,
+                                         void* dX, void* dW, void* ws, size_t ws_bytes, flce_stream_t stream) {
+  return soft_fwd_bwd(p, k, X, W, tgt_idx, tgt_prob, loss, lse, dX, dW, ws, ws_bytes, stream, true);
 }
 
 // ----------------------------------------------------------------------------- vocabulary / sequence shards

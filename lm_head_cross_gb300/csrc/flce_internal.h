@@ -99,6 +99,7 @@ struct TcParams {
   // element counts of the buffers above that are indexed by computed offsets (checked in
   // builds with FLCE_DEBUG_CHECKS): part_m / part_l, mtile, topk_val / topk_idx, rowscale
   int64_t part_count, mtile_count, topk_count, rowscale_count;
+  int soft_grad;        // grad: soft targets (every row valid, no one-hot; grad_rows carries s Q_i)
 };
 
 // Unit order of the forward modes: units (row tile, vocabulary range) run row
@@ -184,6 +185,14 @@ cudaError_t launch_reduce_final(int nblk, const double* blk_loss, const int* blk
 cudaError_t launch_convert_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
 // fp32 -> bf16 (round to nearest even) of any count; src and dst 16-byte aligned.
 cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t count, cudaStream_t stream);
+
+// Soft targets on the bounded path: per row s Q_i (the grad launch's
+// coefficient), and a vocabulary chunk's target entries G_ij -= s q_k in place.
+cudaError_t launch_soft_rowcoef(int n, int k, const float* soft_prob, const float* scale, float* coef,
+                               cudaStream_t stream);
+cudaError_t launch_soft_chunk_targets(int n, int k, const int32_t* soft_idx, const float* soft_prob,
+                                      const float* scale, int c0, int cw, int64_t pitch, void* G, int v, int* status,
+                                      cudaStream_t stream);
 
 // Vocabulary shards.  A shard's kernels read labels in shard-local form: -1 for an
 // ignored row (the shard calls run with ignore_index -1), y - v0 for a label the

@@ -804,8 +804,11 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
       }
     } else if (MODE == kModeGrad) {
       const int row = t.m0 + r;
-      const int y = (row < p.n) ? label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index) : p.ignore_index;
-      const bool valid = (row < p.n) && (y != p.ignore_index);
+      // soft targets: G / s = Q p here (the per-row coefficient carries s Q_i), the
+      // targets' -s q_k are subtracted from the stored chunk afterwards
+      const int y = (row >= p.n) ? p.ignore_index
+                                 : (p.soft_grad ? kNotOwned : label_at(p.labels, row, p.shift, p.seq_len, p.ignore_index));
+      const bool valid = (row < p.n) && (p.soft_grad || y != p.ignore_index);
       const float coef = valid ? (p.grad_rows ? p.grad_rows[row] : scale) : 0.f;
       const float lse2 = (row < p.n) ? p.lse[row] * kLog2e : 0.f;
       const int ycol = y - (p.c0 + t.n0);  // label position inside this tile (if any)
@@ -1081,13 +1084,30 @@ __global__ void __launch_bounds__(kFinalizeThreads) fwd_finalize_kernel(
     float m;
     const float lse = merge_ranges(part_m, part_l, vsplit, n, row, &m) * kLn2;
     lse_out[row] = lse;
-    const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
-    if (y != ignore_index) {
-      if (y >= 0 && y < v) {
+    if (lv.soft_k > 0) {
+      // KL(q || p) over the row's targets: sum_t q_t log q_t + Q lse - sum_t q_t z_t, Q = sum_t q_t
+      // (tgt holds sum_t q_t z_t; target ids were checked when it was gathered)
+      double qd = 0.0, cd = 0.0;
+      for (int t = 0; t < lv.soft_k; ++t) {
+        const float q = lv.soft_prob[static_cast<int64_t>(row) * lv.soft_k + t];
+        if (q > 0.f) {
+          qd += static_cast<double>(q);
+          cd += static_cast<double>(q) * log(static_cast<double>(q));
+        }
+      }
+      if (qd > 0.0) {
         valid = 1;
-        li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
-      } else {
-        atomicCAS(status, 0, kErrLabel);
+        li = cd + qd * static_cast<double>(lse) - static_cast<double>(tgt[row]);
+      }
+    } else {
+      const int y = label_at(lv.labels, row, lv.shift, lv.seq_len, ignore_index);
+      if (y != ignore_index) {
+        if (y >= 0 && y < v) {
+          valid = 1;
+          li = static_cast<double>(lse) - static_cast<double>(tgt[row]);
+        } else {
+          atomicCAS(status, 0, kErrLabel);
+        }
       }
     }
     if (loss_rows) loss_rows[row] = static_cast<float>(li);
@@ -1630,6 +1650,44 @@ __global__ void f32_to_bf16_kernel(const float* __restrict__ src, __nv_bfloat16*
   for (int64_t i = 8 * count8 + tid; i < count; i += stride) dst[i] = __float2bfloat16_rn(src[i]);
 }
 
+// ----------------------------------------------------------------------------- soft targets, bounded path
+
+// Per row the gradient coefficient s Q_i (Q_i = the row's target mass; 0 for a
+// row without targets), s the device scalar of the reduction.
+__global__ void soft_rowcoef_kernel(int n, int k, const float* __restrict__ soft_prob, const float* __restrict__ scale,
+                                    float* __restrict__ coef) {
+  griddep_begin();
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  float Q = 0.f;
+  for (int t = 0; t < k; ++t) {
+    const float q = soft_prob[static_cast<int64_t>(row) * k + t];
+    if (q > 0.f) Q += q;
+  }
+  coef[row] = *scale * Q;
+}
+
+// One vocabulary chunk of bf16 G, [n, pitch] with columns [c0, c0 + cw): the
+// targets' term, G_ij -= s q_k at j = id_k, in place.  One thread per row takes
+// the row's targets in order, so repeated ids add up.
+__global__ void soft_chunk_targets_kernel(int n, int k, const int32_t* __restrict__ soft_idx,
+                                          const float* __restrict__ soft_prob, const float* __restrict__ scale,
+                                          int c0, int cw, int64_t pitch, __nv_bfloat16* __restrict__ G, int v,
+                                          int* __restrict__ status) {
+  griddep_begin();
+  const int row = blockIdx.x * blockDim.x + threadIdx.x;
+  if (row >= n) return;
+  const float s = *scale;
+  for (int t = 0; t < k; ++t) {
+    const float q = soft_prob[static_cast<int64_t>(row) * k + t];
+    const int id = soft_idx[static_cast<int64_t>(row) * k + t];
+    if (!(q > 0.f) || id < c0 || id >= c0 + cw || id >= v) continue;
+    const int64_t at = static_cast<int64_t>(row) * pitch + (id - c0);
+    if (!in_bounds(at, static_cast<int64_t>(n) * pitch, status)) continue;
+    G[at] = __float2bfloat16_rn(__bfloat162float(G[at]) - s * q);
+  }
+}
+
 // ----------------------------------------------------------------------------- vocabulary shards
 // ("What-Each-Parallelism-Actually-Shards" §7.2: each rank covers one range of the
 // vocabulary; ranks without the label still take part in the global max and
@@ -1874,6 +1932,18 @@ cudaError_t launch_f32_to_bf16(const float* src, void* dst, int64_t count, cudaS
   if (blocks < 1) blocks = 1;
   return launch_k(f32_to_bf16_kernel, dim3(static_cast<int>(blocks)), dim3(256), 0, stream, src,
                   static_cast<__nv_bfloat16*>(dst), count);
+}
+
+cudaError_t launch_soft_rowcoef(int n, int k, const float* soft_prob, const float* scale, float* coef,
+                               cudaStream_t stream) {
+  return launch_k(soft_rowcoef_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, n, k, soft_prob, scale, coef);
+}
+
+cudaError_t launch_soft_chunk_targets(int n, int k, const int32_t* soft_idx, const float* soft_prob,
+                                      const float* scale, int c0, int cw, int64_t pitch, void* G, int v, int* status,
+                                      cudaStream_t stream) {
+  return launch_k(soft_chunk_targets_kernel, dim3((n + 255) / 256), dim3(256), 0, stream, n, k, soft_idx, soft_prob,
+                  scale, c0, cw, pitch, static_cast<__nv_bfloat16*>(G), v, status);
 }
 
 cudaError_t launch_shard_labels(int n, int64_t v_total, int64_t v0, int64_t vs, LabelView lv, int32_t* lab_local,

@@ -37,6 +37,18 @@ def main():
             assert_lse(lse.cpu().numpy(), ref["lse"])
             assert_grad(dX.float().cpu().numpy(), ref["dX"], name="dX")
             assert_grad(dW.float().cpu().numpy(), ref["dW"], name="dW")
+        rng = np.random.default_rng(p.n)
+        sidx = rng.integers(0, p.v, size=(p.n, 4)).astype(np.int32)
+        sq = rng.random((p.n, 4)).astype(np.float32)
+        sq /= sq.sum(axis=1, keepdims=True)
+        sref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), sidx, sq.astype(np.float64), "mean")
+        for rowchunk in (False, True):
+            loss, lse_s, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(sidx).cuda(), torch.from_numpy(sq).cuda(),
+                                                        "mean", rowchunk=rowchunk)
+            assert flce.read_device_status(ws) == 0, ("soft", p.n, rowchunk)
+            assert_loss(float(loss.item()), sref["loss"])
+            assert_grad(dX.float().cpu().numpy(), sref["dX"], name="soft dX")
+            assert_grad(dW.float().cpu().numpy(), sref["dW"], name="soft dW")
         idx, val, lse_t, ws = flce.topk(X, W, 8)
         assert flce.read_device_status(ws) == 0
         oi, ov, _ = oracle.topk(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), 8)

@@ -41,14 +41,20 @@ def _teacher_targets(n, h, v, k, seed):
     return idx.astype(np.int32), q.astype(np.float32)
 
 
+# the soft-target KL on the bounded path (flce_soft_fwd_bwd) and the row-chunk path
+PATHS = pytest.mark.parametrize("rowchunk", [False, True], ids=["bounded", "rowchunk"])
+
+
 @pytest.mark.parametrize("red", ["mean", "sum", "none"])
-def test_soft_targets_match_oracle(red):
+@PATHS
+def test_soft_targets_match_oracle(red, rowchunk):
     n, h, v, k = 1500, 128, 4001, 8
     idx, q = _teacher_targets(n, h, v, k, seed=81)
     q[7] = 0.0                                                      # a row without targets
     p = synth.make_problem(n, h, v, seed=82, w_std=0.05)
     X, W, _ = to_device(p)
-    loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), red)
+    loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), red,
+                                              rowchunk=rowchunk)
     assert flce.read_device_status(ws) == 0
     ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), red)
     if red == "none":
@@ -63,28 +69,32 @@ def test_soft_targets_match_oracle(red):
     assert torch.count_nonzero(dX[7]).item() == 0
 
 
-def test_soft_k1_equals_hard_labels():
+@PATHS
+def test_soft_k1_equals_hard_labels(rowchunk):
     p = synth.make_problem(700, 192, 3000, seed=83, labels="zipf", ignore_frac=0.0)
     X, W, y = to_device(p)
-    a = flce.fwd_bwd(X, W, y, p.ignore_index, "mean")
-    b = flce.soft_fwd_bwd(X, W, y.reshape(-1, 1).contiguous(), torch.ones(700, 1, device="cuda"), "mean")
+    a = flce.fwd_bwd(X, W, y, p.ignore_index, "mean", rowchunk=rowchunk)
+    b = flce.soft_fwd_bwd(X, W, y.reshape(-1, 1).contiguous(), torch.ones(700, 1, device="cuda"), "mean",
+                          rowchunk=rowchunk)
     assert abs(float(a[0].item()) - float(b[0].item())) <= 1e-5 * abs(float(a[0].item()))
     assert (a[2].float() - b[2].float()).abs().max().item() <= 1e-2 * a[2].float().abs().max().item()
     assert (a[3].float() - b[3].float()).abs().max().item() <= 1e-2 * a[3].float().abs().max().item()
 
 
-def test_soft_target_id_out_of_range_sets_status():
+@PATHS
+def test_soft_target_id_out_of_range_sets_status(rowchunk):
     p = synth.make_problem(256, 64, 300, seed=84)
     X, W, _ = to_device(p)
     idx = torch.zeros(256, 2, dtype=torch.int32, device="cuda")
     idx[:, 1] = 1
     idx[10, 1] = 300
     q = torch.full((256, 2), 0.5, device="cuda")
-    _, _, _, _, ws = flce.soft_fwd_bwd(X, W, idx, q)
+    _, _, _, _, ws = flce.soft_fwd_bwd(X, W, idx, q, rowchunk=rowchunk)
     assert flce.read_device_status(ws) == 5
 
 
-def test_soft_targets_wide_logit_range_and_repeated_ids():
+@PATHS
+def test_soft_targets_wide_logit_range_and_repeated_ids(rowchunk):
     """Rows whose logits spread far past the reference span (×16 and ×64 rows: the
     list fix-up with soft targets), and a row that names one id twice (its two
     probabilities add), over two row chunks."""
@@ -95,7 +105,8 @@ def test_soft_targets_wide_logit_range_and_repeated_ids():
     xf = synth.bf16_bits_to_f32(p.X) * np.array([1.0, 16.0, 64.0], np.float32)[np.arange(n) % 3][:, None]
     p.X = synth.f32_to_bf16_bits(xf)
     X, W, _ = to_device(p)
-    loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), "mean")
+    loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), "mean",
+                                              rowchunk=rowchunk)
     assert flce.read_device_status(ws) == 0
     ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), "mean")
     assert_loss(float(loss.item()), ref["loss"])
@@ -158,10 +169,11 @@ def test_soft_targets_random_shapes():
         q[rng.random(n) < 0.1] = 0.0                                # rows without targets
         p = synth.make_problem(n, h, v, seed=900 + case, x_std=float(rng.choice([0.5, 1.0, 4.0])), w_std=0.05)
         X, W, _ = to_device(p)
-        loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), red)
+        loss, lse, dX, dW, ws = flce.soft_fwd_bwd(X, W, torch.from_numpy(idx).cuda(), torch.from_numpy(q).cuda(), red,
+                                                  rowchunk=bool(case % 2))
         assert flce.read_device_status(ws) == 0, case
         ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), red)
-        what = f"case {case}: n={n} h={h} v={v} k={k} {red}"
+        what = f"case {case}: n={n} h={h} v={v} k={k} {red} rowchunk={case % 2}"
         if red == "none":
             got = loss.cpu().numpy()
             assert np.abs(got - ref["loss"]).max() <= 2e-3 + 1e-3 * np.abs(ref["loss"]).max(), what
@@ -174,7 +186,8 @@ def test_soft_targets_random_shapes():
 
 
 @pytest.mark.parametrize("red,upstream", [("mean", 1.0), ("sum", 0.5)])
-def test_sparse_kl_autograd(red, upstream):
+@PATHS
+def test_sparse_kl_autograd(red, upstream, rowchunk):
     """The autograd wrapper of the soft-target KL: loss and the gradients reaching
     x and w match the oracle (times the upstream gradient)."""
     n, h, v, k = 2 * 300, 128, 3001, 4
@@ -184,7 +197,7 @@ def test_sparse_kl_autograd(red, upstream):
     x3 = X.reshape(2, 300, h).clone().requires_grad_(True)
     w = W.clone().requires_grad_(True)
     loss = flce.sparse_kl_divergence(x3, w, torch.from_numpy(idx).cuda().reshape(2, 300, k),
-                                     torch.from_numpy(q).cuda().reshape(2, 300, k), red)
+                                     torch.from_numpy(q).cuda().reshape(2, 300, k), red, rowchunk=rowchunk)
     (loss * upstream).backward()
     ref = oracle.soft_full(oracle.widen_bf16(p.X), oracle.widen_bf16(p.W), idx, q.astype(np.float64), red,
                            grad_output=upstream)
