@@ -241,8 +241,7 @@ int choose_vsplit_uncached(int row_tiles, int vocab_tiles, int grid, int cap, in
     for (long long u = 0; u < units; ++u) {
       int rt = 0, sp = 0;
       unit_coords(static_cast<int>(u), row_tiles, vs, group, &rt, &sp);
-      const long long tiles =
-          (static_cast<long long>(sp + 1) * vocab_tiles / vs) - (static_cast<long long>(sp) * vocab_tiles / vs);
+      const long long tiles = range_begin(sp + 1, vocab_tiles, vs) - range_begin(sp, vocab_tiles, vs);
       std::pop_heap(heap.begin(), heap.end(), cmp);
       heap.back().first += tiles;
       makespan = std::max(makespan, heap.back().first);

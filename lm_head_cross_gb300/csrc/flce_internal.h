@@ -114,6 +114,15 @@ inline int units_group_rows(int row_tiles, int64_t h) {
   return static_cast<int>(g < row_tiles ? g : row_tiles);
 }
 
+// First vocabulary tile of range sp when vocab_tiles tiles are cut into vsplit
+// ranges: the first (vocab_tiles % vsplit) ranges take one tile more than the
+// rest, so the units handed out last (the highest ranges) are the smaller ones.
+FLCE_HOST_DEVICE inline int range_begin(int sp, int vocab_tiles, int vsplit) {
+  const int base = vocab_tiles / vsplit;
+  const int rem = vocab_tiles % vsplit;
+  return sp * base + (sp < rem ? sp : rem);
+}
+
 // The (row tile, range) of unit u in that order.
 FLCE_HOST_DEVICE inline void unit_coords(int u, int row_tiles, int vsplit, int group, int* rt, int* sp) {
   const int per_group = group * vsplit;

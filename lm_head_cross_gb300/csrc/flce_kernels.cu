@@ -126,8 +126,8 @@ __device__ __forceinline__ void fwd_unit_begin(const TcParams& p, Sched& s) {
     return;
   }
   unit_coords(s.unit, p.row_tiles, p.vsplit, p.units_group, &s.rt, &s.sp);
-  s.vt = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
-  s.ve = static_cast<int>(static_cast<int64_t>(s.sp + 1) * p.vocab_tiles / p.vsplit);
+  s.vt = range_begin(s.sp, p.vocab_tiles, p.vsplit);
+  s.ve = range_begin(s.sp + 1, p.vocab_tiles, p.vsplit);
 }
 
 template <int MODE>
@@ -148,7 +148,7 @@ __device__ __forceinline__ bool sched_get(const TcParams& p, const Pair& pr, con
   const int half = static_cast<int>(pr.rank) * kBM;
   if (kUnits<MODE>) {
     if (s.done) return false;
-    const int vb = static_cast<int>(static_cast<int64_t>(s.sp) * p.vocab_tiles / p.vsplit);
+    const int vb = range_begin(s.sp, p.vocab_tiles, p.vsplit);
     t.m0 = s.rt * kPairM + half;  // row inside the chunk [r0, row_end)
     t.n0 = s.vt * kBN;
     t.kblocks = ceil_div(p.h, kBK);
