@@ -56,6 +56,7 @@ def test_tiny_workload_full(rowchunk):
     (640, 256, 17000, "mean", "zipf"),        # three backward vocabulary chunks, ragged last chunk
     (1000, 520, 8200, "sum", "uniform"),      # chunk boundary + 8 past it; H not a tile multiple
     (1500, 128, 4001, "mean", "zipf"),        # fused path: two row chunks, the last one ragged; odd V
+    (70, 64, 262147, "mean", "uniform"),      # 2^18 + 3 ids: 1025 vocabulary tiles, 33 backward chunks
 ])
 @PATHS
 def test_ragged_shapes(n, h, v, red, labels, rowchunk):
