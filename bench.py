@@ -483,6 +483,9 @@ def e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, wor
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
+    clocks = ClockSampler(dev.index if dev.index is not None else 0)
+    clocks.start()
+    clocks.mark_start()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for st_ in (comp, cin, cout):
@@ -494,6 +497,8 @@ def e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, wor
         stream.wait_event(fin)
     e1.record(stream)
     torch.cuda.synchronize()
+    clocks.mark_end()
+    clk = clocks.stop() or {}
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
     for _, buf, _ in slots:
         st_code = flce.read_device_status(buf)
@@ -503,8 +508,12 @@ def e2e_measure(args, flce, torch, dev, dist, problem, X, W, y, out, stream, wor
     h2d = sum(t.numel() * t.element_size() for t in (X, W, y))
     d2h = sum(t.numel() * t.element_size() for t in out)
 
-    return {"value": job_tflops(world, flops, args.e2e_steps, e2e_ms), "unit": UNIT,
+    e2e_value = job_tflops(world, flops, args.e2e_steps, e2e_ms)
+    return {"value": e2e_value, "unit": UNIT,
+            "tflops_per_ghz": e2e_value / world / (clk["sm_mhz"] / 1e3) if clk.get("sm_mhz") else None,
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": args.e2e_steps,
+            "clocks": {k: clk.get(k) for k in ("sm_mhz", "sm_mhz_min", "reasons", "samples", "power_cap_frac",
+                                               "power_w_instant_median")},
             "note": "flce_fwd_bwd_host (bounded path) through the C-ABI: pinned host X, W, labels copied in "
                     "and loss, lse, dX, dW copied out every step, on their own streams; two device buffers "
                     "alternate so copies overlap the neighbouring steps' kernels"}
