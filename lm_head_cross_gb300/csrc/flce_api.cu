@@ -526,11 +526,11 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
   TcMaps gm;  // grad: X, W K-major; G store
   if (!make_map(&gm.a, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, kBK, kBM)) return FLCE_ERR_CUDA;
   if (!make_map(&gm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, kBK, kBoxB)) return FLCE_ERR_CUDA;
-  TcMaps bm;  // bwd: W MN-major (dX B operand), X MN-major (dW B operand), dX fp32 acc, dW store
+  TcMaps bm;  // bwd: W MN-major (dX B operand), X MN-major (dW B operand), dW store; dX goes to dx_acc directly
   if (!make_map(&bm.b, W, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.b2, X, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.n, p.h * 2, 64, kBK)) return FLCE_ERR_CUDA;
-  if (!make_map(&bm.out, dx_acc, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.h, p.n, p.h * 4, 32, 32)) return FLCE_ERR_CUDA;
   if (!make_map(&bm.out2, dW, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.h, p.v, p.h * 2, 64, 32)) return FLCE_ERR_CUDA;
+  bm.out = bm.out2;  // unused by these tiles (a valid map for the prologue's prefetch)
 
   for (int64_t c0 = 0; c0 < p.v; c0 += chunk) {
     const int cw = static_cast<int>(std::min<int64_t>(chunk, p.v - c0));
@@ -563,6 +563,7 @@ flce_status_t run_backward(const Ctx& c, const void* X, const void* W, const int
     tp.dw_tiles = tp.dw_m_tiles * tp.h_tiles;
     tp.dx_tiles = tp.row_tiles * tp.h_tiles;
     tp.dx_out = c0 > 0 ? kOutF32Add : kOutF32Store;
+    tp.dx_f32 = dx_acc;
     tp.dw_out = kOutBF16;
     tp.dx_k = cw;
     tp.dw_k = tp.n;
@@ -741,6 +742,7 @@ flce_status_t run_fused(const Ctx& c, const void* X, const void* W, const LabelV
       bm.out2 = dw_bf16_map;
     } else {
       bp.dw_out = last ? kOutF32AccToBF16 : (r0 == 0 ? kOutF32Store : kOutF32Add);
+      bp.dw_f32 = last ? nullptr : c.dx_acc();
       bm.out2 = dw_acc_map;
       bm.out3 = dw_bf16_map;
     }

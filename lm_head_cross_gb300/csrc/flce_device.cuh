@@ -193,12 +193,10 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, const void*
                : "memory");
 }
 
-// Element-wise add of a shared-memory tile into global memory (performed at L2).
-__device__ __forceinline__ void tma_reduce_add_2d(const CUtensorMap* map, const void* src, int32_t c0,
-                                                  int32_t c1) {
-  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(smem_u32(src)), "r"(c0), "r"(c1)
+// Four fp32 values added to global memory at L2 (16-byte aligned address).
+__device__ __forceinline__ void red_add_v4_f32(float* dst, uint4 v) {
+  asm volatile("red.relaxed.gpu.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(__uint_as_float(v.x)),
+               "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
                : "memory");
 }
 

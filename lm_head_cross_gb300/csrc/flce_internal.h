@@ -50,8 +50,8 @@ constexpr int kTopkSplit = 16;   // most vocabulary splits of the top-k pass (bo
 
 // Output format of the dX / dW tiles of a kModeBwd launch.
 enum OutMode : int {
-  kOutF32Store = 0,      // fp32 through `out`/`out2`
-  kOutF32Add = 1,        // fp32 added at L2 through `out`/`out2`
+  kOutF32Store = 0,      // fp32 stored to dx_f32 / dw_f32
+  kOutF32Add = 1,        // fp32 added at L2 to dx_f32 / dw_f32
   kOutBF16 = 2,          // bf16 through `out`/`out2`
   kOutF32AccToBF16 = 3,  // dW only: read the fp32 accumulator through `out2`, add, write bf16 through `out3`
 };
@@ -80,6 +80,8 @@ struct TcParams {
   int h_tiles;          // ceil(h / kBN)
   int dw_m_tiles;       // ceil(cw / kPairRows)
   int dx_out, dw_out;   // OutMode of the dX and dW tiles
+  float* dx_f32;        // bwd: the fp32 dX accumulator [n, h] for kOutF32Store / kOutF32Add dX tiles (else null)
+  float* dw_f32;        // bwd: the fp32 dW accumulator [v, h] for kOutF32Store / kOutF32Add dW tiles (else null)
   int dx_k, dw_k;       // K extents: dX tiles run over dx_k vocabulary ids, dW tiles over dw_k rows
   int dx_first;         // 1: dX tiles are listed first (they are the long ones)
   int* tile_counter;    // bwd: global tile counter, zero at launch

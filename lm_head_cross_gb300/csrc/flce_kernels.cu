@@ -403,11 +403,10 @@ __device__ __forceinline__ void stage_rows(uint8_t* buf, int lane, const uint32_
     *reinterpret_cast<uint4*>(row + ((c ^ (lane & 7)) << 4)) = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
 }
 
-// Stage 32 rows x 128 B and hand them to TMA (store or reduce-add); two
-// alternating buffers per warp so the next tile overlaps the previous copy.
+// Stage 32 rows x 128 B and hand them to a TMA store; two alternating buffers
+// per warp so the next tile overlaps the previous copy.
 __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t* stg, int& sbuf, int lane,
-                                                const uint32_t (&w)[32], int x, int y, bool reduce,
-                                                int* status) {
+                                                const uint32_t (&w)[32], int x, int y, int* status) {
   if (!tma_x_ok(x, 4, status) || !in_bounds(y, INT32_MAX, status)) return;  // (y >= 0: no store starts above the tensor)
   uint8_t* buf = stg + sbuf * kStagingBuf;
   if (lane == 0) bulk_wait_group_read<1>();
@@ -416,10 +415,7 @@ __device__ __forceinline__ void stage_and_store(const CUtensorMap* map, uint8_t*
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
-    if (reduce)
-      tma_reduce_add_2d(map, buf, x, y);
-    else
-      tma_store_2d(map, buf, x, y);
+    tma_store_2d(map, buf, x, y);
     bulk_commit_group();
   }
   sbuf ^= 1;
@@ -737,7 +733,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           const int nv = p.v - col0;
           uint32_t w[32];
           sum += exp_pack_group(v, w, nv, ref);
-          stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false, p.status);
+          stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, p.status);
         }
         const bool over = !(sum <= kRefSumMax);  // also true for a non-finite sum
         if (__any_sync(0xffffffffu, over)) {
@@ -772,7 +768,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
             uint32_t w[32];
             const float gs = exp_pack_group(v, w, p.v - col0, ref);
             if (over) sum += gs;
-            stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, false, p.status);
+            stage_and_store(&maps.out, stg, sbuf, lane, w, col0, t.m0 + quarter * 32, p.status);
           }
         }
         release_accumulator(&tempty[acc], lane);
@@ -829,7 +825,7 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           w[j] = pack_bf16x2(a, b);
         }
         // columns at or beyond the chunk width fall outside the store box's tensor and are dropped by TMA
-        stage_and_store(&maps.out, stg, sbuf, lane, w, t.n0 + g * 64, t.m0 + quarter * 32, false, p.status);
+        stage_and_store(&maps.out, stg, sbuf, lane, w, t.n0 + g * 64, t.m0 + quarter * 32, p.status);
       }
       release_accumulator(&tempty[acc], lane);
     } else {
@@ -902,9 +898,19 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
 #pragma unroll
           for (int j = 0; j < 32; ++j)
             w[j] = pack_bf16x2(__uint_as_float(v[2 * j]) * osc, __uint_as_float(v[2 * j + 1]) * osc);
-          stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, false, p.status);
+          stage_and_store(omap, stg, sbuf, lane, w, t.n0 + g * 64, y0, p.status);
         }
       } else {
+        // fp32 accumulator (the bounded path's dX, the row-chunk path's dW before its last
+        // chunk): the staged rows are read back four rows per warp instruction and stored /
+        // added at L2 with 16-byte accesses from the epilogue warps, which keeps this
+        // traffic (a tile's 128 KiB per CTA, every 64 K steps for the bounded path's dX
+        // tiles) off the TMA unit that feeds the operand stages
+        float* const fbase = is_dx ? p.dx_f32 : p.dw_f32;
+        const int frows = fbase ? (is_dx ? p.n : p.v) : 0;  // no address: nothing written, error recorded
+        if (!fbase && lane == 0) atomicCAS(p.status, 0, kErrBounds);
+        if (lane == 0) bulk_wait_group_read<0>();  // earlier TMA stores are done with the staging buffers
+        __syncwarp();
 #pragma unroll 1
         for (int c = 0; c < kBN / 32; ++c) {
           if (t.n0 + c * 32 >= p.h) break;
@@ -913,7 +919,23 @@ __device__ void run_epilogue(const TcMaps& maps, const TcParams& p, const Pair& 
           tmem_ld_32x32(tbase + c * 32, v);
 #pragma unroll
           for (int j = 0; j < 32; ++j) v[j] = __float_as_uint(__uint_as_float(v[j]) * osc);
-          stage_and_store(omap, stg, sbuf, lane, v, t.n0 + c * 32, y0, omode == kOutF32Add, p.status);
+          stage_rows(stg, lane, v);
+          __syncwarp();
+          const int x = t.n0 + c * 32 + (lane & 7) * 4;  // h is a multiple of 8: x < h means x + 4 <= h
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            const int rr = q * 4 + (lane >> 3);
+            const int yy = y0 + rr;
+            const uint4 val = *reinterpret_cast<const uint4*>(stg + rr * 128 + (((lane & 7) ^ (rr & 7)) << 4));
+            const int64_t at = static_cast<int64_t>(yy) * p.h + x;
+            if (yy < frows && x < p.h && in_bounds(at + 3, static_cast<int64_t>(frows) * p.h, p.status)) {
+              if (omode == kOutF32Add)
+                red_add_v4_f32(fbase + at, val);
+              else
+                *reinterpret_cast<uint4*>(fbase + at) = val;
+            }
+          }
+          __syncwarp();  // every lane has read the staged rows before the next group rewrites them
         }
       }
       release_accumulator(&tempty[acc], lane);
